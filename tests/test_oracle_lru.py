@@ -1,0 +1,134 @@
+"""Pins for the oracle's LRU batch rule against a textbook LRU (an ordered map,
+least recent first) that handles one forward call's experts as a batch: every
+member is pinned while the batch is served, the misses are filled in ascending
+expert id from free slots (lowest index first) and then by evicting the least
+recently used unpinned entry, and finally every member is refreshed in
+ascending id. (Without the pinning a plain one-touch-at-a-time LRU can evict a
+member that a later touch of the same call needs; the layer needs all of its
+experts resident at once, so the cache pins them.)"""
+import itertools
+from collections import OrderedDict
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+class TextbookLRU:
+    def __init__(self, S):
+        self.S = S
+        self.order = OrderedDict()   # key -> slot, least recent first
+        self.free = list(range(S))
+
+    def batch(self, keys, pinned=()):
+        pin = set(keys) | set(pinned)
+        res = {}
+        for key in keys:
+            if key in self.order:
+                res[key] = (1, self.order[key], -1)
+                continue
+            if self.free:
+                slot = self.free.pop(0)
+                ev = -1
+            else:
+                ev = next(k for k in self.order if k not in pin)
+                slot = self.order.pop(ev)
+            self.order[key] = slot
+            res[key] = (0, slot, ev)
+        for key in keys:
+            self.order.move_to_end(key)
+        return [res[k] for k in keys]
+
+    def touch(self, key):
+        return self.batch([key])[0]
+
+
+def _run_both(L, E, S, trace):
+    """trace: list of (layer, sorted members)."""
+    o = oracle.LRU(L, E, S)
+    t = TextbookLRU(S)
+    for layer, members in trace:
+        ev = o.batch(layer, np.array(members, np.int32))
+        ref = t.batch([layer * E + e for e in members])
+        for p, e in enumerate(members):
+            hit, slot, evicted = ref[p]
+            assert ev["expert"][p] == e
+            assert ev["hit"][p] == hit
+            assert ev["slot"][p] == slot
+            assert ev["evicted"][p] == evicted
+    return o, t
+
+
+@pytest.mark.parametrize("S", [2, 3])
+def test_exhaustive_short_traces(S):
+    keys = range(4)
+    # every trace of up to 6 batches of one key, plus batches of pairs
+    for n in range(1, 7):
+        for tr in itertools.product(keys, repeat=n):
+            _run_both(1, 4, S, [(0, [k]) for k in tr])
+    pairs = [list(c) for c in itertools.combinations(keys, 2)]
+    for tr in itertools.product(range(len(pairs)), repeat=4):
+        _run_both(1, 4, S, [(0, pairs[i]) for i in tr])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_traces_multi_layer(seed):
+    rng = np.random.default_rng(seed)
+    L, E, S = 3, 16, 11
+    trace = []
+    for _ in range(60):
+        layer = int(rng.integers(L))
+        m = sorted(rng.choice(E, size=int(rng.integers(1, 6)), replace=False).tolist())
+        trace.append((layer, m))
+    _run_both(L, E, S, trace)
+
+
+def test_capacity_error():
+    o = oracle.LRU(1, 8, 3)
+    with pytest.raises(oracle.LRU.CapacityError):
+        o.batch(0, np.array([0, 1, 2, 3], np.int32))
+
+
+def test_prefetch_protects_current_layer_and_fills_next():
+    L, E, S = 3, 4, 10
+    o = oracle.LRU(L, E, S)
+    ev = o.access(0, np.array([1, 3], np.int32), T=16, prefetch=True)
+    assert list(ev["prefetch"]) == [0, 0, 1, 1, 1, 1]
+    assert np.all(o.table[E:2 * E] >= 0)                 # layer 1 fully resident
+    # next call on layer 1 hits everything it touches
+    ev = o.access(1, np.array([0, 2], np.int32), T=16, prefetch=True)
+    assert list(ev["hit"][:2]) == [1, 1]
+    # layer 0's experts were protected while layer 1 was prefetched
+    o2 = oracle.LRU(L, E, 6)       # S = |U| + E exactly
+    o2.access(0, np.array([0, 1], np.int32), T=16, prefetch=True)
+    assert o2.table[0] >= 0 and o2.table[1] >= 0
+    assert np.all(o2.table[E:2 * E] >= 0)
+
+
+def test_no_prefetch_for_decode_or_when_short_of_room():
+    o = oracle.LRU(2, 4, 5)
+    ev = o.access(0, np.array([0, 1], np.int32), T=8, prefetch=True)
+    assert len(ev["expert"]) == 2
+    ev = o.access(0, np.array([0, 1], np.int32), T=9, prefetch=True)   # 5 < 2 + 4
+    assert len(ev["expert"]) == 2
+
+
+def test_lru_with_prefetch_equals_textbook():
+    # a prefetch batch is a textbook batch over the next layer's E keys with the
+    # current layer's experts pinned as well
+    L, E, S = 4, 6, 14
+    rng = np.random.default_rng(5)
+    o = oracle.LRU(L, E, S)
+    t = TextbookLRU(S)
+    for step in range(30):
+        layer = step % L
+        u = sorted(rng.choice(E, size=int(rng.integers(1, 5)), replace=False).tolist())
+        ev = o.access(layer, np.array(u, np.int32), T=32, prefetch=True)
+        own = [layer * E + e for e in u]
+        ref = t.batch(own)
+        if layer + 1 < L and S >= len(u) + E:
+            ref += t.batch([(layer + 1) * E + e for e in range(E)], pinned=own)
+        assert len(ev["expert"]) == len(ref)
+        for i, r in enumerate(ref):
+            assert (ev["hit"][i], ev["slot"][i], ev["evicted"][i]) == r
