@@ -1,0 +1,562 @@
+// Expert FFNs of the routed MoE layer: SwiGLU gate/up projection, down
+// projection and the gate-weighted combine, over the active experts that the
+// router and cache kernels listed (routed experts in ascending id, then the
+// always-on shared experts).
+//
+// Hits of the cache "run on the GPU" (freetoken.wiki architecture page, decode
+// paragraph); the expert weights come in the formats the FreeToken pages list
+// (bhrtaym-blog post, section on supported models and quantisation formats:
+// MXFP4, NVFP4, BF16).
+//
+// MMA kernels use mma.sync m16n8k16 in swap-AB form: the weight rows are the
+// M = 16 operand, the tokens routed to the expert are the N = 8 columns. FP4
+// codes are widened to f16 in registers (exact) and multiplied by their block
+// scale after each 16-element MMA step, in fp32; activations are fed as f16
+// (FP4 weights) or bf16 (BF16 weights). The per-tensor NVFP4 scale multiplies
+// the finished dot product.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// --------------------------------------------------------------------------
+// register-level helpers
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                        const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                         const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+// four bytes of packed E2M1 pairs -> four f16x2 (low nibble -> low half)
+__device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// eight E4M3 bytes -> eight floats (byte i -> o[i])
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 v, float (&o)[8]) {
+    uint32_t h[4];
+    asm("{\n.reg .b16 l0, h0, l1, h1;\n"
+        "mov.b32 {l0, h0}, %4;\n"
+        "mov.b32 {l1, h1}, %5;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, l0;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, h0;\n"
+        "cvt.rn.f16x2.e4m3x2 %2, l1;\n"
+        "cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(v.x), "r"(v.y));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 x = *reinterpret_cast<__half2*>(&h[i]);
+        o[2 * i] = __low2float(x);
+        o[2 * i + 1] = __high2float(x);
+    }
+}
+
+// E8M0 byte -> 2^(b-127) as a float (b = 0 gives 2^-127)
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    return __uint_as_float(b == 0 ? 0x00400000u : (b << 23));
+}
+
+// per-step block scales of one row for one 128-element group
+template <int FMT>
+__device__ __forceinline__ void load_step_scales(const uint8_t* sc_row, int j, float mul, float (&s)[8]) {
+    if constexpr (FMT == FMT_NVFP4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(sc_row + 8 * j);
+        e4m3x8_to_f32(v, s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[i] *= mul;
+    } else if constexpr (FMT == FMT_MXFP4) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(sc_row + 4 * j);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float f = e8m0_to_f32((v >> (8 * b)) & 0xFFu) * mul;
+            s[2 * b] = f;
+            s[2 * b + 1] = f;
+        }
+    }
+}
+
+// A operand words of one row for one group: FP4 -> 4 words (16 B); BF16 -> 16 words (64 B)
+template <int FMT>
+struct RowWords {
+    static constexpr int N = FMT == FMT_BF16 ? 16 : 4;
+    uint32_t w[N];
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_row(const uint8_t* row, int j, int q, RowWords<FMT>& r) {
+    if constexpr (FMT == FMT_BF16) {
+        const uint4* p = reinterpret_cast<const uint4*>(row + (static_cast<size_t>(j) * 128 + 32 * q) * 2);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 x = __ldg(p + v);
+            r.w[4 * v] = x.x; r.w[4 * v + 1] = x.y; r.w[4 * v + 2] = x.z; r.w[4 * v + 3] = x.w;
+        }
+    } else {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(j) * 64 + 16 * q));
+        r.w[0] = x.x; r.w[1] = x.y; r.w[2] = x.z; r.w[3] = x.w;
+    }
+}
+
+// A operand words of one row for all 8 MMA steps of a group: A[s][lo] holds
+// elements +0,+1 and A[s][hi] elements +2,+3 of the row's share of step s
+template <int FMT>
+__device__ __forceinline__ void row_to_a(const RowWords<FMT>& r, uint32_t (&A)[8][4], int lo, int hi) {
+    if constexpr (FMT == FMT_BF16) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            A[s][lo] = r.w[2 * s];
+            A[s][hi] = r.w[2 * s + 1];
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t o[4];
+            fp4x8_to_f16x2(r.w[w], o);
+            A[2 * w][lo] = o[0];
+            A[2 * w][hi] = o[1];
+            A[2 * w + 1][lo] = o[2];
+            A[2 * w + 1][hi] = o[3];
+        }
+    }
+}
+
+// 64-byte B run (32 activations of one column for one group) -> 16 words; zeros if p is null
+__device__ __forceinline__ void load_b(const uint16_t* p, uint32_t (&b)[16]) {
+    if (p) {
+        const uint4* v4 = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 x = v4[v];
+            b[4 * v] = x.x; b[4 * v + 1] = x.y; b[4 * v + 2] = x.z; b[4 * v + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i] = 0u;
+    }
+}
+
+// position of intermediate unit i in device K-order
+__device__ __forceinline__ int dpos(int i) {
+    const int w = i & 127, s = w >> 4, q = (w >> 2) & 3, e = w & 3;
+    return (i & ~127) + 32 * q + 4 * s + e;
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// one group (8 MMA steps) of a 16-row x (8 * NC)-column tile; rows ra (M rows
+// 0-7) and rb (M rows 8-15); bptr[c] = this lane's B run of column tile c
+template <int FMT, int NC>
+__device__ __forceinline__ void mma_group(const RowWords<FMT>& ra, const RowWords<FMT>& rb, const float (&sa)[8],
+                                          const float (&sb)[8], const uint16_t* const (&bptr)[NC], int ncols,
+                                          float (&acc)[NC][4]) {
+    uint32_t A[8][4];
+    row_to_a<FMT>(ra, A, 0, 2);
+    row_to_a<FMT>(rb, A, 1, 3);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        if (c < ncols) {
+            uint32_t bw[16];
+            load_b(bptr[c], bw);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                if constexpr (FMT == FMT_BF16) {
+                    mma_bf16(acc[c], A[s], bw[2 * s], bw[2 * s + 1], acc[c]);
+                } else {
+                    float d[4];
+                    const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_f16(d, A[s], bw[2 * s], bw[2 * s + 1], z);
+                    acc[c][0] = __fmaf_rn(sa[s], d[0], acc[c][0]);
+                    acc[c][1] = __fmaf_rn(sa[s], d[1], acc[c][1]);
+                    acc[c][2] = __fmaf_rn(sb[s], d[2], acc[c][2]);
+                    acc[c][3] = __fmaf_rn(sb[s], d[3], acc[c][3]);
+                }
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// gate/up + SwiGLU: h[r, i] = gate_r * act(W_gate x_t)_i * (W_up x_t)_i
+// grid (I/8 unit tiles, max active experts), 4 warps split K = H by group
+// --------------------------------------------------------------------------
+
+template <int FMT, int NC>
+__global__ void __launch_bounds__(128) k_gu(CallArgs a) {
+    const int u = blockIdx.y;
+    if (u >= *a.n_active) return;
+    __shared__ float red[4][NC][32][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int H = a.H, I = a.I, G = H / kGroupK;
+    const uint8_t* blob = a.act_ptr[u];
+    const int row0 = a.act_row0[u], cnt = a.act_cnt[u];
+    const int i0 = blockIdx.x * 8;
+    const int rg = (i0 / 64) * 128 + (i0 % 64) + g;  // device gu row of gate unit i0+g
+    const int ru = rg + 64;                           // and of its up unit
+    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(H) * 2 : static_cast<size_t>(H) / 2;
+    const uint8_t* row_g = blob + a.lay.gu + rg * rowbytes;
+    const uint8_t* row_u = blob + a.lay.gu + ru * rowbytes;
+    const int sc_per_row = FMT == FMT_NVFP4 ? H / 16 : H / 32;
+    const uint8_t* sc_g = blob + a.lay.gus + static_cast<size_t>(rg) * sc_per_row;
+    const uint8_t* sc_u = blob + a.lay.gus + static_cast<size_t>(ru) * sc_per_row;
+    float gs_gate = 1.0f, gs_up = 1.0f;
+    if constexpr (FMT == FMT_NVFP4) {
+        const float* gsc = reinterpret_cast<const float*>(blob + a.lay.gsc);
+        gs_gate = gsc[0];
+        gs_up = gsc[1];
+    }
+    const uint16_t* xh = reinterpret_cast<const uint16_t*>(a.xh);
+    for (int cb = 0; cb < cnt; cb += 8 * NC) {
+        const int ncols = min(NC, (cnt - cb + 7) / 8);
+        float acc[NC][4];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
+        int tok[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int n = cb + 8 * c + g;
+            tok[c] = n < cnt ? a.row_tok[row0 + n] : -1;
+        }
+        for (int j = warp; j < G; j += 4) {
+            RowWords<FMT> ra, rb;
+            load_row<FMT>(row_g, j, q, ra);
+            load_row<FMT>(row_u, j, q, rb);
+            float sa[8], sb[8];
+            load_step_scales<FMT>(sc_g, j, 1.0f, sa);
+            load_step_scales<FMT>(sc_u, j, 1.0f, sb);
+            const uint16_t* bp[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+                bp[c] = tok[c] >= 0 ? xh + static_cast<size_t>(tok[c]) * H + j * 128 + 32 * q : nullptr;
+            mma_group<FMT, NC>(ra, rb, sa, sb, bp, ncols, acc);
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp][c][lane][i] = acc[c][i];
+        __syncthreads();
+        // epilogue: warp w finishes column tiles c = w, w+4, ...
+        for (int c = warp; c < ncols; c += 4) {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = ((red[0][c][lane][i] + red[1][c][lane][i]) + red[2][c][lane][i]) + red[3][c][lane][i];
+            const int unit = i0 + g;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = cb + 8 * c + 2 * q + h;
+                if (n < cnt) {
+                    const int r = row0 + n;
+                    const float gate = v[h] * gs_gate, up = v[2 + h] * gs_up;
+                    const float act = a.mode == 1 ? gate : silu(gate);
+                    const float hv = act * up * a.row_gate[r];
+                    const size_t o = static_cast<size_t>(r) * I + dpos(unit);
+                    if constexpr (FMT == FMT_BF16) reinterpret_cast<__nv_bfloat16*>(a.hbuf)[o] = __float2bfloat16_rn(hv);
+                    else reinterpret_cast<__half*>(a.hbuf)[o] = __float2half_rn(hv);
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// --------------------------------------------------------------------------
+// decode down projection + combine: out[t, r] = sum over active experts u of
+// (W_down,u h_{u,t})[r]; the gate is already folded into h. The token index is
+// the MMA column, so all experts accumulate into one tile.
+// grid (H/16 row tiles), 4 warps split K = I by group
+// --------------------------------------------------------------------------
+
+template <int FMT, int ACT>
+__global__ void __launch_bounds__(128) k_down_dec(CallArgs a) {
+    __shared__ float red[4][32][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int H = a.H, I = a.I, T = a.T, GI = I / kGroupK;
+    const int r0 = blockIdx.x * 16 + g;
+    const int na = *a.n_active;
+    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
+    const int sc_per_row = FMT == FMT_NVFP4 ? I / 16 : I / 32;
+    const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    for (int u = 0; u < na; ++u) {
+        const uint8_t* blob = a.act_ptr[u];
+        const int hr = g < T ? a.tok_row[u * kDecodeMaxT + g] : -1;
+        float gsd = 1.0f;
+        if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
+        const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
+        const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
+        const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * sc_per_row;
+        const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * sc_per_row;
+        for (int j = warp; j < GI; j += 4) {
+            RowWords<FMT> ra, rb;
+            load_row<FMT>(rowa, j, q, ra);
+            load_row<FMT>(rowb, j, q, rb);
+            float sa[8], sb[8];
+            load_step_scales<FMT>(sca, j, gsd, sa);
+            load_step_scales<FMT>(scb, j, gsd, sb);
+            const uint16_t* bp[1] = {hr >= 0 ? hb + static_cast<size_t>(hr) * I + j * 128 + 32 * q : nullptr};
+            mma_group<FMT, 1>(ra, rb, sa, sb, bp, 1, acc);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[warp][lane][i] = acc[0][i];
+    __syncthreads();
+    if (warp == 0) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ((red[0][lane][i] + red[1][lane][i]) + red[2][lane][i]) + red[3][lane][i];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = 2 * q + h;
+            if (t < T) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const size_t o = static_cast<size_t>(t) * H + r0 + 8 * rr;
+                    const float x = v[2 * rr + h];
+                    if constexpr (ACT == ACT_BF16) reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(x);
+                    else reinterpret_cast<float*>(a.out)[o] = x;
+                }
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// prefill down projection: Y[r, :] = W_down,u h_r for every row r of expert u
+// grid (H/16 row tiles, max active experts)
+// --------------------------------------------------------------------------
+
+template <int FMT, int NC>
+__global__ void __launch_bounds__(128) k_down_rows(CallArgs a) {
+    const int u = blockIdx.y;
+    if (u >= *a.n_active) return;
+    __shared__ float red[4][NC][32][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int H = a.H, I = a.I, GI = I / kGroupK;
+    const uint8_t* blob = a.act_ptr[u];
+    const int row0 = a.act_row0[u], cnt = a.act_cnt[u];
+    const int r0 = blockIdx.x * 16 + g;
+    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
+    const int sc_per_row = FMT == FMT_NVFP4 ? I / 16 : I / 32;
+    float gsd = 1.0f;
+    if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
+    const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
+    const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
+    const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * sc_per_row;
+    const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * sc_per_row;
+    const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
+    __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(a.ybuf);
+    for (int cb = 0; cb < cnt; cb += 8 * NC) {
+        const int ncols = min(NC, (cnt - cb + 7) / 8);
+        float acc[NC][4];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
+        for (int j = warp; j < GI; j += 4) {
+            RowWords<FMT> ra, rb;
+            load_row<FMT>(rowa, j, q, ra);
+            load_row<FMT>(rowb, j, q, rb);
+            float sa[8], sb[8];
+            load_step_scales<FMT>(sca, j, gsd, sa);
+            load_step_scales<FMT>(scb, j, gsd, sb);
+            const uint16_t* bp[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const int n = cb + 8 * c + g;
+                bp[c] = n < cnt ? hb + static_cast<size_t>(row0 + n) * I + j * 128 + 32 * q : nullptr;
+            }
+            mma_group<FMT, NC>(ra, rb, sa, sb, bp, ncols, acc);
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp][c][lane][i] = acc[c][i];
+        __syncthreads();
+        for (int c = warp; c < ncols; c += 4) {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = ((red[0][c][lane][i] + red[1][c][lane][i]) + red[2][c][lane][i]) + red[3][c][lane][i];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = cb + 8 * c + 2 * q + h;
+                if (n < cnt) {
+                    const size_t o = static_cast<size_t>(row0 + n) * H;
+                    Y[o + r0] = __float2bfloat16_rn(v[h]);
+                    Y[o + r0 + 8] = __float2bfloat16_rn(v[2 + h]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// out[t, :] = sum_j Y[inv_perm[t*k + j], :] (j ascending) + sum_s Y[shared row of t]
+template <int ACT>
+__global__ void __launch_bounds__(256) k_combine(CallArgs a) {
+    const int H = a.H, T = a.T, k = a.k;
+    const size_t n8 = static_cast<size_t>(T) * H / 8;
+    const __nv_bfloat16* Y = reinterpret_cast<const __nv_bfloat16*>(a.ybuf);
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n8;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx / (H / 8));
+        const int c = 8 * static_cast<int>(idx % (H / 8));
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const int nrows = k + a.n_shared;
+        for (int j = 0; j < nrows; ++j) {
+            const int r = j < k ? a.inv_perm[t * k + j] : T * k + (j - k) * T + t;
+            const uint4 v = *reinterpret_cast<const uint4*>(Y + static_cast<size_t>(r) * H + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[2 * i] += __uint_as_float(w[i] << 16);
+                s[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+        if constexpr (ACT == ACT_BF16) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(s[2 * i], s[2 * i + 1]);
+                o[i] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * H + c) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            float* o = reinterpret_cast<float*>(a.out) + static_cast<size_t>(t) * H + c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = s[i];
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// FP32 weights: plain SIMT kernels (small shapes)
+// --------------------------------------------------------------------------
+
+template <int ACT>
+__device__ __forceinline__ float ldx(const void* p, size_t i) {
+    if constexpr (ACT == ACT_BF16)
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[i]) << 16);
+    else
+        return reinterpret_cast<const float*>(p)[i];
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(256) k_gu_f32(CallArgs a) {
+    const int u = blockIdx.y;
+    if (u >= *a.n_active) return;
+    const int H = a.H, I = a.I;
+    const float* Wg = reinterpret_cast<const float*>(a.act_ptr[u] + a.lay.gu);
+    const float* Wu = Wg + static_cast<size_t>(I) * H;
+    const int row0 = a.act_row0[u], cnt = a.act_cnt[u];
+    float* hb = reinterpret_cast<float*>(a.hbuf);
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < cnt * I; idx += gridDim.x * blockDim.x) {
+        const int n = idx / I, i = idx % I, r = row0 + n, t = a.row_tok[r];
+        float gs = 0.f, us = 0.f;
+        for (int h = 0; h < H; ++h) {
+            const float x = ldx<ACT>(a.hidden, static_cast<size_t>(t) * H + h);
+            gs = __fadd_rn(gs, __fmul_rn(Wg[static_cast<size_t>(i) * H + h], x));
+            us = __fadd_rn(us, __fmul_rn(Wu[static_cast<size_t>(i) * H + h], x));
+        }
+        const float act = a.mode == 1 ? gs : gs / (1.0f + expf(-gs));
+        hb[static_cast<size_t>(r) * I + i] = act * us * a.row_gate[r];
+    }
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(256) k_down_f32(CallArgs a) {
+    const int H = a.H, I = a.I, T = a.T, k = a.k;
+    const float* hb = reinterpret_cast<const float*>(a.hbuf);
+    const int nu = *a.n_uniq;
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < T * H; idx += gridDim.x * blockDim.x) {
+        const int t = idx / H, c = idx % H;
+        float acc = 0.f;
+        for (int j = 0; j < k + a.n_shared; ++j) {
+            int r, u;
+            if (j < k) {
+                r = a.inv_perm[t * k + j];
+                u = a.e2u[a.topk[t * k + j]];
+            } else {
+                r = T * k + (j - k) * T + t;
+                u = nu + (j - k);
+            }
+            const float* Wd = reinterpret_cast<const float*>(a.act_ptr[u] + a.lay.d);
+            float y = 0.f;
+            for (int i = 0; i < I; ++i)
+                y = __fadd_rn(y, __fmul_rn(Wd[static_cast<size_t>(c) * I + i], hb[static_cast<size_t>(r) * I + i]));
+            acc = __fadd_rn(acc, y);
+        }
+        if constexpr (ACT == ACT_BF16) reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(acc);
+        else reinterpret_cast<float*>(a.out)[idx] = acc;
+    }
+}
+
+// --------------------------------------------------------------------------
+
+template <int FMT, int ACT>
+static void launch_mma_path(const CallArgs& a, cudaStream_t s) {
+    const int max_active = min(a.E, a.T * a.k) + a.n_shared;
+    if (a.T <= kDecodeMaxT) {
+        k_gu<FMT, 1><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
+        k_down_dec<FMT, ACT><<<a.H / 16, 128, 0, s>>>(a);
+    } else {
+        k_gu<FMT, 8><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
+        k_down_rows<FMT, 8><<<dim3(a.H / 16, max_active), 128, 0, s>>>(a);
+        const size_t n8 = static_cast<size_t>(a.T) * a.H / 8;
+        const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 148 * 16));
+        k_combine<ACT><<<blocks, 256, 0, s>>>(a);
+    }
+}
+
+cudaError_t launch_experts(const CallArgs& a, cudaStream_t s) {
+    if (a.fmt == FMT_FP32) {
+        const int max_active = min(a.E, a.T * a.k) + a.n_shared;
+        const int gx = min((a.T * a.I + 255) / 256, 64);
+        const int gd = min((a.T * a.H + 255) / 256, 148 * 8);
+        if (a.act == ACT_BF16) {
+            k_gu_f32<ACT_BF16><<<dim3(gx, max_active), 256, 0, s>>>(a);
+            k_down_f32<ACT_BF16><<<gd, 256, 0, s>>>(a);
+        } else {
+            k_gu_f32<ACT_FP32><<<dim3(gx, max_active), 256, 0, s>>>(a);
+            k_down_f32<ACT_FP32><<<gd, 256, 0, s>>>(a);
+        }
+        return cudaGetLastError();
+    }
+    const bool bf = a.act == ACT_BF16;
+    switch (a.fmt) {
+        case FMT_BF16: bf ? launch_mma_path<FMT_BF16, ACT_BF16>(a, s) : launch_mma_path<FMT_BF16, ACT_FP32>(a, s); break;
+        case FMT_NVFP4: bf ? launch_mma_path<FMT_NVFP4, ACT_BF16>(a, s) : launch_mma_path<FMT_NVFP4, ACT_FP32>(a, s); break;
+        case FMT_MXFP4: bf ? launch_mma_path<FMT_MXFP4, ACT_BF16>(a, s) : launch_mma_path<FMT_MXFP4, ACT_FP32>(a, s); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,106 @@
+// Internal definitions shared by the host runtime and the CUDA kernels of the
+// routed MoE layer (not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kDecodeMaxT = 8;     // T <= 8 takes the decode path
+constexpr int kMaxExperts = 1024;  // E limit (router keeps E/32 logits per lane)
+constexpr int kMaxTopK = 32;
+constexpr int kGroupK = 128;       // K elements per device-order group
+constexpr int kMaxSlots = 16384;   // pool slots (slot index fits 14 bits)
+constexpr int kSortMax = 16384;    // bitonic sort size bound for victim selection
+
+enum Fmt { FMT_FP32 = 0, FMT_BF16 = 1, FMT_NVFP4 = 2, FMT_MXFP4 = 3 };
+enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
+
+// Device layout of one expert ("blob"), identical in the pinned host bank and
+// in a pool slot, so that a miss is one contiguous copy.
+//   gu  : gate/up rows [2I][H]. Rows come in blocks of 128: 64 gate rows then
+//         the 64 up rows of the same intermediate units (FP32: plain [gate I][up I]).
+//   d   : down rows [H][I].
+//   gus, ds: per-row block scales of gu and d (FP4 formats), canonical order.
+//   gsc : float[4] per-tensor scales (gate, up, down, 1) — NVFP4; else 1.
+// Within every row, K is stored in "device order" (FP32 excepted): each group
+// of 128 consecutive elements is reordered so that position 32q + 4s + i holds
+// element 16s + 4q + i of the group (q < 4, s < 8, i < 4). A warp lane with
+// quad index q then finds, in one contiguous 16-byte (FP4) or 64-byte (BF16)
+// run, its operands for the eight m16n8k16 MMA steps s of the group, and step s
+// covers exactly one 16-element NVFP4 scale block (half of an MXFP4 block).
+// Activations fed to the same MMAs are stored in the same order.
+struct BlobLayout {
+    size_t gu, d, gus, ds, gsc, bytes;
+};
+
+// Written by the cache kernel into mapped host memory; read by the host after
+// the cache kernel completes.
+struct CallInfo {
+    int32_t status;          // 0 ok, else a negative moe_status
+    int32_t n_uniq;
+    int32_t n_hit, n_miss;   // demand batch
+    int32_t n_pf, n_pf_hit, n_pf_miss;  // prefetch batch (n_pf = 0: none)
+    int32_t n_events;
+    // misses to copy: demand misses first, then prefetch misses
+    int32_t miss_layer[2 * kMaxExperts];
+    int32_t miss_expert[2 * kMaxExperts];
+    int32_t miss_slot[2 * kMaxExperts];
+    // event log of both batches in service order
+    int32_t ev_layer[2 * kMaxExperts];
+    int32_t ev_expert[2 * kMaxExperts];
+    int32_t ev_hit[2 * kMaxExperts];
+    int32_t ev_slot[2 * kMaxExperts];
+    int32_t ev_evicted[2 * kMaxExperts];
+    int32_t ev_prefetch[2 * kMaxExperts];
+};
+
+struct CallArgs {
+    // shape
+    int T, E, k, H, I, n_shared, L, layer, S;
+    int fmt, act, mode;
+    int prefetch, log_events;
+    // caller buffers (device)
+    const void* hidden;    // [T][H] act
+    const void* router_w;  // [E][H] act
+    void* out;             // [T][H] act
+    // scratch (device)
+    void* xh;              // [T][H] f16 (FP4) or bf16 (BF16), device K-order
+    float* logits;         // [T][E]
+    int32_t* topk;         // [T*k]
+    float* gates;          // [T*k]
+    int32_t* counts;       // [E]
+    int32_t* offsets;      // [E+1]
+    int32_t* perm;         // [T*k]
+    int32_t* inv_perm;     // [T*k]
+    int32_t* row_tok;      // [T*k + T*n_shared]
+    float* row_gate;       // [T*k + T*n_shared]
+    int32_t* act_expert;   // [E + n_shared]  active experts: routed (ascending), then shared
+    int32_t* act_row0;     // [E + n_shared]  first h/Y row of the active expert
+    int32_t* act_cnt;      // [E + n_shared]  rows (tokens) of the active expert
+    const uint8_t** act_ptr;  // [E + n_shared] blob address
+    int32_t* e2u;          // [E] active index of routed expert e, or -1
+    int32_t* tok_row;      // [(E + n_shared) * 8] decode: h row of (active u, token t) or -1
+    int32_t* n_uniq;       // [1]
+    int32_t* n_active;     // [1]
+    void* hbuf;            // [rows][I] intermediate (f16 / bf16 / f32)
+    void* ybuf;            // [rows][H] bf16 down-projection rows (prefill)
+    // cache (device)
+    int32_t* table;        // [L*E] slot or -1
+    int32_t* owner;        // [S] key or -1
+    unsigned long long* stamp;  // [S] recency (0 = never filled)
+    unsigned long long* clock;  // [1]
+    const uint8_t* pool;   // S * blob bytes
+    const uint8_t* shared_base;  // this layer's shared experts (n_shared blobs)
+    BlobLayout lay;
+    CallInfo* info;        // mapped host memory (device pointer)
+};
+
+// launchers (kernels.cu); all enqueue on `s` and return cudaGetLastError()
+cudaError_t launch_router(const CallArgs& a, cudaStream_t s);
+cudaError_t launch_cache(const CallArgs& a, cudaStream_t s);
+cudaError_t launch_experts(const CallArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,549 @@
+// Host runtime of the routed MoE layer: the C ABI declared in include/moe.h.
+//
+// Two-tier expert memory as on "FreeToken量子化：MoE推論のセットアップガイド"
+// (freetoken.wiki, architecture page): every routed expert lives in host RAM
+// (here: library-owned pinned banks, one per layer), the GPU holds one expert
+// cache shared by all MoE layers (a pool of S slots), misses are copied over
+// PCIe, and prefill streams the next layer's experts while the current layer
+// computes. Cache resizing happens at a safe point (moe_cache_config), as the
+// same page describes for the scheduler's safe points.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+cudaError_t routing_set_attributes();
+}
+
+using moe::BlobLayout;
+using moe::CallArgs;
+using moe::CallInfo;
+
+struct moe_handle {
+    moe_model_desc d{};
+    BlobLayout lay{};
+    int max_tokens = 0;
+    // host banks: per layer, E blobs (pinned); loaded flags
+    std::vector<uint8_t*> bank;
+    std::vector<uint8_t> loaded;
+    // shared experts: device resident [L][n_shared] blobs
+    uint8_t* shared_dev = nullptr;
+    // pool and LRU state
+    uint8_t* pool = nullptr;
+    int S = 0;
+    unsigned flags = 0;
+    int32_t* table = nullptr;
+    int32_t* owner = nullptr;
+    unsigned long long* stamp = nullptr;
+    unsigned long long* clock = nullptr;
+    // scratch
+    void* scratch = nullptr;
+    CallArgs base{};
+    CallInfo* info_h = nullptr;
+    CallInfo* info_d = nullptr;
+    // streams / events
+    cudaStream_t stream = nullptr, copy = nullptr;
+    cudaEvent_t ev_cache = nullptr, ev_copy = nullptr, ev_prefetch = nullptr;
+    bool prefetch_pending = false;
+    // last call
+    int last_T = 0;
+    cudaStream_t last_stream = nullptr;
+    // stats
+    moe_stats_t st{};
+    std::vector<moe_event> events;
+    std::string err;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int fail(moe_handle* h, int code, const std::string& msg) {
+    if (h) h->err = msg;
+    return code;
+}
+
+int cuda_fail(moe_handle* h, cudaError_t e, const char* what) {
+    return fail(h, MOE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(h, x)                                          \
+    do {                                                  \
+        cudaError_t e_ = (x);                             \
+        if (e_ != cudaSuccess) return cuda_fail(h, e_, #x); \
+    } while (0)
+
+int validate_desc(const moe_model_desc* d, std::string* why) {
+    auto bad = [&](const char* m) { *why = m; return MOE_ERR_INVALID; };
+    if (!d) return bad("desc is NULL");
+    if (d->num_layers < 1) return bad("num_layers must be >= 1");
+    if (d->num_experts < 1 || d->num_experts > moe::kMaxExperts) return bad("num_experts must be in 1..1024");
+    if (d->num_shared < 0 || d->num_shared > 1) return bad("num_shared must be 0 or 1");
+    if (d->top_k < 1 || d->top_k > moe::kMaxTopK || d->top_k > d->num_experts) return bad("top_k must be in 1..min(E, 32)");
+    if (d->weight_fmt < 0 || d->weight_fmt > 3) return bad("unknown weight_fmt");
+    if (d->act_dtype < 0 || d->act_dtype > 1) return bad("unknown act_dtype");
+    if (d->act_mode < 0 || d->act_mode > 1) return bad("unknown act_mode");
+    if (d->max_tokens < 0) return bad("max_tokens must be >= 0");
+    if (d->weight_fmt == moe::FMT_FP32) {
+        if (d->hidden < 8 || d->hidden % 8) return bad("hidden must be a positive multiple of 8");
+        if (d->inter < 1) return bad("inter must be >= 1");
+    } else {
+        if (d->hidden < 128 || d->hidden % 128) return bad("hidden must be a positive multiple of 128");
+        if (d->inter < 128 || d->inter % 128) return bad("inter must be a positive multiple of 128");
+    }
+    const size_t xbytes = static_cast<size_t>(8) * d->hidden * (d->act_dtype == moe::ACT_BF16 ? 2 : 4);
+    if (xbytes > 200 * 1024) return bad("hidden too large for the router's shared-memory tile");
+    return MOE_OK;
+}
+
+BlobLayout layout_for(const moe_model_desc& d) {
+    BlobLayout L{};
+    const size_t H = d.hidden, I = d.inter;
+    size_t o = 0;
+    switch (d.weight_fmt) {
+        case moe::FMT_FP32:
+            L.gu = 0; o = 2 * I * H * 4;
+            L.d = align_up(o, 256); o = L.d + H * I * 4;
+            L.gus = L.ds = L.gsc = align_up(o, 256); o = L.gsc + 16;
+            break;
+        case moe::FMT_BF16:
+            L.gu = 0; o = 2 * I * H * 2;
+            L.d = align_up(o, 256); o = L.d + H * I * 2;
+            L.gus = L.ds = L.gsc = align_up(o, 256); o = L.gsc + 16;
+            break;
+        default: {
+            const size_t blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
+            L.gu = 0; o = 2 * I * H / 2;
+            L.d = align_up(o, 256); o = L.d + H * I / 2;
+            L.gus = align_up(o, 256); o = L.gus + 2 * I * H / blk;
+            L.ds = align_up(o, 256); o = L.ds + H * I / blk;
+            L.gsc = align_up(o, 256); o = L.gsc + 16;
+        }
+    }
+    L.bytes = align_up(o, 1024);
+    return L;
+}
+
+// device gu row of canonical gate (which = 0) / up (which = 1) row i
+inline size_t gu_row(int i, int which) { return static_cast<size_t>(i / 64) * 128 + 64 * which + (i % 64); }
+
+// one canonical row of K elements -> device K-order
+void reorder_row_fp4(const uint8_t* src, uint8_t* dst, int K) {
+    for (int j = 0; j < K / 128; ++j) {
+        const uint8_t* s = src + 64 * j;
+        uint8_t* d = dst + 64 * j;
+        for (int q = 0; q < 4; ++q)
+            for (int st = 0; st < 8; ++st) {
+                d[16 * q + 2 * st] = s[8 * st + 2 * q];
+                d[16 * q + 2 * st + 1] = s[8 * st + 2 * q + 1];
+            }
+    }
+}
+
+void reorder_row_bf16(const uint16_t* src, uint16_t* dst, int K) {
+    for (int j = 0; j < K / 128; ++j) {
+        const uint16_t* s = src + 128 * j;
+        uint16_t* d = dst + 128 * j;
+        for (int q = 0; q < 4; ++q)
+            for (int st = 0; st < 8; ++st) std::memcpy(d + 32 * q + 4 * st, s + 16 * st + 4 * q, 8);
+    }
+}
+
+// canonical expert -> device blob (host memory)
+int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert_host* w, uint8_t* blob,
+                  std::string* why) {
+    const int H = d.hidden, I = d.inter;
+    const moe_tensor_host* ts[3] = {&w->gate, &w->up, &w->down};
+    for (int i = 0; i < 3; ++i) {
+        if (!ts[i]->data) { *why = "expert tensor data is NULL"; return MOE_ERR_INVALID; }
+        if (d.weight_fmt >= moe::FMT_NVFP4 && !ts[i]->scales) { *why = "expert scales are NULL"; return MOE_ERR_INVALID; }
+    }
+    std::memset(blob, 0, L.bytes);
+    float* gsc = reinterpret_cast<float*>(blob + L.gsc);
+    gsc[0] = gsc[1] = gsc[2] = gsc[3] = 1.0f;
+    switch (d.weight_fmt) {
+        case moe::FMT_FP32: {
+            const size_t n = static_cast<size_t>(I) * H;
+            std::memcpy(blob + L.gu, w->gate.data, n * 4);
+            std::memcpy(blob + L.gu + n * 4, w->up.data, n * 4);
+            std::memcpy(blob + L.d, w->down.data, n * 4);
+            break;
+        }
+        case moe::FMT_BF16: {
+            uint16_t* gu = reinterpret_cast<uint16_t*>(blob + L.gu);
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = static_cast<const uint16_t*>(ts[which]->data);
+                for (int i = 0; i < I; ++i)
+                    reorder_row_bf16(src + static_cast<size_t>(i) * H, gu + gu_row(i, which) * H, H);
+            }
+            const uint16_t* src = static_cast<const uint16_t*>(w->down.data);
+            uint16_t* dd = reinterpret_cast<uint16_t*>(blob + L.d);
+            for (int r = 0; r < H; ++r)
+                reorder_row_bf16(src + static_cast<size_t>(r) * I, dd + static_cast<size_t>(r) * I, I);
+            break;
+        }
+        default: {
+            const int blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
+            uint8_t* gu = blob + L.gu;
+            uint8_t* gus = blob + L.gus;
+            for (int which = 0; which < 2; ++which) {
+                const uint8_t* src = static_cast<const uint8_t*>(ts[which]->data);
+                const uint8_t* sc = ts[which]->scales;
+                for (int i = 0; i < I; ++i) {
+                    const size_t dr = gu_row(i, which);
+                    reorder_row_fp4(src + static_cast<size_t>(i) * H / 2, gu + dr * H / 2, H);
+                    std::memcpy(gus + dr * (H / blk), sc + static_cast<size_t>(i) * (H / blk), H / blk);
+                }
+            }
+            const uint8_t* src = static_cast<const uint8_t*>(w->down.data);
+            for (int r = 0; r < H; ++r)
+                reorder_row_fp4(src + static_cast<size_t>(r) * I / 2, blob + L.d + static_cast<size_t>(r) * I / 2, I);
+            std::memcpy(blob + L.ds, w->down.scales, static_cast<size_t>(H) * (I / blk));
+            if (d.weight_fmt == moe::FMT_NVFP4) {
+                gsc[0] = w->gate.global_scale;
+                gsc[1] = w->up.global_scale;
+                gsc[2] = w->down.global_scale;
+            }
+        }
+    }
+    return MOE_OK;
+}
+
+void free_pool(moe_handle* h) {
+    cudaFree(h->pool); h->pool = nullptr;
+    cudaFree(h->table); h->table = nullptr;
+    cudaFree(h->owner); h->owner = nullptr;
+    cudaFree(h->stamp); h->stamp = nullptr;
+    cudaFree(h->clock); h->clock = nullptr;
+    h->S = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes) {
+    std::string why;
+    const int v = validate_desc(desc, &why);
+    if (v != MOE_OK) return v;
+    if (!bytes) return MOE_ERR_INVALID;
+    *bytes = layout_for(*desc).bytes;
+    return MOE_OK;
+}
+
+int moe_init(const moe_model_desc* desc, moe_handle** out) {
+    if (!out) return MOE_ERR_INVALID;
+    *out = nullptr;
+    std::string why;
+    int v = validate_desc(desc, &why);
+    if (v != MOE_OK) return v;
+    moe_handle* h = new (std::nothrow) moe_handle();
+    if (!h) return MOE_ERR_OOM;
+    h->d = *desc;
+    h->max_tokens = desc->max_tokens > 0 ? desc->max_tokens : 4096;
+    h->lay = layout_for(h->d);
+    auto bail = [&](int code) { moe_destroy(h); return code; };
+    cudaError_t e = cudaSetDevice(desc->device);
+    if (e != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (moe::routing_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared, k = h->d.top_k;
+    const size_t H = h->d.hidden, I = h->d.inter, Tm = h->max_tokens;
+    h->bank.assign(L, nullptr);
+    h->loaded.assign(static_cast<size_t>(L) * E, 0);
+    if (ns > 0) {
+        if (cudaMalloc(&h->shared_dev, static_cast<size_t>(L) * ns * h->lay.bytes) != cudaSuccess) return bail(MOE_ERR_OOM);
+        cudaMemset(h->shared_dev, 0, static_cast<size_t>(L) * ns * h->lay.bytes);
+    }
+    // scratch carve-up
+    const size_t rows = Tm * (k + ns);
+    const size_t hes = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
+    struct Part { size_t bytes; void** dst; };
+    CallArgs& a = h->base;
+    std::vector<Part> parts = {
+        {Tm * H * 2, &a.xh},
+        {Tm * E * 4, reinterpret_cast<void**>(&a.logits)},
+        {Tm * k * 4, reinterpret_cast<void**>(&a.topk)},
+        {Tm * k * 4, reinterpret_cast<void**>(&a.gates)},
+        {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.counts)},
+        {static_cast<size_t>(E + 1) * 4, reinterpret_cast<void**>(&a.offsets)},
+        {Tm * k * 4, reinterpret_cast<void**>(&a.perm)},
+        {Tm * k * 4, reinterpret_cast<void**>(&a.inv_perm)},
+        {rows * 4, reinterpret_cast<void**>(&a.row_tok)},
+        {rows * 4, reinterpret_cast<void**>(&a.row_gate)},
+        {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_expert)},
+        {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_row0)},
+        {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_cnt)},
+        {static_cast<size_t>(E + ns) * 8, reinterpret_cast<void**>(&a.act_ptr)},
+        {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.e2u)},
+        {static_cast<size_t>(E + ns) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.tok_row)},
+        {4, reinterpret_cast<void**>(&a.n_uniq)},
+        {4, reinterpret_cast<void**>(&a.n_active)},
+        {rows * I * hes, &a.hbuf},
+        {h->d.weight_fmt == moe::FMT_FP32 || Tm <= moe::kDecodeMaxT ? 16 : rows * H * 2, &a.ybuf},
+    };
+    size_t total = 0;
+    for (auto& p : parts) total += align_up(p.bytes, 256);
+    if (cudaMalloc(&h->scratch, total) != cudaSuccess) return bail(MOE_ERR_OOM);
+    cudaMemset(h->scratch, 0, total);
+    size_t off = 0;
+    for (auto& p : parts) {
+        *p.dst = static_cast<uint8_t*>(h->scratch) + off;
+        off += align_up(p.bytes, 256);
+    }
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->info_h), sizeof(CallInfo), cudaHostAllocMapped) != cudaSuccess)
+        return bail(MOE_ERR_OOM);
+    std::memset(h->info_h, 0, sizeof(CallInfo));
+    if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->info_d), h->info_h, 0) != cudaSuccess)
+        return bail(MOE_ERR_CUDA);
+    if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaEventCreateWithFlags(&h->ev_cache, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaEventCreateWithFlags(&h->ev_copy, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaEventCreateWithFlags(&h->ev_prefetch, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    a.E = E; a.k = k; a.H = static_cast<int>(H); a.I = static_cast<int>(I); a.n_shared = ns; a.L = L;
+    a.fmt = h->d.weight_fmt; a.act = h->d.act_dtype; a.mode = h->d.act_mode;
+    a.lay = h->lay;
+    a.info = h->info_d;
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host* w) {
+    if (!h || !w) return MOE_ERR_INVALID;
+    const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared;
+    if (layer < 0 || layer >= L) return fail(h, MOE_ERR_INVALID, "layer out of range");
+    if (expert < 0 || expert >= E + ns) return fail(h, MOE_ERR_INVALID, "expert out of range");
+    CK(h, cudaSetDevice(h->d.device));
+    const size_t B = h->lay.bytes;
+    std::string why;
+    if (expert >= E) {
+        std::vector<uint8_t> tmp(B);
+        int r = repack_expert(h->d, h->lay, w, tmp.data(), &why);
+        if (r != MOE_OK) return fail(h, r, why);
+        CK(h, cudaMemcpy(h->shared_dev + (static_cast<size_t>(layer) * ns + (expert - E)) * B, tmp.data(), B,
+                         cudaMemcpyHostToDevice));
+        return MOE_OK;
+    }
+    if (!h->bank[layer]) {
+        void* p = nullptr;
+        if (cudaHostAlloc(&p, static_cast<size_t>(E) * B, cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, MOE_ERR_OOM, "pinned host bank allocation failed");
+        }
+        h->bank[layer] = static_cast<uint8_t*>(p);
+    }
+    int r = repack_expert(h->d, h->lay, w, h->bank[layer] + static_cast<size_t>(expert) * B, &why);
+    if (r != MOE_OK) return fail(h, r, why);
+    h->loaded[static_cast<size_t>(layer) * E + expert] = 1;
+    return MOE_OK;
+}
+
+int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
+    if (!h) return MOE_ERR_INVALID;
+    if (capacity_slots < h->d.top_k) return fail(h, MOE_ERR_CAPACITY, "capacity below top_k");
+    if (capacity_slots > moe::kMaxSlots) return fail(h, MOE_ERR_INVALID, "capacity above 16384 slots");
+    CK(h, cudaSetDevice(h->d.device));
+    CK(h, cudaDeviceSynchronize());
+    free_pool(h);
+    const int L = h->d.num_layers, E = h->d.num_experts;
+    const size_t S = capacity_slots;
+    if (cudaMalloc(&h->pool, S * h->lay.bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free_pool(h);
+        return fail(h, MOE_ERR_OOM, "device pool allocation failed");
+    }
+    if (cudaMalloc(&h->table, static_cast<size_t>(L) * E * 4) != cudaSuccess ||
+        cudaMalloc(&h->owner, S * 4) != cudaSuccess || cudaMalloc(&h->stamp, S * 8) != cudaSuccess ||
+        cudaMalloc(&h->clock, 8) != cudaSuccess) {
+        cudaGetLastError();
+        free_pool(h);
+        return fail(h, MOE_ERR_OOM, "LRU table allocation failed");
+    }
+    CK(h, cudaMemset(h->table, 0xFF, static_cast<size_t>(L) * E * 4));
+    CK(h, cudaMemset(h->owner, 0xFF, S * 4));
+    CK(h, cudaMemset(h->stamp, 0, S * 8));
+    CK(h, cudaMemset(h->clock, 0, 8));
+    CK(h, cudaDeviceSynchronize());
+    h->S = capacity_slots;
+    h->flags = flags;
+    h->prefetch_pending = false;
+    CallArgs& a = h->base;
+    a.table = h->table; a.owner = h->owner; a.stamp = h->stamp; a.clock = h->clock;
+    a.pool = h->pool; a.S = h->S;
+    a.prefetch = (flags & MOE_CACHE_PREFETCH_NEXT_LAYER) ? 1 : 0;
+    a.log_events = (flags & MOE_CACHE_LOG_EVENTS) ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, int layer_id, int T, void* out,
+                      void* stream) {
+    if (!h) return MOE_ERR_INVALID;
+    if (!h->pool) return fail(h, MOE_ERR_STATE, "moe_cache_config has not been called");
+    const int L = h->d.num_layers, E = h->d.num_experts;
+    if (layer_id < 0 || layer_id >= L) return fail(h, MOE_ERR_INVALID, "layer out of range");
+    if (T < 0 || T > h->max_tokens) return fail(h, MOE_ERR_INVALID, "T out of range");
+    if (T == 0) return MOE_OK;
+    if (!hidden || !router_w || !out) return fail(h, MOE_ERR_INVALID, "NULL device buffer");
+    if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(router_w) |
+         reinterpret_cast<uintptr_t>(out)) & 15u)
+        return fail(h, MOE_ERR_INVALID, "device buffers must be 16-byte aligned");
+    for (int e = 0; e < E; ++e)
+        if (!h->loaded[static_cast<size_t>(layer_id) * E + e]) return fail(h, MOE_ERR_STATE, "layer has unloaded experts");
+    const bool decode = T <= moe::kDecodeMaxT;
+    const bool want_pf = !decode && (h->flags & MOE_CACHE_PREFETCH_NEXT_LAYER) && layer_id + 1 < L;
+    if (want_pf)
+        for (int e = 0; e < E; ++e)
+            if (!h->loaded[static_cast<size_t>(layer_id + 1) * E + e])
+                return fail(h, MOE_ERR_STATE, "next layer has unloaded experts");
+    CK(h, cudaSetDevice(h->d.device));
+    cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+    CallArgs a = h->base;
+    a.T = T;
+    a.layer = layer_id;
+    a.hidden = hidden;
+    a.router_w = router_w;
+    a.out = out;
+    a.shared_base = h->shared_dev ? h->shared_dev + static_cast<size_t>(layer_id) * h->d.num_shared * h->lay.bytes
+                                  : nullptr;
+    h->info_h->status = 1;
+    CK(h, moe::launch_router(a, s));
+    CK(h, moe::launch_cache(a, s));
+    CK(h, cudaEventRecord(h->ev_cache, s));
+    CK(h, cudaEventSynchronize(h->ev_cache));
+    volatile CallInfo* inf = h->info_h;
+    h->last_T = T;
+    h->last_stream = s;
+    if (inf->status == MOE_ERR_CAPACITY) {
+        h->st.device_errors++;
+        return fail(h, MOE_ERR_CAPACITY, "the layer's experts do not fit in the expert pool");
+    }
+    if (inf->status != 0) return fail(h, MOE_ERR_CUDA, "cache kernel did not complete");
+    const int nm = inf->n_miss, npm = inf->n_pf_miss;
+    const size_t B = h->lay.bytes;
+    // demand misses: copy, then make the compute stream wait for them
+    for (int i = 0; i < nm; ++i) {
+        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
+        CK(h, cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
+                              cudaMemcpyHostToDevice, h->copy));
+    }
+    if (nm > 0) {
+        CK(h, cudaEventRecord(h->ev_copy, h->copy));
+        CK(h, cudaStreamWaitEvent(s, h->ev_copy, 0));
+    }
+    // experts prefetched by an earlier call must have landed before they are used
+    if (h->prefetch_pending) {
+        CK(h, cudaStreamWaitEvent(s, h->ev_prefetch, 0));
+        h->prefetch_pending = false;
+    }
+    // prefetch of the next layer: streams behind this layer's compute
+    for (int i = nm; i < nm + npm; ++i) {
+        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
+        CK(h, cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
+                              cudaMemcpyHostToDevice, h->copy));
+    }
+    if (npm > 0) {
+        CK(h, cudaEventRecord(h->ev_prefetch, h->copy));
+        h->prefetch_pending = true;
+    }
+    CK(h, moe::launch_experts(a, s));
+    // bookkeeping
+    h->st.calls++;
+    (decode ? h->st.decode_calls : h->st.prefill_calls)++;
+    h->st.hits += inf->n_hit;
+    h->st.misses += nm;
+    h->st.prefetch_hits += inf->n_pf_hit;
+    h->st.prefetch_misses += npm;
+    h->st.copies_h2d += nm + npm;
+    h->st.bytes_h2d += static_cast<uint64_t>(nm + npm) * B;
+    const int nev = inf->n_events;
+    for (int i = 0; i < nev; ++i) {
+        if (inf->ev_evicted[i] >= 0) h->st.evictions++;
+        if (h->flags & MOE_CACHE_LOG_EVENTS) {
+            moe_event ev{inf->ev_layer[i], inf->ev_expert[i], inf->ev_hit[i], inf->ev_slot[i], inf->ev_evicted[i],
+                         inf->ev_prefetch[i]};
+            h->events.push_back(ev);
+        }
+    }
+    return MOE_OK;
+}
+
+int moe_stats(moe_handle* h, moe_stats_t* s) {
+    if (!h || !s) return MOE_ERR_INVALID;
+    *s = h->st;
+    return MOE_OK;
+}
+
+int moe_stats_reset(moe_handle* h) {
+    if (!h) return MOE_ERR_INVALID;
+    h->st = moe_stats_t{};
+    h->events.clear();
+    return MOE_OK;
+}
+
+int moe_stats_events(moe_handle* h, moe_event* buf, int cap, int* n) {
+    if (!h || !n || cap < 0 || (cap > 0 && !buf)) return MOE_ERR_INVALID;
+    const int m = std::min<int>(cap, static_cast<int>(h->events.size()));
+    for (int i = 0; i < m; ++i) buf[i] = h->events[i];
+    h->events.erase(h->events.begin(), h->events.begin() + m);
+    *n = m;
+    return MOE_OK;
+}
+
+int moe_debug_routing(moe_handle* h, int32_t* topk_idx, float* gates, int32_t* perm, int32_t* counts,
+                      int32_t* uniq, int32_t* n_uniq) {
+    if (!h) return MOE_ERR_INVALID;
+    CK(h, cudaSetDevice(h->d.device));
+    if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
+    const size_t n = static_cast<size_t>(h->last_T) * h->d.top_k;
+    const CallArgs& a = h->base;
+    if (topk_idx) CK(h, cudaMemcpy(topk_idx, a.topk, n * 4, cudaMemcpyDeviceToHost));
+    if (gates) CK(h, cudaMemcpy(gates, a.gates, n * 4, cudaMemcpyDeviceToHost));
+    if (perm) CK(h, cudaMemcpy(perm, a.perm, n * 4, cudaMemcpyDeviceToHost));
+    if (counts) CK(h, cudaMemcpy(counts, a.counts, static_cast<size_t>(h->d.num_experts) * 4, cudaMemcpyDeviceToHost));
+    int32_t nu = 0;
+    CK(h, cudaMemcpy(&nu, a.n_uniq, 4, cudaMemcpyDeviceToHost));
+    if (uniq) CK(h, cudaMemcpy(uniq, a.act_expert, static_cast<size_t>(nu) * 4, cudaMemcpyDeviceToHost));
+    if (n_uniq) *n_uniq = nu;
+    return MOE_OK;
+}
+
+int moe_debug_lru_table(moe_handle* h, int32_t* table) {
+    if (!h || !table) return MOE_ERR_INVALID;
+    if (!h->table) return fail(h, MOE_ERR_STATE, "moe_cache_config has not been called");
+    CK(h, cudaSetDevice(h->d.device));
+    if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
+    CK(h, cudaMemcpy(table, h->table, static_cast<size_t>(h->d.num_layers) * h->d.num_experts * 4,
+                     cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+const char* moe_last_error(const moe_handle* h) { return h ? h->err.c_str() : "NULL handle"; }
+
+void moe_destroy(moe_handle* h) {
+    if (!h) return;
+    cudaSetDevice(h->d.device);
+    cudaDeviceSynchronize();
+    free_pool(h);
+    for (auto* b : h->bank)
+        if (b) cudaFreeHost(b);
+    cudaFree(h->shared_dev);
+    cudaFree(h->scratch);
+    if (h->info_h) cudaFreeHost(h->info_h);
+    if (h->ev_cache) cudaEventDestroy(h->ev_cache);
+    if (h->ev_copy) cudaEventDestroy(h->ev_copy);
+    if (h->ev_prefetch) cudaEventDestroy(h->ev_prefetch);
+    if (h->stream) cudaStreamDestroy(h->stream);
+    if (h->copy) cudaStreamDestroy(h->copy);
+    delete h;
+}
+
+}  // extern "C"

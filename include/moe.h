@@ -1,0 +1,178 @@
+/*
+ * moe.h — C ABI of the B300 routed Mixture-of-Experts layer with an LRU expert
+ * cache fed from pinned host memory.
+ *
+ * The operation (what one moe_layer_forward call computes), following
+ * "FreeToken量子化：MoE推論のセットアップガイド" (freetoken.wiki, architecture
+ * page: two-tier expert memory, decode LRU cache, prefill whole-layer double
+ * buffering) and the bhrtaym-blog post on FreeToken (section on the four MoE
+ * backends, `offload`: experts live in host RAM, the GPU holds LRU slots,
+ * misses stream over PCIe):
+ *
+ *   logits[t,e] = sum_h hidden[t,h] * router_w[e,h]      (one fixed fp32 order)
+ *   p[t,:]      = softmax(logits[t,:])
+ *   idx[t,0..k) = the k largest logits (ties: lower expert index), descending
+ *   gate[t,j]   = p[t,idx[t,j]] / sum_j' p[t,idx[t,j']]
+ *   out[t]      = sum_j gate[t,j] * FFN_{idx[t,j]}(hidden[t]) + sum_s SHARED_s(hidden[t])
+ *   FFN_e(x)    = W_down,e ( silu(W_gate,e x) * (W_up,e x) )
+ *
+ * Every routed expert of every layer lives in a library-owned pinned host
+ * bank; the GPU holds one pool of S expert slots shared by all layers. Each
+ * call looks its experts up in a device-side LRU table; misses are copied into
+ * the pool with cudaMemcpyAsync on a side stream. Prefill calls (T > 8) with
+ * MOE_CACHE_PREFETCH_NEXT_LAYER also stream all experts of layer+1 into the
+ * pool while this layer computes, when the pool has room for both.
+ *
+ * Conventions
+ *  - Every call returns MOE_OK (0) or a negative moe_status. Nothing throws and
+ *    nothing aborts. moe_last_error() gives a human-readable reason.
+ *  - Device pointers: hidden, router_w, out (caller-owned, caller keeps them
+ *    alive until the work on `stream` has completed).
+ *  - Host pointers: everything in moe_model_desc / moe_expert_host / result
+ *    buffers; the library copies what it keeps before returning.
+ *  - One handle is used by one host thread, and all forward calls on a handle
+ *    are issued on one CUDA stream (the cache's slot reuse is ordered by it).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = -1,   /* bad argument or unsupported shape */
+    MOE_ERR_OOM = -2,       /* host (pinned) or device allocation failed */
+    MOE_ERR_CUDA = -3,      /* a CUDA runtime call failed */
+    MOE_ERR_CAPACITY = -4,  /* the experts one call needs do not fit in the pool */
+    MOE_ERR_TIMEOUT = -5,   /* a bounded device wait gave up */
+    MOE_ERR_STATE = -6      /* call out of order (e.g. forward before moe_cache_config) */
+} moe_status;
+
+typedef enum moe_weight_fmt {
+    MOE_FMT_FP32 = 0,   /* float32 rows */
+    MOE_FMT_BF16 = 1,   /* bfloat16 rows */
+    MOE_FMT_NVFP4 = 2,  /* E2M1 codes, E4M3 scale per 16 elements, fp32 scale per tensor */
+    MOE_FMT_MXFP4 = 3   /* E2M1 codes, E8M0 scale per 32 elements */
+} moe_weight_fmt;
+
+typedef enum moe_act_dtype { MOE_ACT_FP32 = 0, MOE_ACT_BF16 = 1 } moe_act_dtype;
+
+/* MOE_MODE_LINEAR_TEST replaces silu by the identity; it exists so that tests
+ * can check the layer against closed forms. */
+typedef enum moe_act_mode { MOE_MODE_SWIGLU = 0, MOE_MODE_LINEAR_TEST = 1 } moe_act_mode;
+
+#define MOE_DECODE_MAX_T 8                /* T <= 8: decode path; T > 8: prefill path */
+#define MOE_CACHE_PREFETCH_NEXT_LAYER 1u  /* prefill: stream layer+1 behind layer */
+#define MOE_CACHE_LOG_EVENTS 2u           /* keep a per-expert hit/miss event log */
+
+typedef struct moe_model_desc {
+    int32_t num_layers;   /* L >= 1 */
+    int32_t num_experts;  /* E routed experts per layer, 1..1024 */
+    int32_t num_shared;   /* always-on shared experts per layer, 0..1 */
+    int32_t top_k;        /* k, 1..min(E, 32) */
+    int32_t hidden;       /* H; multiple of 128 (FP32 weights: multiple of 8) */
+    int32_t inter;        /* I; multiple of 128 (FP32 weights: any >= 1) */
+    int32_t weight_fmt;   /* moe_weight_fmt */
+    int32_t act_dtype;    /* moe_act_dtype of hidden, router_w and out */
+    int32_t act_mode;     /* moe_act_mode */
+    int32_t max_tokens;   /* largest T a forward call may pass (0 = 4096) */
+    int32_t device;       /* CUDA device ordinal */
+} moe_model_desc;
+
+/* One weight tensor in the canonical host layout: row-major [N, K] with K the
+ * input dimension (gate, up: [I, H]; down: [H, I]).
+ *  FP32 / BF16: data = N*K elements; scales unused.
+ *  NVFP4: data = N*K/2 bytes, element 2i in the low nibble of byte i;
+ *         scales = N*K/16 E4M3 bytes (row-major [N, K/16]); global_scale used.
+ *  MXFP4: data as NVFP4; scales = N*K/32 E8M0 bytes ([N, K/32]). */
+typedef struct moe_tensor_host {
+    const void* data;
+    const uint8_t* scales;
+    float global_scale;
+} moe_tensor_host;
+
+typedef struct moe_expert_host {
+    moe_tensor_host gate, up, down;
+} moe_expert_host;
+
+typedef struct moe_stats_t {
+    uint64_t calls, decode_calls, prefill_calls;
+    uint64_t hits, misses;                    /* demand accesses of routed experts */
+    uint64_t prefetch_hits, prefetch_misses;  /* next-layer prefetch batches */
+    uint64_t evictions;
+    uint64_t copies_h2d, bytes_h2d;           /* expert copies issued */
+    uint64_t device_errors;
+} moe_stats_t;
+
+typedef struct moe_event {
+    int32_t layer, expert, hit, slot, evicted_key, prefetch;
+} moe_event;
+
+typedef struct moe_handle moe_handle;
+
+/* Creates a handle: validates the shape, picks the device, creates the copy
+ * stream and events, and allocates the per-call device scratch (sized for
+ * max_tokens). Host banks are allocated lazily per layer by moe_load_expert.
+ * Returns MOE_ERR_INVALID for an unsupported shape, MOE_ERR_OOM/CUDA on
+ * allocation failure (nothing is leaked). */
+int moe_init(const moe_model_desc* desc, moe_handle** out);
+
+/* Bytes of one expert in the library's device layout (the unit the cache
+ * stores and copies). */
+int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
+
+/* Copies one expert from the canonical host layout into the library's pinned
+ * host bank (routed experts, expert < E) or into device-resident memory
+ * (shared experts, E <= expert < E + num_shared), repacking it into the device
+ * layout. The caller's buffers may be freed on return. Synchronous. */
+int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host* w);
+
+/* A safe point: waits until the device is idle, then (re)builds the expert
+ * pool with capacity_slots slots shared by all layers, and empties the LRU
+ * table. flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS. Every
+ * routed expert must have been loaded before the first forward call.
+ * capacity_slots < top_k gives MOE_ERR_CAPACITY. */
+int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
+
+/* One call of MoE layer `layer_id` on T tokens (0 <= T <= max_tokens):
+ * hidden [T, H], router_w [E, H], out [T, H], all device memory in the handle's
+ * act_dtype, row-major. Enqueued on `stream` (a cudaStream_t; NULL = the
+ * handle's own stream). The call blocks the host until this layer's routing
+ * and cache lookup have run on the device (the misses must be known to issue
+ * their copies); the expert FFN work itself is left running on `stream`.
+ * MOE_ERR_CAPACITY if the layer's experts exceed the pool (the cache is left
+ * unchanged and out is not written). */
+int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, int layer_id,
+                      int T, void* out, void* stream);
+
+/* Cumulative counters since moe_init (or the last moe_stats_reset). */
+int moe_stats(moe_handle* h, moe_stats_t* s);
+int moe_stats_reset(moe_handle* h);
+
+/* Drains up to cap logged events (MOE_CACHE_LOG_EVENTS) into buf, in the order
+ * the cache served them; *n receives the number written. */
+int moe_stats_events(moe_handle* h, moe_event* buf, int cap, int* n);
+
+/* Host copies of the routing of the last forward call (any pointer may be
+ * NULL): topk_idx [T*k], gates [T*k], perm [T*k], counts [E], uniq [E]
+ * (ascending experts with at least one token; *n_uniq entries). Synchronous. */
+int moe_debug_routing(moe_handle* h, int32_t* topk_idx, float* gates, int32_t* perm,
+                      int32_t* counts, int32_t* uniq, int32_t* n_uniq);
+
+/* Host copy of the LRU table [L*E] (slot or -1) after the last call. */
+int moe_debug_lru_table(moe_handle* h, int32_t* table);
+
+const char* moe_last_error(const moe_handle* h);
+
+void moe_destroy(moe_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

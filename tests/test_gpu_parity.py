@@ -1,0 +1,177 @@
+"""CUDA path vs oracle on the same seeded inputs, through the C ABI.
+
+Bit-exact: top-k indices, permutation, counts, unique-expert list and the LRU
+hit/miss/slot/eviction event sequence. Outputs: max |y - y_ref| / max |y_ref|
+<= 2e-2 (bf16 I/O, fp32 accumulation). Small shapes span several 128-wide
+K groups, 16-row tiles and 8-column tiles with ragged tails; the workload
+shapes run on a subset of their layers with sampled output rows."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+try:
+    import torch
+    HAVE_GPU = torch.cuda.is_available()
+except Exception:  # pragma: no cover
+    HAVE_GPU = False
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not HAVE_GPU:
+        pytest.skip("no CUDA device")
+    from expert_offload_softmax_b300 import build
+    build.build()
+
+
+def _run(shape, seed, L, capacity, calls, flags=0, sample=None, max_tokens=0):
+    """calls: list of (layer, T, step). Returns the measured errors."""
+    from moe_harness import GpuStack, OracleStack, compare
+    g = GpuStack(shape, seed, L, capacity, flags, max_tokens=max_tokens)
+    o = OracleStack(shape, seed, L, capacity, prefetch=bool(flags & 1))
+    errs = []
+    try:
+        for (layer, T, step) in calls:
+            x = synth.hidden_states(shape, seed, layer, T, step)
+            toks = None if sample is None or T <= sample else np.linspace(0, T - 1, sample).astype(int)
+            gr = g.forward(layer, x)
+            orr = o.forward(layer, x, toks)
+            errs.append(compare(gr, orr))
+    finally:
+        g.close()
+    return errs
+
+
+def test_tiny_fp32_workload():
+    s = synth.TINY_FP32
+    errs = _run(s, 0, 1, 8, [(0, 4, 0), (0, 4, 1), (0, 1, 2)])
+    assert max(e["out_err"] for e in errs) < 1e-5
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_small_decode_all_formats(fmt, T):
+    s = synth.Shape("small", L=3, E=16, k=4, H=384, I=256, fmt=fmt, act=synth.ACT_BF16)
+    calls = [(l % 3, T, l) for l in range(7)]
+    _run(s, 11, 3, 10, calls)
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("T", [9, 37, 200])
+def test_small_prefill_all_formats(fmt, T):
+    s = synth.Shape("small", L=3, E=16, k=4, H=384, I=256, fmt=fmt, act=synth.ACT_BF16)
+    calls = [(l % 3, T, l) for l in range(5)]
+    _run(s, 12, 3, 20, calls, flags=0)
+
+
+def test_prefill_prefetch_next_layer():
+    s = synth.Shape("small", L=4, E=16, k=4, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
+    calls = [(l, 64, 0) for l in range(4)] + [(l, 64, 1) for l in range(4)]
+    _run(s, 13, 4, 40, calls, flags=1)  # 40 >= 16 + 16: prefetch runs
+
+
+def test_shared_expert_and_fp32_activations():
+    s = synth.Shape("shared", L=2, E=8, k=2, H=256, I=128, fmt=synth.FMT_MXFP4, act=synth.ACT_FP32, shared=1)
+    _run(s, 14, 2, 6, [(0, 5, 0), (1, 5, 0), (0, 20, 1), (1, 1, 2)])
+
+
+def test_linear_mode_closed_form_path():
+    s = synth.Shape("lin", L=1, E=8, k=3, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16, act_mode=1)
+    _run(s, 15, 1, 8, [(0, 6, 0), (0, 40, 1)])
+
+
+def test_zipf_skewed_decode_many_steps():
+    s = synth.Shape("zipf", L=4, E=64, k=8, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16, zipf_s=1.0)
+    calls = [(l, 1 + (st % 8), st) for st in range(12) for l in range(4)]
+    _run(s, 16, 4, 64, calls)
+
+
+def test_capacity_error_leaves_cache_unchanged():
+    import expert_offload_softmax_b300 as moe
+    from moe_harness import GpuStack
+    s = synth.Shape("cap", L=1, E=16, k=4, H=256, I=128, fmt=synth.FMT_BF16, act=synth.ACT_BF16)
+    g = GpuStack(s, 17, 1, 4)
+    try:
+        g.forward(0, synth.hidden_states(s, 17, 0, 1, 0))
+        before = moe.moe_debug_lru_table(g.h, 1, 16).copy()
+        x = synth.hidden_states(s, 17, 0, 8, 1)   # 8 tokens x 4 experts: more than 4 distinct
+        with pytest.raises(moe.MoeError) as ei:
+            g.forward(0, x)
+        assert ei.value.code == moe.MOE_ERR_CAPACITY
+        assert np.array_equal(before, moe.moe_debug_lru_table(g.h, 1, 16))
+    finally:
+        g.close()
+
+
+def test_empty_call_and_bad_arguments():
+    import expert_offload_softmax_b300 as moe
+    from moe_harness import GpuStack
+    s = synth.Shape("e", L=2, E=8, k=2, H=128, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
+    g = GpuStack(s, 18, 2, 8)
+    try:
+        x = g.to_dev(synth.hidden_states(s, 18, 0, 2, 0))
+        out = g.out_buf(2)
+        moe.moe_layer_forward(g.h, x.data_ptr(), g.router[0].data_ptr(), 0, 0, out.data_ptr())
+        for layer, T in ((2, 2), (-1, 2), (0, 100000)):
+            with pytest.raises(moe.MoeError) as ei:
+                moe.moe_layer_forward(g.h, x.data_ptr(), g.router[0].data_ptr(), layer, T, out.data_ptr())
+            assert ei.value.code == moe.MOE_ERR_INVALID
+    finally:
+        g.close()
+
+
+def test_two_runs_bitwise_identical():
+    from moe_harness import GpuStack
+    s = synth.Shape("det", L=2, E=32, k=4, H=512, I=256, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
+    outs = []
+    for _ in range(2):
+        g = GpuStack(s, 19, 2, 64)
+        try:
+            outs.append([g.forward(l, synth.hidden_states(s, 19, l, T, 0))["out"] for l, T in ((0, 3), (1, 77))])
+        finally:
+            g.close()
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- workload shapes
+
+def test_workload_decode_nvfp4_layer_subset():
+    """decode-40L-H2048-E256-k8-I512-nvfp4 on 4 of its layers (same per-layer
+    shape, Zipf s=1.0), pool = 25% of the experts of those layers."""
+    s = synth.DECODE_NVFP4
+    L = 4
+    cap = synth.capacity_slots(synth.Shape("x", L=L, E=s.E, k=s.k, H=s.H, I=s.I, fmt=s.fmt, act=s.act), 0.25)
+    calls = [(l, T, st) for st, T in enumerate((1, 8, 1, 8, 1)) for l in range(L)]
+    _run(s, 0, L, cap, calls)
+
+
+def test_workload_prefill_bf16_layer_subset():
+    """prefill-40L-H2048-E256-k8-I512-bf16 at T=4096 on 2 layers with prefetch,
+    routing in full, outputs on 48 sampled tokens."""
+    s = synth.PREFILL_BF16
+    _run(s, 0, 2, 256 + 256 + 8, [(0, 4096, 0), (1, 4096, 0)], flags=1, sample=48, max_tokens=4096)
+
+
+def test_workload_large_mxfp4_shared_layer_subset():
+    """large-24L-H4096-E256+1-k8-I2048-mxfp4: decode T=1 and prefill T=2048 on
+    2 layers, outputs on sampled tokens."""
+    s = synth.LARGE_MXFP4
+    _run(s, 0, 2, 300, [(0, 1, 0), (1, 1, 0), (0, 2048, 1)], sample=6, max_tokens=2048)
+
+
+def test_workload_stress_nvfp4_layer_subset():
+    """stress-16L-H6144-E160-k8-I2048-nvfp4: decode T=1 with Zipf s=1.1 and
+    step reuse (p=0.7) on 3 layers, pool of 10% of those layers' experts."""
+    s = synth.STRESS_NVFP4
+    L = 3
+    cap = max(s.k, int(0.10 * s.E * L))
+    reuse = synth.reuse_flags(0, 12, 0.7)
+    calls, src = [], 0
+    for st in range(12):
+        src = src if reuse[st] else st
+        calls += [(l, 1, src) for l in range(L)]
+    _run(s, 0, L, cap, calls)
