@@ -56,7 +56,7 @@ def test_tiny_fp32_workload():
 def test_small_decode_all_formats(fmt, T):
     s = synth.Shape("small", L=3, E=16, k=4, H=384, I=256, fmt=fmt, act=synth.ACT_BF16)
     calls = [(l % 3, T, l) for l in range(7)]
-    _run(s, 11, 3, 10, calls)
+    _run(s, 11, 3, 10 if T < 8 else 20, calls)
 
 
 @pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4])
@@ -75,7 +75,7 @@ def test_prefill_prefetch_next_layer():
 
 def test_shared_expert_and_fp32_activations():
     s = synth.Shape("shared", L=2, E=8, k=2, H=256, I=128, fmt=synth.FMT_MXFP4, act=synth.ACT_FP32, shared=1)
-    _run(s, 14, 2, 6, [(0, 5, 0), (1, 5, 0), (0, 20, 1), (1, 1, 2)])
+    _run(s, 14, 2, 10, [(0, 5, 0), (1, 5, 0), (0, 20, 1), (1, 1, 2)])
 
 
 def test_linear_mode_closed_form_path():
