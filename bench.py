@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE layer stack with the LRU expert cache.
+
+One step = one batch of T tokens through every layer of the stack, the whole
+hot path per layer: activation prep, router logits, softmax/top-k, permutation,
+device LRU, miss copies from pinned host banks, SwiGLU experts and combine.
+Default workload: decode T=1 on the 40-layer NVFP4 stack (H=2048, E=256, k=8,
+I=512, Zipf s=1.0 routing) with a pool of 25% of all experts; every step draws
+fresh seeded hidden states for each layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|decode8|prefill]
+
+Prints one JSON line. --impl reference times the oracle (plain single-threaded
+CPU) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode T=1, prefill T=4096); % of HBM / FP4 tensor roofline"
+UNIT = "tokens/s"
+
+WORKLOADS = {
+    # name: (shape, T, pool fraction, cache flags, layers used)
+    "decode": (synth.DECODE_NVFP4, 1, 0.25, 0, 40),
+    "decode8": (synth.DECODE_NVFP4, 8, 0.25, 0, 40),
+    "prefill": (synth.PREFILL_BF16, 4096, 0.5, 1, 8),
+}
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = max(mx, float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source has not changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[f"{kernel}/{workload}"]
+        if e["source_hash"] != _source_hash(e["sources"]):
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------- our arm
+
+def load_stack(moe, shape, L, capacity, flags, device, max_tokens, seed=0):
+    desc = moe.make_desc(L, shape.E, shape.k, shape.H, shape.I, shape.fmt, shape.act, shared=shape.shared,
+                         mode=shape.act_mode, max_tokens=max_tokens, device=device)
+    h = moe.moe_init(desc)
+
+    def load_layer(l):
+        for e in range(shape.E + shape.shared):
+            moe.moe_load_expert(h, l, e, synth.expert_weights(shape, seed, l, e))
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(load_layer, range(L)))
+    moe.moe_cache_config(h, capacity, flags)
+    return h
+
+
+def h2d_peak_gbs(torch, device, nbytes=1 << 30, reps=5):
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    best = 0.0
+    s = torch.cuda.Stream(device=device)
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            dst.copy_(src, non_blocking=True)
+            b.record(s)
+        s.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import expert_offload_softmax_b300 as moe
+    from expert_offload_softmax_b300 import build
+    build.build()
+    moe.load()
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shape, T, frac, flags, L = WORKLOADS[args.workload]
+    cap_shape = synth.Shape("cap", L=L, E=shape.E, k=shape.k, H=shape.H, I=shape.I, fmt=shape.fmt, act=shape.act)
+    S = synth.capacity_slots(cap_shape, frac)
+    t_load = time.time()
+    h = load_stack(moe, shape, L, S, flags, local, max_tokens=max(T, 8))
+    t_load = time.time() - t_load
+    router = []
+    for l in range(L):
+        r = synth.router_weights(shape, 0, l)
+        router.append(torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16))
+    nsteps = args.warmup + args.steps
+    # per (step, layer) hidden states, distinct across ranks
+    hid = np.empty((nsteps, L, T, shape.H), np.uint16)
+    for st in range(nsteps):
+        for l in range(L):
+            hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + st)
+    x_dev = torch.from_numpy(hid.view(np.int16)).to(dev).view(torch.bfloat16)
+    out_dev = torch.empty((L, T, shape.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def step(st):
+        for l in range(L):
+            moe.moe_layer_forward(h, x_dev[st, l].data_ptr(), router[l].data_ptr(), l, T, out_dev[l].data_ptr(), sp)
+
+    for st in range(args.warmup):
+        step(st)
+    stream.synchronize()
+    moe.moe_stats_reset(h)
+    moe.moe_timing_enable(h, True)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for st in range(args.warmup, nsteps):
+        step(st)
+    ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    timing = moe.moe_timing(h)
+    moe.moe_timing_enable(h, False)
+    stats = moe.moe_stats(h)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public call with host buffers: per step, copy the
+    # step's hidden states from pinned host memory, run every layer, read the
+    # outputs back into pinned host memory
+    hid_pin = torch.from_numpy(hid.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_pin = torch.empty((L, T, shape.H), dtype=torch.bfloat16).pin_memory()
+    xin = torch.empty((L, T, shape.H), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for st in range(args.warmup, nsteps):
+        with torch.cuda.stream(stream):
+            xin.copy_(hid_pin[st], non_blocking=True)
+        for l in range(L):
+            moe.moe_layer_forward(h, xin[l].data_ptr(), router[l].data_ptr(), l, T, out_dev[l].data_ptr(), sp)
+        with torch.cuda.stream(stream):
+            out_pin.copy_(out_dev, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_wall = (time.perf_counter() - w0) * 1e3
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    moe.moe_destroy(h)
+
+    if rank != 0:
+        return None
+    pcie = h2d_peak_gbs(torch, dev)
+    peaks, peak_kind = _peaks()
+    K = args.steps
+    value = world * K * T / (ms * 1e-3)
+    # dominant library kernel by device time
+    kern = {"gate_up": (timing["gate_up_ms"], timing["gate_up_bytes"]),
+            "down": (timing["down_ms"], timing["down_bytes"])}
+    if timing["combine_ms"] > 0:
+        kern["combine"] = (timing["combine_ms"], timing["combine_bytes"])
+    dom = max(kern, key=lambda n: kern[n][0])
+    dms, dbytes = kern[dom]
+    calls = max(1, timing["calls"])
+    achieved = dbytes / (dms * 1e-3) / 1e9 if dms > 0 else 0.0
+    peak = peaks.get("hbm_gbs", 6400.0)
+    traffic = _traffic_for(dom, args.workload)
+    cpu = cpu_baseline(shape, T, L, budget_s=args.cpu_budget) if world == 1 else None
+    cap_hits = stats["hits"] + stats["misses"]
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 weights x f16 activations, fp32 accumulate"
+        if shape.fmt == synth.FMT_NVFP4 else "bf16 x bf16, fp32 accumulate",
+        "data": "synthetic (seeded; random weights of the stated shape)",
+        "config": {"workload": shape.name if T == 1 or args.workload != "decode8" else shape.name,
+                   "T": T, "layers": L, "pool_slots": S, "pool_frac": frac,
+                   "router_zipf_s": shape.zipf_s, "cache_flags": flags,
+                   "l2": "per-step working set (active experts' weights, %d MB) exceeds the 126 MB L2"
+                         % ((timing["gate_up_bytes"] + timing["down_bytes"]) // max(1, K) // (1 << 20)),
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 6.4 TB/s",
+                     "algorithmic_bytes_per_launch": int(dbytes // calls),
+                     "avg_launch_us": round(dms * 1e3 / calls, 3),
+                     "traffic": traffic},
+        "kernels_ms_per_step": {"route+cache": round(timing["route_ms"] / K, 4),
+                                "gate_up": round(timing["gate_up_ms"] / K, 4),
+                                "down": round(timing["down_ms"] / K, 4),
+                                "combine": round(timing["combine_ms"] / K, 4),
+                                "h2d_copies": round(timing["copy_ms"] / K, 4)},
+        "cache": {"hit_rate": round(stats["hits"] / cap_hits, 4) if cap_hits else None,
+                  "misses_per_step": round(stats["misses"] / K, 3),
+                  "h2d_bytes_per_step": int(stats["bytes_h2d"] // K),
+                  "prefetch_misses_per_step": round(stats["prefetch_misses"] / K, 3)},
+        "pcie": {"h2d_peak_gbs": round(pcie, 2),
+                 "miss_stream_gbs": round(timing["copy_bytes"] / (timing["copy_ms"] * 1e-3) / 1e9, 2)
+                 if timing["copy_ms"] > 0 else None},
+        "e2e": {"value": round(world * K * T / (e2e_ms * 1e-3), 3), "unit": UNIT,
+                "h2d_bytes_per_step": L * T * shape.H * 2, "d2h_bytes_per_step": L * T * shape.H * 2,
+                "wall_ms": round(e2e_wall, 2)},
+        "gpu_launches": int(stats["kernel_launches"]),
+        "load_s": round(t_load, 1),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- oracle
+
+def oracle_layer_seconds(shape, T, L, budget_s, step0=0):
+    """Times the oracle on layer calls of the workload (T tokens, cycling
+    through the layers) until ~budget_s of oracle time has elapsed. Expert
+    weights are generated untimed; routing, LRU, dequantisation and the expert
+    math are timed. Returns (seconds per layer call, calls)."""
+    import oracle
+    from moe_harness import act_to_f32
+    lru = oracle.LRU(L, shape.E, synth.capacity_slots(shape, 0.25))
+    routers = {}
+    spent, calls = 0.0, 0
+    while spent < budget_s or calls == 0:
+        l = calls % L
+        if l not in routers:
+            routers[l] = act_to_f32(synth.router_weights(shape, 0, l), shape)
+        x = act_to_f32(synth.hidden_states(shape, 0, l, T, step=step0 + calls), shape)
+        t0 = time.perf_counter()
+        r = oracle.route(x, routers[l], shape.k)
+        lru.access(l, r["uniq"], T, False)
+        t1 = time.perf_counter()
+        need = sorted(set(int(e) for e in np.unique(r["topk_idx"])) | set(range(shape.E, shape.E + shape.shared)))
+        raw = {e: synth.expert_weights(shape, 0, l, e) for e in need}
+        t2 = time.perf_counter()
+        ws = {e: oracle.dequant_expert(shape.fmt, raw[e], shape.H, shape.I) for e in need}
+        oracle.layer_tokens(x, r["topk_idx"], r["gates"], ws, shape.E, shape.shared, shape.act_mode, np.arange(T))
+        t3 = time.perf_counter()
+        spent += (t1 - t0) + (t3 - t2)
+        calls += 1
+    return spent / calls, calls
+
+
+def cpu_baseline(shape, T, L, budget_s=15.0):
+    per_call, calls = oracle_layer_seconds(shape, T, L, budget_s)
+    return {"value": round(T / (per_call * L), 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{calls} layer calls (T={T}) of the {L}-layer stack; tokens/s = T / (L x mean s per call)"}
+
+
+def run_reference(args):
+    shape, T, frac, flags, L = WORKLOADS[args.workload]
+    budget = float(os.environ.get("MOE_REF_STEP_BUDGET_S", "1.0"))
+    for _ in range(args.warmup):
+        oracle_layer_seconds(shape, T, L, 0.0)
+    secs = []
+    for st in range(args.steps):
+        per_call, _ = oracle_layer_seconds(shape, T, L, budget, step0=10007 * (st + 1))
+        secs.append(per_call * L)
+    ms = float(np.mean(secs)) * 1e3
+    value = T / (ms * 1e-3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (CPU oracle)",
+        "data": "synthetic (seeded; random weights of the stated shape)",
+        "config": {"workload": shape.name, "T": T, "layers": L, "pool_frac": frac},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: layer calls (T={T}) for ~{budget:.1f} s of oracle time, "
+                                   f"scaled to the {L}-layer stack"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", 1)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -32,7 +32,7 @@ MOE_CACHE_LOG_EVENTS = 2
 # every symbol the header declares
 EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward",
            "moe_stats", "moe_stats_reset", "moe_stats_events", "moe_debug_routing", "moe_debug_lru_table",
-           "moe_last_error", "moe_destroy"]
+           "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing"]
 
 
 class moe_model_desc(ctypes.Structure):
@@ -52,10 +52,20 @@ class moe_expert_host(ctypes.Structure):
 class moe_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "calls", "decode_calls", "prefill_calls", "hits", "misses", "prefetch_hits", "prefetch_misses",
-        "evictions", "copies_h2d", "bytes_h2d", "device_errors")]
+        "evictions", "copies_h2d", "bytes_h2d", "device_errors", "kernel_launches")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class moe_timing_t(ctypes.Structure):
+    _fields_ = [("calls", ctypes.c_uint64)] + [(n, ctypes.c_double) for n in (
+        "route_ms", "gate_up_ms", "down_ms", "combine_ms", "copy_ms")] + [(n, ctypes.c_uint64) for n in (
+        "gate_up_bytes", "down_bytes", "combine_bytes", "copy_bytes")]
+
+    def as_dict(self):
+        return {n: (float(getattr(self, n)) if t is ctypes.c_double else int(getattr(self, n)))
+                for n, t in self._fields_}
 
 
 class moe_event(ctypes.Structure):
@@ -89,6 +99,8 @@ def load(path: str | None = None):
     lib.moe_layer_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp]
     lib.moe_stats.argtypes = [vp, P(moe_stats_t)]
     lib.moe_stats_reset.argtypes = [vp]
+    lib.moe_timing_enable.argtypes = [vp, i32]
+    lib.moe_timing.argtypes = [vp, P(moe_timing_t)]
     lib.moe_stats_events.argtypes = [vp, P(moe_event), i32, P(i32)]
     lib.moe_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, P(ctypes.c_int32)]
     lib.moe_debug_lru_table.argtypes = [vp, vp]
@@ -164,11 +176,21 @@ def moe_stats(h: int) -> dict:
     return s.as_dict()
 
 
+def moe_timing_enable(h: int, enable: bool = True) -> None:
+    _check(h, load().moe_timing_enable(h, 1 if enable else 0))
+
+
+def moe_timing(h: int) -> dict:
+    t = moe_timing_t()
+    _check(h, load().moe_timing(h, ctypes.byref(t)))
+    return t.as_dict()
+
+
 def moe_stats_reset(h: int) -> None:
     _check(h, load().moe_stats_reset(h))
 
 
-def moe_stats_events(h: int, cap: int = 1 << 20) -> np.ndarray:
+def moe_stats_events(h: int, cap: int = 8192) -> np.ndarray:
     """Drains the event log: int32 array [n, 6] (layer, expert, hit, slot, evicted_key, prefetch)."""
     buf = (moe_event * cap)()
     n = ctypes.c_int()

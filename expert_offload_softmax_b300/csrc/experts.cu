@@ -521,41 +521,59 @@ __global__ void __launch_bounds__(256) k_down_f32(CallArgs a) {
 // --------------------------------------------------------------------------
 
 template <int FMT, int ACT>
-static void launch_mma_path(const CallArgs& a, cudaStream_t s) {
+static int launch_mma_path(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down) {
     const int max_active = min(a.E, a.T * a.k) + a.n_shared;
     if (a.T <= kDecodeMaxT) {
         k_gu<FMT, 1><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
+        if (ev_gu) cudaEventRecord(ev_gu, s);
         k_down_dec<FMT, ACT><<<a.H / 16, 128, 0, s>>>(a);
-    } else {
-        k_gu<FMT, 8><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
-        k_down_rows<FMT, 8><<<dim3(a.H / 16, max_active), 128, 0, s>>>(a);
-        const size_t n8 = static_cast<size_t>(a.T) * a.H / 8;
-        const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 148 * 16));
-        k_combine<ACT><<<blocks, 256, 0, s>>>(a);
+        if (ev_down) cudaEventRecord(ev_down, s);
+        return 2;
     }
+    k_gu<FMT, 8><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
+    if (ev_gu) cudaEventRecord(ev_gu, s);
+    k_down_rows<FMT, 8><<<dim3(a.H / 16, max_active), 128, 0, s>>>(a);
+    if (ev_down) cudaEventRecord(ev_down, s);
+    const size_t n8 = static_cast<size_t>(a.T) * a.H / 8;
+    const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 148 * 16));
+    k_combine<ACT><<<blocks, 256, 0, s>>>(a);
+    return 3;
 }
 
-cudaError_t launch_experts(const CallArgs& a, cudaStream_t s) {
+cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
+                           int* launches) {
+    int n = 0;
     if (a.fmt == FMT_FP32) {
         const int max_active = min(a.E, a.T * a.k) + a.n_shared;
         const int gx = min((a.T * a.I + 255) / 256, 64);
         const int gd = min((a.T * a.H + 255) / 256, 148 * 8);
-        if (a.act == ACT_BF16) {
-            k_gu_f32<ACT_BF16><<<dim3(gx, max_active), 256, 0, s>>>(a);
-            k_down_f32<ACT_BF16><<<gd, 256, 0, s>>>(a);
-        } else {
-            k_gu_f32<ACT_FP32><<<dim3(gx, max_active), 256, 0, s>>>(a);
-            k_down_f32<ACT_FP32><<<gd, 256, 0, s>>>(a);
+        if (a.act == ACT_BF16) k_gu_f32<ACT_BF16><<<dim3(gx, max_active), 256, 0, s>>>(a);
+        else k_gu_f32<ACT_FP32><<<dim3(gx, max_active), 256, 0, s>>>(a);
+        if (ev_gu) cudaEventRecord(ev_gu, s);
+        if (a.act == ACT_BF16) k_down_f32<ACT_BF16><<<gd, 256, 0, s>>>(a);
+        else k_down_f32<ACT_FP32><<<gd, 256, 0, s>>>(a);
+        if (ev_down) cudaEventRecord(ev_down, s);
+        n = 2;
+    } else {
+        const bool bf = a.act == ACT_BF16;
+        switch (a.fmt) {
+            case FMT_BF16:
+                n = bf ? launch_mma_path<FMT_BF16, ACT_BF16>(a, s, ev_gu, ev_down)
+                       : launch_mma_path<FMT_BF16, ACT_FP32>(a, s, ev_gu, ev_down);
+                break;
+            case FMT_NVFP4:
+                n = bf ? launch_mma_path<FMT_NVFP4, ACT_BF16>(a, s, ev_gu, ev_down)
+                       : launch_mma_path<FMT_NVFP4, ACT_FP32>(a, s, ev_gu, ev_down);
+                break;
+            case FMT_MXFP4:
+                n = bf ? launch_mma_path<FMT_MXFP4, ACT_BF16>(a, s, ev_gu, ev_down)
+                       : launch_mma_path<FMT_MXFP4, ACT_FP32>(a, s, ev_gu, ev_down);
+                break;
+            default:
+                return cudaErrorInvalidValue;
         }
-        return cudaGetLastError();
     }
-    const bool bf = a.act == ACT_BF16;
-    switch (a.fmt) {
-        case FMT_BF16: bf ? launch_mma_path<FMT_BF16, ACT_BF16>(a, s) : launch_mma_path<FMT_BF16, ACT_FP32>(a, s); break;
-        case FMT_NVFP4: bf ? launch_mma_path<FMT_NVFP4, ACT_BF16>(a, s) : launch_mma_path<FMT_NVFP4, ACT_FP32>(a, s); break;
-        case FMT_MXFP4: bf ? launch_mma_path<FMT_MXFP4, ACT_BF16>(a, s) : launch_mma_path<FMT_MXFP4, ACT_FP32>(a, s); break;
-        default: return cudaErrorInvalidValue;
-    }
+    if (launches) *launches = n;
     return cudaGetLastError();
 }
 

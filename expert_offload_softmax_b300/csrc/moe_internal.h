@@ -101,6 +101,10 @@ struct CallArgs {
 // launchers (kernels.cu); all enqueue on `s` and return cudaGetLastError()
 cudaError_t launch_router(const CallArgs& a, cudaStream_t s);
 cudaError_t launch_cache(const CallArgs& a, cudaStream_t s);
-cudaError_t launch_experts(const CallArgs& a, cudaStream_t s);
+// launches the expert kernels; records ev_gu after the gate/up kernel and
+// ev_down after the down-projection kernel when they are non-null; *launches
+// receives the number of kernels launched
+cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
+                           int* launches);
 
 }  // namespace moe

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <deque>
 #include <cstring>
 #include <new>
 #include <string>
@@ -26,6 +27,14 @@ cudaError_t routing_set_attributes();
 using moe::BlobLayout;
 using moe::CallArgs;
 using moe::CallInfo;
+
+// CUDA events of one timed forward call
+struct TimedCall {
+    cudaEvent_t r0 = nullptr, r1 = nullptr, f0 = nullptr, f1 = nullptr, f2 = nullptr, f3 = nullptr;
+    cudaEvent_t c0 = nullptr, c1 = nullptr;
+    bool has_copy = false, has_combine = false;
+    uint64_t gu_bytes = 0, down_bytes = 0, combine_bytes = 0, copy_bytes = 0;
+};
 
 struct moe_handle {
     moe_model_desc d{};
@@ -56,6 +65,11 @@ struct moe_handle {
     // last call
     int last_T = 0;
     cudaStream_t last_stream = nullptr;
+    // timing
+    bool timing = false;
+    moe_timing_t tm{};
+    std::deque<TimedCall*> pending;
+    std::vector<TimedCall*> spare;
     // stats
     moe_stats_t st{};
     std::vector<moe_event> events;
@@ -224,6 +238,70 @@ void free_pool(moe_handle* h) {
     cudaFree(h->stamp); h->stamp = nullptr;
     cudaFree(h->clock); h->clock = nullptr;
     h->S = 0;
+}
+
+TimedCall* acquire_timed(moe_handle* h) {
+    if (!h->spare.empty()) {
+        TimedCall* t = h->spare.back();
+        h->spare.pop_back();
+        t->has_copy = t->has_combine = false;
+        return t;
+    }
+    TimedCall* t = new (std::nothrow) TimedCall();
+    if (!t) return nullptr;
+    cudaEvent_t* evs[8] = {&t->r0, &t->r1, &t->f0, &t->f1, &t->f2, &t->f3, &t->c0, &t->c1};
+    for (auto* e : evs)
+        if (cudaEventCreate(e) != cudaSuccess) return nullptr;
+    return t;
+}
+
+float elapsed(cudaEvent_t a, cudaEvent_t b) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) {
+        cudaGetLastError();
+        return 0.f;
+    }
+    return ms;
+}
+
+// folds finished timed calls into the totals; wait = block until all finished
+void harvest(moe_handle* h, bool wait) {
+    while (!h->pending.empty()) {
+        TimedCall* t = h->pending.front();
+        cudaEvent_t last = t->has_combine ? t->f3 : t->f2;
+        if (wait) {
+            cudaEventSynchronize(last);
+            if (t->has_copy) cudaEventSynchronize(t->c1);
+        } else if (cudaEventQuery(last) != cudaSuccess || (t->has_copy && cudaEventQuery(t->c1) != cudaSuccess)) {
+            cudaGetLastError();
+            break;
+        }
+        h->tm.calls++;
+        h->tm.route_ms += elapsed(t->r0, t->r1);
+        h->tm.gate_up_ms += elapsed(t->f0, t->f1);
+        h->tm.down_ms += elapsed(t->f1, t->f2);
+        if (t->has_combine) h->tm.combine_ms += elapsed(t->f2, t->f3);
+        if (t->has_copy) h->tm.copy_ms += elapsed(t->c0, t->c1);
+        h->tm.gate_up_bytes += t->gu_bytes;
+        h->tm.down_bytes += t->down_bytes;
+        h->tm.combine_bytes += t->combine_bytes;
+        h->tm.copy_bytes += t->copy_bytes;
+        h->pending.pop_front();
+        h->spare.push_back(t);
+    }
+}
+
+void free_timed(moe_handle* h) {
+    auto kill = [](TimedCall* t) {
+        cudaEvent_t evs[8] = {t->r0, t->r1, t->f0, t->f1, t->f2, t->f3, t->c0, t->c1};
+        for (auto e : evs)
+            if (e) cudaEventDestroy(e);
+        delete t;
+    };
+    for (auto* t : h->pending) kill(t);
+    for (auto* t : h->spare) kill(t);
+    h->pending.clear();
+    h->spare.clear();
 }
 
 }  // namespace
@@ -415,8 +493,17 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     a.shared_base = h->shared_dev ? h->shared_dev + static_cast<size_t>(layer_id) * h->d.num_shared * h->lay.bytes
                                   : nullptr;
     h->info_h->status = 1;
+    TimedCall* tc = nullptr;
+    if (h->timing) {
+        harvest(h, false);
+        tc = acquire_timed(h);
+        if (!tc) return fail(h, MOE_ERR_OOM, "timing events");
+        CK(h, cudaEventRecord(tc->r0, s));
+    }
     CK(h, moe::launch_router(a, s));
     CK(h, moe::launch_cache(a, s));
+    h->st.kernel_launches += (h->d.weight_fmt != moe::FMT_FP32 ? 1 : 0) + 3 + 1;
+    if (tc) CK(h, cudaEventRecord(tc->r1, s));
     CK(h, cudaEventRecord(h->ev_cache, s));
     CK(h, cudaEventSynchronize(h->ev_cache));
     volatile CallInfo* inf = h->info_h;
@@ -429,6 +516,10 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     if (inf->status != 0) return fail(h, MOE_ERR_CUDA, "cache kernel did not complete");
     const int nm = inf->n_miss, npm = inf->n_pf_miss;
     const size_t B = h->lay.bytes;
+    if (tc && nm + npm > 0) {
+        CK(h, cudaEventRecord(tc->c0, h->copy));
+        tc->has_copy = true;
+    }
     // demand misses: copy, then make the compute stream wait for them
     for (int i = 0; i < nm; ++i) {
         const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
@@ -454,7 +545,36 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         CK(h, cudaEventRecord(h->ev_prefetch, h->copy));
         h->prefetch_pending = true;
     }
-    CK(h, moe::launch_experts(a, s));
+    if (tc && tc->has_copy) CK(h, cudaEventRecord(tc->c1, h->copy));
+    if (tc) CK(h, cudaEventRecord(tc->f0, s));
+    int nl = 0;
+    CK(h, moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &nl));
+    h->st.kernel_launches += nl;
+    if (tc) {
+        tc->has_combine = nl == 3;
+        if (tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
+        // algorithmic bytes of this call
+        const uint64_t H = h->d.hidden, I = h->d.inter, k = h->d.top_k, ns = h->d.num_shared;
+        const uint64_t na = static_cast<uint64_t>(inf->n_uniq) + ns;
+        const uint64_t rows = static_cast<uint64_t>(T) * (k + ns);
+        const uint64_t ea = h->d.act_dtype == moe::ACT_BF16 ? 2 : 4;
+        const uint64_t he = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
+        uint64_t wgu, wd;
+        switch (h->d.weight_fmt) {
+            case moe::FMT_FP32: wgu = 2 * I * H * 4; wd = H * I * 4; break;
+            case moe::FMT_BF16: wgu = 2 * I * H * 2; wd = H * I * 2; break;
+            default: {
+                const uint64_t blk = h->d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
+                wgu = 2 * I * H / 2 + 2 * I * H / blk;
+                wd = H * I / 2 + H * I / blk;
+            }
+        }
+        tc->gu_bytes = na * wgu + T * H * ea + rows * I * he;
+        tc->down_bytes = na * wd + rows * I * he + (tc->has_combine ? rows * H * 2 : T * H * ea);
+        tc->combine_bytes = tc->has_combine ? rows * H * 2 + T * H * ea : 0;
+        tc->copy_bytes = static_cast<uint64_t>(nm + npm) * B;
+        h->pending.push_back(tc);
+    }
     // bookkeeping
     h->st.calls++;
     (decode ? h->st.decode_calls : h->st.prefill_calls)++;
@@ -473,6 +593,23 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
             h->events.push_back(ev);
         }
     }
+    return MOE_OK;
+}
+
+int moe_timing_enable(moe_handle* h, int enable) {
+    if (!h) return MOE_ERR_INVALID;
+    CK(h, cudaSetDevice(h->d.device));
+    harvest(h, true);
+    h->tm = moe_timing_t{};
+    h->timing = enable != 0;
+    return MOE_OK;
+}
+
+int moe_timing(moe_handle* h, moe_timing_t* t) {
+    if (!h || !t) return MOE_ERR_INVALID;
+    CK(h, cudaSetDevice(h->d.device));
+    harvest(h, true);
+    *t = h->tm;
     return MOE_OK;
 }
 
@@ -532,6 +669,7 @@ void moe_destroy(moe_handle* h) {
     if (!h) return;
     cudaSetDevice(h->d.device);
     cudaDeviceSynchronize();
+    free_timed(h);
     free_pool(h);
     for (auto* b : h->bank)
         if (b) cudaFreeHost(b);

@@ -107,7 +107,24 @@ typedef struct moe_stats_t {
     uint64_t evictions;
     uint64_t copies_h2d, bytes_h2d;           /* expert copies issued */
     uint64_t device_errors;
+    uint64_t kernel_launches;                 /* CUDA kernels this library launched */
 } moe_stats_t;
+
+/* Per-kernel device time and algorithmic bytes, measured with CUDA events
+ * recorded around the library's own launches on the launching stream (and
+ * around each call's copies on the copy stream) while timing is enabled.
+ * Algorithmic bytes count what each step must move at least once: the active
+ * experts' weights and block scales, the activations read and the results
+ * written. */
+typedef struct moe_timing_t {
+    uint64_t calls;
+    double route_ms;      /* activation prep, router, top-k, permutation, cache kernels */
+    double gate_up_ms;    /* gate/up projection + SwiGLU */
+    double down_ms;       /* down projection (+ combine, decode) */
+    double combine_ms;    /* prefill combine */
+    double copy_ms;       /* expert copies (misses and prefetch) on the copy stream */
+    uint64_t gate_up_bytes, down_bytes, combine_bytes, copy_bytes;
+} moe_timing_t;
 
 typedef struct moe_event {
     int32_t layer, expert, hit, slot, evicted_key, prefetch;
@@ -153,6 +170,13 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
 /* Cumulative counters since moe_init (or the last moe_stats_reset). */
 int moe_stats(moe_handle* h, moe_stats_t* s);
 int moe_stats_reset(moe_handle* h);
+
+/* enable != 0: start timing the following forward calls (accumulators reset);
+ * enable == 0: stop. */
+int moe_timing_enable(moe_handle* h, int enable);
+
+/* Waits for all timed work to finish and returns the accumulated totals. */
+int moe_timing(moe_handle* h, moe_timing_t* t);
 
 /* Drains up to cap logged events (MOE_CACHE_LOG_EVENTS) into buf, in the order
  * the cache served them; *n receives the number written. */
