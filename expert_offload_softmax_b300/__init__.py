@@ -32,7 +32,8 @@ MOE_CACHE_LOG_EVENTS = 2
 # every symbol the header declares
 EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward",
            "moe_stats", "moe_stats_reset", "moe_stats_events", "moe_debug_routing", "moe_debug_lru_table",
-           "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing"]
+           "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing", "moe_route_topk_noalloc"]
+MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
 
 
 class moe_model_desc(ctypes.Structure):
@@ -104,6 +105,7 @@ def load(path: str | None = None):
     lib.moe_stats_events.argtypes = [vp, P(moe_event), i32, P(i32)]
     lib.moe_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp, P(ctypes.c_int32)]
     lib.moe_debug_lru_table.argtypes = [vp, vp]
+    lib.moe_route_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.moe_last_error.argtypes = [vp]
     lib.moe_last_error.restype = ctypes.c_char_p
     lib.moe_destroy.argtypes = [vp]
@@ -216,6 +218,15 @@ def moe_debug_lru_table(h: int, L: int, E: int) -> np.ndarray:
     t = np.empty(L * E, np.int32)
     _check(h, load().moe_debug_lru_table(h, _np_ptr(t)))
     return t
+
+
+def moe_route_topk_noalloc(hidden: int, router_w: int, T: int, E: int, H: int, k: int, act_dtype: int,
+                           topk_idx: int, gates: int, stream: int | None = None) -> None:
+    """Router top-k into caller-provided device outputs; allocates nothing (for
+    callers that cannot call cudaMalloc). Pointers are device addresses."""
+    rc = load().moe_route_topk_noalloc(hidden, router_w, T, E, H, k, act_dtype, topk_idx, gates, stream)
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_route_topk_noalloc failed")
 
 
 def moe_last_error(h: int) -> str:

@@ -191,6 +191,28 @@ int moe_debug_routing(moe_handle* h, int32_t* topk_idx, float* gates, int32_t* p
 /* Host copy of the LRU table [L*E] (slot or -1) after the last call. */
 int moe_debug_lru_table(moe_handle* h, int32_t* table);
 
+/* Router top-k that allocates nothing (the pages describe no counterpart: it
+ * exists for callers that cannot call cudaMalloc, e.g. a plugin whose host
+ * framework's memory pool owns all device memory, or a path that must not
+ * allocate; moe_init allocates, so those callers cannot create a handle).
+ * Computes, for T tokens, the router logits in the same fixed summation order
+ * as moe_layer_forward, the softmax, the top-k experts (larger logit first,
+ * ties to the lower index) and the renormalised gates.
+ *  hidden [T, H], router_w [E, H]: device, act_dtype (MOE_ACT_*), 16-byte aligned
+ *  topk_idx [T*k] int32, gates [T*k] float32: device outputs, written on stream
+ *  stream: a cudaStream_t (NULL = legacy default stream), on the current device
+ * Scratch: a file-scope device array of MOE_ROUTE_NOALLOC_MAX_LOGITS floats
+ * (4 MiB, held by every GPU that loads the library until exit); T*E above it,
+ * E > 1024, k > min(E, 32), H not a positive multiple of 8 or too large for the
+ * shared-memory tile give MOE_ERR_INVALID. Calls no allocator. The first call
+ * on a device, with that device current, looks the array's address up
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make it
+ * before any stream capture. All calls share the array and it keeps the last
+ * call's contents; calls whose work overlaps on the GPU race on it. */
+#define MOE_ROUTE_NOALLOC_MAX_LOGITS (1 << 20)
+int moe_route_topk_noalloc(const void* hidden, const void* router_w, int T, int E, int H, int k, int act_dtype,
+                           int32_t* topk_idx, float* gates, void* stream);
+
 const char* moe_last_error(const moe_handle* h);
 
 void moe_destroy(moe_handle* h);
