@@ -183,6 +183,8 @@ def run_ours(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     shape, T, frac, flags, L = WORKLOADS[args.workload]
+    if args.layers:
+        L = min(L, args.layers)
     cap_shape = synth.Shape("cap", L=L, E=shape.E, k=shape.k, H=shape.H, I=shape.I, fmt=shape.fmt, act=shape.act)
     S = synth.capacity_slots(cap_shape, frac)
     t_load = time.time()
@@ -399,6 +401,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0, help="run only the first N layers of the stack (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

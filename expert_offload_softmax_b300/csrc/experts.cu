@@ -541,8 +541,20 @@ static int launch_mma_path(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
 }
 
 cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
-                           int* launches) {
+                           const UmmaMaps* maps, int num_sms, int* launches) {
     int n = 0;
+    if (prefill_uses_umma(a.fmt, a.T)) {
+        if (!maps || !maps->have_pool || !maps->have_io) return cudaErrorInvalidValue;
+        cudaError_t e = launch_prefill_umma(a, *maps, num_sms, s, ev_gu, &n);
+        if (e != cudaSuccess) return e;
+        if (ev_down) cudaEventRecord(ev_down, s);
+        const size_t n8 = static_cast<size_t>(a.T) * a.H / 8;
+        const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(num_sms) * 16));
+        if (a.act == ACT_BF16) k_combine<ACT_BF16><<<blocks, 256, 0, s>>>(a);
+        else k_combine<ACT_FP32><<<blocks, 256, 0, s>>>(a);
+        if (launches) *launches = n + 1;
+        return cudaGetLastError();
+    }
     if (a.fmt == FMT_FP32) {
         const int max_active = min(a.E, a.T * a.k) + a.n_shared;
         const int gx = min((a.T * a.I + 255) / 256, 64);

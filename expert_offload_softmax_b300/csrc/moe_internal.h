@@ -44,6 +44,7 @@ struct CallInfo {
     int32_t n_hit, n_miss;   // demand batch
     int32_t n_pf, n_pf_hit, n_pf_miss;  // prefetch batch (n_pf = 0: none)
     int32_t n_events;
+    int32_t dev_err;         // sticky device error word at the time of this call (0 = none)
     // misses to copy: demand misses first, then prefetch misses
     int32_t miss_layer[2 * kMaxExperts];
     int32_t miss_expert[2 * kMaxExperts];
@@ -83,6 +84,9 @@ struct CallArgs {
     const uint8_t** act_ptr;  // [E + n_shared] blob address
     int32_t* e2u;          // [E] active index of routed expert e, or -1
     int32_t* tok_row;      // [(E + n_shared) * 8] decode: h row of (active u, token t) or -1
+    int32_t* act_slot;     // [E + n_shared]  pool slot of the active expert; shared: -(1 + layer*n_shared + s)
+    void* xperm;           // [T*k + T*n_shared][H] bf16 gathered activations, device K-order (prefill, BF16)
+    int32_t* dev_err;      // [1] sticky device error word (bounded waits that gave up)
     int32_t* n_uniq;       // [1]
     int32_t* n_active;     // [1]
     void* hbuf;            // [rows][I] intermediate (f16 / bf16 / f32)
@@ -98,13 +102,46 @@ struct CallArgs {
     CallInfo* info;        // mapped host memory (device pointer)
 };
 
+// device error codes written to CallArgs::dev_err
+enum DevErr {
+    DEVERR_NONE = 0,
+    MOE_DEVERR_TIMEOUT_PRODUCER = 1,
+    MOE_DEVERR_TIMEOUT_MMA = 2,
+    MOE_DEVERR_TIMEOUT_EPILOGUE = 3
+};
+
+// an opaque CUtensorMap (128 bytes, 64-byte aligned)
+struct alignas(64) UmmaMap {
+    unsigned char bytes[128];
+};
+
+// TMA descriptors of the prefill tensor-core path: the pool's gate/up and down
+// regions (3-D: K, rows, slot), the resident shared experts (same), the gathered
+// activations and the intermediate h (2-D: K, rows)
+struct UmmaMaps {
+    UmmaMap pool_gu, pool_d, shared_gu, shared_d, x, h;
+    bool have_pool = false, have_io = false;
+};
+
+bool umma_map_2d(UmmaMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool umma_map_3d(UmmaMap* m, const void* base, uint64_t slots, uint64_t slot_bytes, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
+cudaError_t umma_set_attributes();
+// gather + gate/up + down on the tensor cores (prefill, BF16 weights); records
+// ev_gu after the gate/up GEMM when non-null
+cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s,
+                                cudaEvent_t ev_gu, int* launches);
+
 // launchers (kernels.cu); all enqueue on `s` and return cudaGetLastError()
 cudaError_t launch_router(const CallArgs& a, cudaStream_t s);
 cudaError_t launch_cache(const CallArgs& a, cudaStream_t s);
 // launches the expert kernels; records ev_gu after the gate/up kernel and
 // ev_down after the down-projection kernel when they are non-null; *launches
-// receives the number of kernels launched
+// receives the number of kernels launched. Prefill with BF16 weights takes the
+// tensor-core path when `maps` holds valid descriptors.
 cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
-                           int* launches);
+                           const UmmaMaps* maps, int num_sms, int* launches);
+// true when a prefill call of this shape takes the tensor-core path
+inline bool prefill_uses_umma(int fmt, int T) { return fmt == FMT_BF16 && T > kDecodeMaxT; }
 
 }  // namespace moe

@@ -1,0 +1,552 @@
+// Prefill expert GEMMs of the routed MoE layer on the 5th-generation tensor
+// cores: tcgen05.mma (kind::f16, BF16 operands, fp32 accumulators in tensor
+// memory), operand tiles staged by TMA into 128-byte-swizzled shared memory,
+// one persistent CTA per SM with warp-specialised roles.
+//
+// Prefill is where the layer is a real dense contraction: with T tokens and
+// top-k routing every active expert sees about T*k/E tokens (128 at T=4096,
+// E=256, k=8), so each expert's weights are streamed once and reused across
+// its tokens. The pages' prefill paragraph (freetoken.wiki architecture page:
+// whole-layer double buffering, the next layer's experts streaming over PCIe
+// while the current layer computes) is served by the host runtime; these
+// kernels are the "current layer computes" part.
+//
+// Swap-AB: the weight rows are the MMA's M = 128 operand (A), the tokens routed
+// to one expert are N (B), K is the projection's input dimension. Both operands
+// are K-major; the K permutation the library stores weights in (see
+// moe_internal.h) is applied to the activations too, so every dot product is
+// over the same pairs.
+//
+//  gate/up: per tile, 128 intermediate units x up to 128 tokens; two
+//           accumulators (gate rows, up rows of the same units); the epilogue
+//           applies SwiGLU and the routing gate and writes h (bf16).
+//  down:    per tile, 128 output rows x up to 128 tokens; the epilogue writes
+//           the expert's output rows Y (bf16), combined later per token.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2-5 = epilogue (TMEM lane quarter = warp % 4). Every wait is
+// bounded by %globaltimer; on timeout the kernel records an error, lets its
+// copies and MMAs in flight finish (bounded again), frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;  // weight rows per accumulator (MMA M)
+constexpr int BN = 128;  // tokens per tile (MMA N at most)
+constexpr int BK = 64;   // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand tile
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+enum { MODE_GU = 0, MODE_DOWN = 1 };
+
+template <int MODE>
+struct Cfg {
+    static constexpr int kATiles = MODE == MODE_GU ? 2 : 1;           // gate + up, or down
+    static constexpr int kStageBytes = (kATiles + 1) * kTileBytes;   // A tiles + B tile
+    static constexpr int kStages = MODE == MODE_GU ? 4 : 6;
+    static constexpr int kAccCols = kATiles * BN;                    // TMEM columns per accumulator set
+    static constexpr int kTmemCols = 2 * kAccCols;                   // double-buffered: 512 / 256
+    static constexpr int kSmem = kStages * kStageBytes + 1024;       // + alignment slack
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of parity `parity` to complete. Gives up (false) when
+// another role of this CTA has aborted or after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        if (mbar_test(b, parity)) return true;
+        if (*abort_flag) return false;
+        if (gtimer() - t0 > kWaitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused when swizzled)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: next 8-row atom
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: BF16 x BF16 -> F32, both operands K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+
+// this thread's TMEM lane, 32 consecutive fp32 columns starting at taddr
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// position of intermediate unit i in the library's K order
+__device__ __forceinline__ int kpos(int i) {
+    const int w = i & 127, s = w >> 4, q = (w >> 2) & 3, e = w & 3;
+    return (i & ~127) + 32 * q + 4 * s + e;
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct TileSched {
+    int32_t start[kMaxExperts + 2];  // first tile of active expert u; start[n_active] = total
+};
+
+__device__ __forceinline__ int find_expert(const TileSched& ts, int na, int t) {
+    int lo = 0, hi = na - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ts.start[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_umma_grouped(const __grid_constant__ CUtensorMap map_pool, const __grid_constant__ CUtensorMap map_shared,
+                   const __grid_constant__ CUtensorMap map_b, CallArgs a) {
+    using C = Cfg<MODE>;
+    extern __shared__ unsigned char dyn_raw[];
+    __shared__ TileSched ts;
+    __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+    const int na = *a.n_active;
+    const int n_mt = MODE == MODE_GU ? a.I / BM : a.H / BM;
+    const int n_kb = MODE == MODE_GU ? a.H / BK : a.I / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_tfull[s], 1);
+            mbar_init(&bar_tempty[s], 128);
+        }
+        mbar_init(&bar_drain, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s_tmem)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // tile schedule: active expert u owns n_mt * ceil(cnt_u / BN) tiles, token tiles fastest
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < na; base += 32) {
+            const int u = base + lane;
+            const int v = u < na ? n_mt * ((a.act_cnt[u] + BN - 1) / BN) : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (u < na) ts.start[u] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) ts.start[na] = carry;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const int total = ts.start[na];
+    volatile int* abort_flag = &s_abort;
+
+    auto fail = [&](int code) {
+        *abort_flag = 1;
+        atomicExch(a.dev_err, code);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[C::kStages];
+#pragma unroll
+            for (int s = 0; s < C::kStages; ++s) issued_phase[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int u = find_expert(ts, na, t);
+                const int local = t - ts.start[u];
+                const int n_nt = (a.act_cnt[u] + BN - 1) / BN;
+                const int mt = local / n_nt, nt = local % n_nt;
+                const int sl = a.act_slot[u];
+                const CUtensorMap* mA = sl >= 0 ? &map_pool : &map_shared;
+                const int z = sl >= 0 ? sl : -sl - 1;
+                const int brow = a.act_row0[u] + nt * BN;
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag)) {
+                        fail(MOE_DEVERR_TIMEOUT_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* st = smem + stage * C::kStageBytes;
+                    mbar_expect_tx(&bar_full[stage], C::kStageBytes);
+                    if constexpr (MODE == MODE_GU) {
+                        // gate rows of units [128 mt, 128 mt + 128) sit in two 64-row blocks
+                        // 128 rows apart; the up rows follow each block
+                        const int r0 = (mt * BM / 64) * 128;
+                        tma_3d(st, mA, &bar_full[stage], kb * BK, r0, z);
+                        tma_3d(st + kTileBytes / 2, mA, &bar_full[stage], kb * BK, r0 + 128, z);
+                        tma_3d(st + kTileBytes, mA, &bar_full[stage], kb * BK, r0 + 64, z);
+                        tma_3d(st + kTileBytes + kTileBytes / 2, mA, &bar_full[stage], kb * BK, r0 + 192, z);
+                    } else {
+                        tma_3d(st, mA, &bar_full[stage], kb * BK, mt * BM, z);
+                    }
+                    tma_2d(st + C::kATiles * kTileBytes, &map_b, &bar_full[stage], kb * BK, brow);
+                    issued_phase[stage] = static_cast<int>(phase);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA can exit
+                for (int s = 0; s < C::kStages; ++s)
+                    if (issued_phase[s] >= 0) {
+                        const uint64_t t0 = gtimer();
+                        while (!mbar_test(&bar_full[s], static_cast<uint32_t>(issued_phase[s])) &&
+                               gtimer() - t0 < kWaitNs) {
+                        }
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const int u = find_expert(ts, na, t);
+                const int local = t - ts.start[u];
+                const int n_nt = (a.act_cnt[u] + BN - 1) / BN;
+                const int nt = local % n_nt;
+                const int rows = min(BN, a.act_cnt[u] - nt * BN);
+                const uint32_t idesc = idesc_bf16(BM, (rows + 15) & ~15);
+                const int acc = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!mbar_wait(&bar_tempty[acc], aph ^ 1u, abort_flag)) {
+                    fail(MOE_DEVERR_TIMEOUT_MMA);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem + acc * C::kAccCols;
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&bar_full[stage], phase, abort_flag)) {
+                        fail(MOE_DEVERR_TIMEOUT_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = su32(smem + stage * C::kStageBytes);
+                    const uint32_t sb = sa + C::kATiles * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t db = sdesc(sb + 32 * kk);
+                        const uint32_t accum = (kb | kk) != 0;
+                        umma_bf16(d0, sdesc(sa + 32 * kk), db, idesc, accum);
+                        if constexpr (MODE == MODE_GU) umma_bf16(d0 + BN, sdesc(sa + kTileBytes + 32 * kk), db, idesc, accum);
+                    }
+                    umma_commit(&bar_empty[stage]);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&bar_tfull[acc]);
+            }
+            // every MMA issued by this thread has completed once bar_drain flips
+            umma_commit(&bar_drain);
+            const uint64_t t0 = gtimer();
+            while (!mbar_test(&bar_drain, 0) && gtimer() - t0 < kWaitNs) {
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2-5)
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const int u = find_expert(ts, na, t);
+            const int local = t - ts.start[u];
+            const int cnt = a.act_cnt[u];
+            const int n_nt = (cnt + BN - 1) / BN;
+            const int mt = local / n_nt, nt = local % n_nt;
+            const int rows = min(BN, cnt - nt * BN);
+            const int r0 = a.act_row0[u] + nt * BN;
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(&bar_tfull[acc], aph, abort_flag)) {
+                fail(MOE_DEVERR_TIMEOUT_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::kAccCols;
+            float gsc0 = 1.0f, gsc1 = 1.0f;
+            if (a.fmt == FMT_NVFP4) {
+                const float* g = reinterpret_cast<const float*>(a.act_ptr[u] + a.lay.gsc);
+                gsc0 = MODE == MODE_GU ? g[0] : g[2];
+                gsc1 = g[1];
+            }
+            if constexpr (MODE == MODE_GU) {
+                const int unit = mt * BM + row_in_tile;
+                __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(a.hbuf) + kpos(unit);
+                for (int c0 = 0; c0 < rows; c0 += 32) {
+                    float g[32], up[32];
+                    tmem_ld32(tbase + c0, g);
+                    tmem_ld32(tbase + BN + c0, up);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < rows) {
+                            const int r = r0 + c0 + j;
+                            const float gv = g[j] * gsc0;
+                            const float act = a.mode == 1 ? gv : gv / (1.0f + expf(-gv));
+                            hrow[static_cast<size_t>(r) * a.I] = __float2bfloat16_rn(act * (up[j] * gsc1) * a.row_gate[r]);
+                        }
+                    }
+                }
+            } else {
+                const int hr = mt * BM + row_in_tile;
+                __nv_bfloat16* ycol = reinterpret_cast<__nv_bfloat16*>(a.ybuf) + hr;
+                for (int c0 = 0; c0 < rows; c0 += 32) {
+                    float y[32];
+                    tmem_ld32(tbase + c0, y);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < rows) ycol[static_cast<size_t>(r0 + c0 + j) * a.H] = __float2bfloat16_rn(y[j] * gsc0);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+    }
+}
+
+// X_perm[r, :] = hidden[row_tok[r], :] as bf16 in the library's K order
+template <int ACT>
+__global__ void __launch_bounds__(256) k_gather_x(CallArgs a, int rows) {
+    const int H = a.H;
+    const size_t n8 = static_cast<size_t>(rows) * H / 8;
+    for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n8;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(idx / (H / 8));
+        const int p = 8 * static_cast<int>(idx % (H / 8));  // destination position
+        const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
+        const size_t src = static_cast<size_t>(a.row_tok[r]) * H + 128 * j + 16 * s + 4 * q;
+        uint32_t o[4];
+        if constexpr (ACT == ACT_BF16) {
+            const uint16_t* x = reinterpret_cast<const uint16_t*>(a.hidden);
+            const uint2 lo = *reinterpret_cast<const uint2*>(x + src);
+            const uint2 hi = *reinterpret_cast<const uint2*>(x + src + 16);
+            o[0] = lo.x; o[1] = lo.y; o[2] = hi.x; o[3] = hi.y;
+        } else {
+            const float* x = reinterpret_cast<const float*>(a.hidden);
+            const float4 lo = *reinterpret_cast<const float4*>(x + src);
+            const float4 hi = *reinterpret_cast<const float4*>(x + src + 16);
+            const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                o[i] = *reinterpret_cast<uint32_t*>(&b);
+            }
+        }
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.xperm) + static_cast<size_t>(r) * H + p) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+// bf16 [rows][cols] row-major, box = box_rows x 64 columns, 128-byte swizzle
+bool umma_map_2d(UmmaMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn || !base || rows == 0) return false;
+    CUtensorMap* t = reinterpret_cast<CUtensorMap*>(m->bytes);
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [slots][rows][cols], slot stride in bytes; box = box_rows x 64 columns x 1 slot
+bool umma_map_3d(UmmaMap* m, const void* base, uint64_t slots, uint64_t slot_bytes, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn || !base || slots == 0) return false;
+    CUtensorMap* t = reinterpret_cast<CUtensorMap*>(m->bytes);
+    const cuuint64_t dims[3] = {cols, rows, slots};
+    const cuuint64_t strides[2] = {cols * 2, slot_bytes};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t umma_set_attributes() {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<MODE_GU>::kSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<MODE_DOWN>::kSmem)))
+        return e;
+    return cudaSuccess;
+}
+
+static CUtensorMap as_map(const UmmaMap& m) {
+    CUtensorMap t;
+    std::memcpy(&t, m.bytes, sizeof(t));
+    return t;
+}
+
+// gather, gate/up + SwiGLU, down; the combine is launched by the caller
+cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s,
+                                cudaEvent_t ev_gu, int* launches) {
+    const int rows = a.T * (a.k + a.n_shared);
+    const size_t n8 = static_cast<size_t>(rows) * a.H / 8;
+    const int gb = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(num_sms) * 16));
+    if (a.act == ACT_BF16) k_gather_x<ACT_BF16><<<gb, 256, 0, s>>>(a, rows);
+    else k_gather_x<ACT_FP32><<<gb, 256, 0, s>>>(a, rows);
+    k_umma_grouped<MODE_GU><<<num_sms, kThreads, Cfg<MODE_GU>::kSmem, s>>>(as_map(maps.pool_gu), as_map(maps.shared_gu),
+                                                                          as_map(maps.x), a);
+    if (ev_gu) cudaEventRecord(ev_gu, s);
+    k_umma_grouped<MODE_DOWN><<<num_sms, kThreads, Cfg<MODE_DOWN>::kSmem, s>>>(as_map(maps.pool_d),
+                                                                              as_map(maps.shared_d), as_map(maps.h), a);
+    if (launches) *launches = 3;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

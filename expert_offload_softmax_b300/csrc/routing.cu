@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kLruThreads) k_lru(CallArgs a) {
             info->n_uniq = nu;
             info->n_hit = info->n_miss = info->n_pf = info->n_pf_hit = info->n_pf_miss = 0;
             info->n_events = 0;
+            info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
             *a.n_active = 0;
         }
         return;
@@ -488,6 +489,7 @@ __global__ void __launch_bounds__(kLruThreads) k_lru(CallArgs a) {
     for (int p = tid; p < nu; p += blockDim.x) {
         const int s = sm.member_slot[p];
         a.act_ptr[p] = a.pool + static_cast<size_t>(s) * a.lay.bytes;
+        a.act_slot[p] = s;
         info->ev_layer[p] = a.layer;
         info->ev_expert[p] = s_members[p];
         info->ev_hit[p] = sm.member_old[p] == -1 && 0;  // set below
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kLruThreads) k_lru(CallArgs a) {
             a.act_row0[u] = T * k + s * T;
             a.act_cnt[u] = T;
             a.act_ptr[u] = a.shared_base + static_cast<size_t>(s) * a.lay.bytes;
+            a.act_slot[u] = -(1 + a.layer * a.n_shared + s);
         }
         for (int t = tid; t < T; t += blockDim.x) {
             a.row_tok[T * k + s * T + t] = t;
@@ -559,6 +562,7 @@ __global__ void __launch_bounds__(kLruThreads) k_lru(CallArgs a) {
         info->n_pf_hit = n_pf - m_pf;
         info->n_pf_miss = m_pf;
         info->n_events = nu + n_pf;
+        info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
         __threadfence_system();
         info->status = 0;
     }

@@ -55,6 +55,9 @@ struct moe_handle {
     unsigned long long* clock = nullptr;
     // scratch
     void* scratch = nullptr;
+    // prefill tensor-core path: TMA descriptors, SM count
+    moe::UmmaMaps maps{};
+    int num_sms = 148;
     CallArgs base{};
     CallInfo* info_h = nullptr;
     CallInfo* info_d = nullptr;
@@ -332,6 +335,9 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     cudaError_t e = cudaSetDevice(desc->device);
     if (e != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::routing_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (moe::umma_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, desc->device) != cudaSuccess)
+        return bail(MOE_ERR_CUDA);
     const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared, k = h->d.top_k;
     const size_t H = h->d.hidden, I = h->d.inter, Tm = h->max_tokens;
     h->bank.assign(L, nullptr);
@@ -343,6 +349,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     // scratch carve-up
     const size_t rows = Tm * (k + ns);
     const size_t hes = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
+    const bool umma = moe::prefill_uses_umma(h->d.weight_fmt, static_cast<int>(Tm));
     struct Part { size_t bytes; void** dst; };
     CallArgs& a = h->base;
     std::vector<Part> parts = {
@@ -362,6 +369,9 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E + ns) * 8, reinterpret_cast<void**>(&a.act_ptr)},
         {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.e2u)},
         {static_cast<size_t>(E + ns) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.tok_row)},
+        {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_slot)},
+        {umma ? rows * H * 2 : 16, &a.xperm},
+        {4, reinterpret_cast<void**>(&a.dev_err)},
         {4, reinterpret_cast<void**>(&a.n_uniq)},
         {4, reinterpret_cast<void**>(&a.n_active)},
         {rows * I * hes, &a.hbuf},
@@ -375,6 +385,18 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     for (auto& p : parts) {
         *p.dst = static_cast<uint8_t*>(h->scratch) + off;
         off += align_up(p.bytes, 256);
+    }
+    if (umma) {
+        // TMA descriptors over the gathered activations, h, and the resident shared experts
+        bool ok = moe::umma_map_2d(&h->maps.x, a.xperm, rows, H, 128) && moe::umma_map_2d(&h->maps.h, a.hbuf, rows, I, 128);
+        if (ok && ns > 0) {
+            ok = moe::umma_map_3d(&h->maps.shared_gu, h->shared_dev + h->lay.gu, static_cast<uint64_t>(L) * ns,
+                                  h->lay.bytes, 2 * I, H, 64) &&
+                 moe::umma_map_3d(&h->maps.shared_d, h->shared_dev + h->lay.d, static_cast<uint64_t>(L) * ns,
+                                  h->lay.bytes, H, I, 128);
+        }
+        if (!ok) return bail(MOE_ERR_CUDA);
+        h->maps.have_io = true;
     }
     if (cudaHostAlloc(reinterpret_cast<void**>(&h->info_h), sizeof(CallInfo), cudaHostAllocMapped) != cudaSuccess)
         return bail(MOE_ERR_OOM);
@@ -450,7 +472,22 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     CK(h, cudaMemset(h->owner, 0xFF, S * 4));
     CK(h, cudaMemset(h->stamp, 0, S * 8));
     CK(h, cudaMemset(h->clock, 0, 8));
+    CK(h, cudaMemset(h->base.dev_err, 0, 4));
     CK(h, cudaDeviceSynchronize());
+    h->maps.have_pool = false;
+    if (h->maps.have_io) {
+        const uint64_t H = h->d.hidden, I = h->d.inter;
+        if (!moe::umma_map_3d(&h->maps.pool_gu, h->pool + h->lay.gu, S, h->lay.bytes, 2 * I, H, 64) ||
+            !moe::umma_map_3d(&h->maps.pool_d, h->pool + h->lay.d, S, h->lay.bytes, H, I, 128)) {
+            free_pool(h);
+            return fail(h, MOE_ERR_CUDA, "TMA descriptor encoding failed");
+        }
+        if (h->d.num_shared == 0) {
+            h->maps.shared_gu = h->maps.pool_gu;  // never selected: no shared experts
+            h->maps.shared_d = h->maps.pool_d;
+        }
+        h->maps.have_pool = true;
+    }
     h->S = capacity_slots;
     h->flags = flags;
     h->prefetch_pending = false;
@@ -514,6 +551,11 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         return fail(h, MOE_ERR_CAPACITY, "the layer's experts do not fit in the expert pool");
     }
     if (inf->status != 0) return fail(h, MOE_ERR_CUDA, "cache kernel did not complete");
+    if (inf->dev_err != 0) {
+        h->st.device_errors++;
+        return fail(h, MOE_ERR_TIMEOUT, "an expert kernel gave up a bounded wait (device error " +
+                                            std::to_string(inf->dev_err) + "); call moe_cache_config to reset");
+    }
     const int nm = inf->n_miss, npm = inf->n_pf_miss;
     const size_t B = h->lay.bytes;
     if (tc && nm + npm > 0) {
@@ -548,10 +590,10 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     if (tc && tc->has_copy) CK(h, cudaEventRecord(tc->c1, h->copy));
     if (tc) CK(h, cudaEventRecord(tc->f0, s));
     int nl = 0;
-    CK(h, moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &nl));
+    CK(h, moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &h->maps, h->num_sms, &nl));
     h->st.kernel_launches += nl;
     if (tc) {
-        tc->has_combine = nl == 3;
+        tc->has_combine = !decode && h->d.weight_fmt != moe::FMT_FP32;
         if (tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
         // algorithmic bytes of this call
         const uint64_t H = h->d.hidden, I = h->d.inter, k = h->d.top_k, ns = h->d.num_shared;

@@ -67,6 +67,22 @@ def test_small_prefill_all_formats(fmt, T):
     _run(s, 12, 3, 20, calls, flags=0)
 
 
+def test_prefill_bf16_tensor_core_multi_tile():
+    """BF16 prefill takes the tcgen05 path: 8 experts x top-2 over 1000 tokens
+    puts ~250 tokens on each expert (two 128-token tiles, ragged second tile),
+    H=640 gives 10 K-blocks of 64 and 5 down-projection row tiles, I=384 gives
+    three 128-unit gate/up tiles."""
+    s = synth.Shape("umma", L=2, E=8, k=2, H=640, I=384, fmt=synth.FMT_BF16, act=synth.ACT_BF16)
+    _run(s, 22, 2, 16, [(0, 1000, 0), (1, 130, 1), (0, 17, 2)], max_tokens=1000)
+
+
+def test_prefill_bf16_tensor_core_shared_expert_fp32_act():
+    """tcgen05 prefill with an always-on shared expert (its weights resident
+    outside the pool) and fp32 activations converted to bf16 in the gather."""
+    s = synth.Shape("umma-shared", L=2, E=16, k=4, H=256, I=256, fmt=synth.FMT_BF16, act=synth.ACT_FP32, shared=1)
+    _run(s, 23, 2, 32, [(0, 300, 0), (1, 41, 0), (1, 2, 1)], max_tokens=512)
+
+
 def test_prefill_prefetch_next_layer():
     s = synth.Shape("small", L=4, E=16, k=4, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
     calls = [(l, 64, 0) for l in range(4)] + [(l, 64, 1) for l in range(4)]
