@@ -19,70 +19,10 @@
 
 #include <algorithm>
 
+#include "mma_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
-
-// --------------------------------------------------------------------------
-// register-level helpers
-// --------------------------------------------------------------------------
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                        const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};\n"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                         const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};\n"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
-}
-
-// four bytes of packed E2M1 pairs -> four f16x2 (low nibble -> low half)
-__device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
-    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-        : "r"(w));
-}
-
-// eight E4M3 bytes -> eight floats (byte i -> o[i])
-__device__ __forceinline__ void e4m3x8_to_f32(uint2 v, float (&o)[8]) {
-    uint32_t h[4];
-    asm("{\n.reg .b16 l0, h0, l1, h1;\n"
-        "mov.b32 {l0, h0}, %4;\n"
-        "mov.b32 {l1, h1}, %5;\n"
-        "cvt.rn.f16x2.e4m3x2 %0, l0;\n"
-        "cvt.rn.f16x2.e4m3x2 %1, h0;\n"
-        "cvt.rn.f16x2.e4m3x2 %2, l1;\n"
-        "cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(v.x), "r"(v.y));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __half2 x = *reinterpret_cast<__half2*>(&h[i]);
-        o[2 * i] = __low2float(x);
-        o[2 * i + 1] = __high2float(x);
-    }
-}
-
-// E8M0 byte -> 2^(b-127) as a float (b = 0 gives 2^-127)
-__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
-    return __uint_as_float(b == 0 ? 0x00400000u : (b << 23));
-}
 
 // per-step block scales of one row for one 128-element group
 template <int FMT>
@@ -163,14 +103,6 @@ __device__ __forceinline__ void load_b(const uint16_t* p, uint32_t (&b)[16]) {
     }
 }
 
-// position of intermediate unit i in device K-order
-__device__ __forceinline__ int dpos(int i) {
-    const int w = i & 127, s = w >> 4, q = (w >> 2) & 3, e = w & 3;
-    return (i & ~127) + 32 * q + 4 * s + e;
-}
-
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
 // one group (8 MMA steps) of a 16-row x (8 * NC)-column tile; rows ra (M rows
 // 0-7) and rb (M rows 8-15); bptr[c] = this lane's B run of column tile c
 template <int FMT, int NC>
@@ -223,9 +155,8 @@ __global__ void __launch_bounds__(128) k_gu(CallArgs a) {
     const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(H) * 2 : static_cast<size_t>(H) / 2;
     const uint8_t* row_g = blob + a.lay.gu + rg * rowbytes;
     const uint8_t* row_u = blob + a.lay.gu + ru * rowbytes;
-    const int sc_per_row = FMT == FMT_NVFP4 ? H / 16 : H / 32;
-    const uint8_t* sc_g = blob + a.lay.gus + static_cast<size_t>(rg) * sc_per_row;
-    const uint8_t* sc_u = blob + a.lay.gus + static_cast<size_t>(ru) * sc_per_row;
+    const uint8_t* sc_g = blob + a.lay.gus + static_cast<size_t>(rg) * a.lay.gus_pitch;
+    const uint8_t* sc_u = blob + a.lay.gus + static_cast<size_t>(ru) * a.lay.gus_pitch;
     float gs_gate = 1.0f, gs_up = 1.0f;
     if constexpr (FMT == FMT_NVFP4) {
         const float* gsc = reinterpret_cast<const float*>(blob + a.lay.gsc);
@@ -302,8 +233,7 @@ __global__ void __launch_bounds__(128) k_down_dec(CallArgs a) {
     const int r0 = blockIdx.x * 16 + g;
     const int na = *a.n_active;
     const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
-    const int sc_per_row = FMT == FMT_NVFP4 ? I / 16 : I / 32;
-    const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
+        const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     for (int u = 0; u < na; ++u) {
         const uint8_t* blob = a.act_ptr[u];
@@ -312,8 +242,8 @@ __global__ void __launch_bounds__(128) k_down_dec(CallArgs a) {
         if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
         const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
         const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
-        const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * sc_per_row;
-        const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * sc_per_row;
+        const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * a.lay.ds_pitch;
+        const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * a.lay.ds_pitch;
         for (int j = warp; j < GI; j += 4) {
             RowWords<FMT> ra, rb;
             load_row<FMT>(rowa, j, q, ra);
@@ -364,13 +294,12 @@ __global__ void __launch_bounds__(128) k_down_rows(CallArgs a) {
     const int row0 = a.act_row0[u], cnt = a.act_cnt[u];
     const int r0 = blockIdx.x * 16 + g;
     const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
-    const int sc_per_row = FMT == FMT_NVFP4 ? I / 16 : I / 32;
-    float gsd = 1.0f;
+        float gsd = 1.0f;
     if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
     const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
     const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
-    const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * sc_per_row;
-    const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * sc_per_row;
+    const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * a.lay.ds_pitch;
+    const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * a.lay.ds_pitch;
     const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
     __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(a.ybuf);
     for (int cb = 0; cb < cnt; cb += 8 * NC) {
@@ -521,8 +450,14 @@ __global__ void __launch_bounds__(256) k_down_f32(CallArgs a) {
 // --------------------------------------------------------------------------
 
 template <int FMT, int ACT>
-static int launch_mma_path(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down) {
+static int launch_mma_path(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down, int num_sms) {
     const int max_active = min(a.E, a.T * a.k) + a.n_shared;
+    if (a.T <= kDecodeMaxT && decode_fp4_supported(FMT, a.T)) {
+        if (launch_decode_fp4(a, num_sms, s) != cudaSuccess) return -1;
+        if (ev_gu) cudaEventRecord(ev_gu, s);
+        if (ev_down) cudaEventRecord(ev_down, s);
+        return 1;
+    }
     if (a.T <= kDecodeMaxT) {
         k_gu<FMT, 1><<<dim3(a.I / 8, max_active), 128, 0, s>>>(a);
         if (ev_gu) cudaEventRecord(ev_gu, s);
@@ -570,20 +505,21 @@ cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
         const bool bf = a.act == ACT_BF16;
         switch (a.fmt) {
             case FMT_BF16:
-                n = bf ? launch_mma_path<FMT_BF16, ACT_BF16>(a, s, ev_gu, ev_down)
-                       : launch_mma_path<FMT_BF16, ACT_FP32>(a, s, ev_gu, ev_down);
+                n = bf ? launch_mma_path<FMT_BF16, ACT_BF16>(a, s, ev_gu, ev_down, num_sms)
+                       : launch_mma_path<FMT_BF16, ACT_FP32>(a, s, ev_gu, ev_down, num_sms);
                 break;
             case FMT_NVFP4:
-                n = bf ? launch_mma_path<FMT_NVFP4, ACT_BF16>(a, s, ev_gu, ev_down)
-                       : launch_mma_path<FMT_NVFP4, ACT_FP32>(a, s, ev_gu, ev_down);
+                n = bf ? launch_mma_path<FMT_NVFP4, ACT_BF16>(a, s, ev_gu, ev_down, num_sms)
+                       : launch_mma_path<FMT_NVFP4, ACT_FP32>(a, s, ev_gu, ev_down, num_sms);
                 break;
             case FMT_MXFP4:
-                n = bf ? launch_mma_path<FMT_MXFP4, ACT_BF16>(a, s, ev_gu, ev_down)
-                       : launch_mma_path<FMT_MXFP4, ACT_FP32>(a, s, ev_gu, ev_down);
+                n = bf ? launch_mma_path<FMT_MXFP4, ACT_BF16>(a, s, ev_gu, ev_down, num_sms)
+                       : launch_mma_path<FMT_MXFP4, ACT_FP32>(a, s, ev_gu, ev_down, num_sms);
                 break;
             default:
                 return cudaErrorInvalidValue;
         }
+        if (n < 0) return cudaErrorLaunchFailure;
     }
     if (launches) *launches = n;
     return cudaGetLastError();

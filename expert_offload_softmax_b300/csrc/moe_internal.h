@@ -23,7 +23,9 @@ enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 //   gu  : gate/up rows [2I][H]. Rows come in blocks of 128: 64 gate rows then
 //         the 64 up rows of the same intermediate units (FP32: plain [gate I][up I]).
 //   d   : down rows [H][I].
-//   gus, ds: per-row block scales of gu and d (FP4 formats), canonical order.
+//   gus, ds: per-row block scales of gu and d (FP4 formats), canonical order;
+//         each scale row is padded to gus_pitch / ds_pitch bytes (multiples of
+//         16, so that any 16-byte aligned run of a row can be bulk-copied).
 //   gsc : float[4] per-tensor scales (gate, up, down, 1) — NVFP4; else 1.
 // Within every row, K is stored in "device order" (FP32 excepted): each group
 // of 128 consecutive elements is reordered so that position 32q + 4s + i holds
@@ -34,6 +36,7 @@ enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 // Activations fed to the same MMAs are stored in the same order.
 struct BlobLayout {
     size_t gu, d, gus, ds, gsc, bytes;
+    size_t gus_pitch, ds_pitch;
 };
 
 // Written by the cache kernel into mapped host memory; read by the host after
@@ -87,6 +90,8 @@ struct CallArgs {
     int32_t* act_slot;     // [E + n_shared]  pool slot of the active expert; shared: -(1 + layer*n_shared + s)
     void* xperm;           // [T*k + T*n_shared][H] bf16 gathered activations, device K-order (prefill, BF16)
     int32_t* dev_err;      // [1] sticky device error word (bounded waits that gave up)
+    int32_t* route_done;   // [1] routing CTAs finished in this call (0 between calls)
+    unsigned int* grid_bar;  // [2] grid barrier of the decode expert kernel: arrivals, generation
     int32_t* n_uniq;       // [1]
     int32_t* n_active;     // [1]
     void* hbuf;            // [rows][I] intermediate (f16 / bf16 / f32)
@@ -132,15 +137,19 @@ cudaError_t umma_set_attributes();
 cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s,
                                 cudaEvent_t ev_gu, int* launches);
 
-// launchers (kernels.cu); all enqueue on `s` and return cudaGetLastError()
-cudaError_t launch_router(const CallArgs& a, cudaStream_t s);
-cudaError_t launch_cache(const CallArgs& a, cudaStream_t s);
+// launchers; all enqueue on `s` and return cudaGetLastError()
+// routing + permutation + LRU cache lookup: one kernel
+cudaError_t launch_route(const CallArgs& a, cudaStream_t s);
 // launches the expert kernels; records ev_gu after the gate/up kernel and
 // ev_down after the down-projection kernel when they are non-null; *launches
 // receives the number of kernels launched. Prefill with BF16 weights takes the
 // tensor-core path when `maps` holds valid descriptors.
 cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
                            const UmmaMaps* maps, int num_sms, int* launches);
+// decode (T <= 8) with FP4 weights: gate/up + down in one cooperative kernel
+bool decode_fp4_supported(int fmt, int T);
+cudaError_t decode_fp4_set_attributes();
+cudaError_t launch_decode_fp4(const CallArgs& a, int num_sms, cudaStream_t s);
 // true when a prefill call of this shape takes the tensor-core path
 inline bool prefill_uses_umma(int fmt, int T) { return fmt == FMT_BF16 && T > kDecodeMaxT; }
 

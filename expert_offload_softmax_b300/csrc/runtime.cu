@@ -117,7 +117,7 @@ int validate_desc(const moe_model_desc* d, std::string* why) {
         if (d->inter < 128 || d->inter % 128) return bad("inter must be a positive multiple of 128");
     }
     const size_t xbytes = static_cast<size_t>(8) * d->hidden * (d->act_dtype == moe::ACT_BF16 ? 2 : 4);
-    if (xbytes > 200 * 1024) return bad("hidden too large for the router's shared-memory tile");
+    if (xbytes > 192 * 1024) return bad("hidden too large for the router's shared-memory tile");
     return MOE_OK;
 }
 
@@ -138,10 +138,12 @@ BlobLayout layout_for(const moe_model_desc& d) {
             break;
         default: {
             const size_t blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
+            L.gus_pitch = align_up(H / blk, 16);
+            L.ds_pitch = align_up(I / blk, 16);
             L.gu = 0; o = 2 * I * H / 2;
             L.d = align_up(o, 256); o = L.d + H * I / 2;
-            L.gus = align_up(o, 256); o = L.gus + 2 * I * H / blk;
-            L.ds = align_up(o, 256); o = L.ds + H * I / blk;
+            L.gus = align_up(o, 256); o = L.gus + 2 * I * L.gus_pitch;
+            L.ds = align_up(o, 256); o = L.ds + H * L.ds_pitch;
             L.gsc = align_up(o, 256); o = L.gsc + 16;
         }
     }
@@ -217,13 +219,15 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
                 for (int i = 0; i < I; ++i) {
                     const size_t dr = gu_row(i, which);
                     reorder_row_fp4(src + static_cast<size_t>(i) * H / 2, gu + dr * H / 2, H);
-                    std::memcpy(gus + dr * (H / blk), sc + static_cast<size_t>(i) * (H / blk), H / blk);
+                    std::memcpy(gus + dr * L.gus_pitch, sc + static_cast<size_t>(i) * (H / blk), H / blk);
                 }
             }
             const uint8_t* src = static_cast<const uint8_t*>(w->down.data);
             for (int r = 0; r < H; ++r)
                 reorder_row_fp4(src + static_cast<size_t>(r) * I / 2, blob + L.d + static_cast<size_t>(r) * I / 2, I);
-            std::memcpy(blob + L.ds, w->down.scales, static_cast<size_t>(H) * (I / blk));
+            for (int r = 0; r < H; ++r)
+                std::memcpy(blob + L.ds + static_cast<size_t>(r) * L.ds_pitch, w->down.scales + static_cast<size_t>(r) * (I / blk),
+                            I / blk);
             if (d.weight_fmt == moe::FMT_NVFP4) {
                 gsc[0] = w->gate.global_scale;
                 gsc[1] = w->up.global_scale;
@@ -336,6 +340,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (e != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::routing_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::umma_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (moe::decode_fp4_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, desc->device) != cudaSuccess)
         return bail(MOE_ERR_CUDA);
     const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared, k = h->d.top_k;
@@ -372,6 +377,8 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_slot)},
         {umma ? rows * H * 2 : 16, &a.xperm},
         {4, reinterpret_cast<void**>(&a.dev_err)},
+        {4, reinterpret_cast<void**>(&a.route_done)},
+        {8, reinterpret_cast<void**>(&a.grid_bar)},
         {4, reinterpret_cast<void**>(&a.n_uniq)},
         {4, reinterpret_cast<void**>(&a.n_active)},
         {rows * I * hes, &a.hbuf},
@@ -473,6 +480,8 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     CK(h, cudaMemset(h->stamp, 0, S * 8));
     CK(h, cudaMemset(h->clock, 0, 8));
     CK(h, cudaMemset(h->base.dev_err, 0, 4));
+    CK(h, cudaMemset(h->base.route_done, 0, 4));
+    CK(h, cudaMemset(h->base.grid_bar, 0, 8));
     CK(h, cudaDeviceSynchronize());
     h->maps.have_pool = false;
     if (h->maps.have_io) {
@@ -537,9 +546,8 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         if (!tc) return fail(h, MOE_ERR_OOM, "timing events");
         CK(h, cudaEventRecord(tc->r0, s));
     }
-    CK(h, moe::launch_router(a, s));
-    CK(h, moe::launch_cache(a, s));
-    h->st.kernel_launches += (h->d.weight_fmt != moe::FMT_FP32 ? 1 : 0) + 3 + 1;
+    CK(h, moe::launch_route(a, s));
+    h->st.kernel_launches += 1;
     if (tc) CK(h, cudaEventRecord(tc->r1, s));
     CK(h, cudaEventRecord(h->ev_cache, s));
     CK(h, cudaEventSynchronize(h->ev_cache));
