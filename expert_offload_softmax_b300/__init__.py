@@ -30,7 +30,7 @@ MOE_CACHE_PREFETCH_NEXT_LAYER = 1
 MOE_CACHE_LOG_EVENTS = 2
 
 # every symbol the header declares
-EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward",
+EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward", "moe_sync",
            "moe_stats", "moe_stats_reset", "moe_stats_events", "moe_debug_routing", "moe_debug_lru_table",
            "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing", "moe_route_topk_noalloc"]
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
@@ -62,7 +62,7 @@ class moe_stats_t(ctypes.Structure):
 class moe_timing_t(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_uint64)] + [(n, ctypes.c_double) for n in (
         "route_ms", "gate_up_ms", "down_ms", "combine_ms", "copy_ms")] + [(n, ctypes.c_uint64) for n in (
-        "gate_up_bytes", "down_bytes", "combine_bytes", "copy_bytes")]
+        "gate_up_bytes", "down_bytes", "combine_bytes", "copy_bytes", "resident_calls")]
 
     def as_dict(self):
         return {n: (float(getattr(self, n)) if t is ctypes.c_double else int(getattr(self, n)))
@@ -98,6 +98,7 @@ def load(path: str | None = None):
     lib.moe_load_expert.argtypes = [vp, i32, i32, P(moe_expert_host)]
     lib.moe_cache_config.argtypes = [vp, i32, u32]
     lib.moe_layer_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+    lib.moe_sync.argtypes = [vp]
     lib.moe_stats.argtypes = [vp, P(moe_stats_t)]
     lib.moe_stats_reset.argtypes = [vp]
     lib.moe_timing_enable.argtypes = [vp, i32]
@@ -170,6 +171,11 @@ def moe_cache_config(h: int, capacity_slots: int, flags: int = 0) -> None:
 def moe_layer_forward(h: int, hidden: int, router_w: int, layer_id: int, T: int, out: int,
                       stream: int | None = None) -> None:
     _check(h, load().moe_layer_forward(h, hidden, router_w, layer_id, T, out, stream))
+
+
+def moe_sync(h: int) -> None:
+    """Waits for every enqueued call; raises the first error found for any of them."""
+    _check(h, load().moe_sync(h))
 
 
 def moe_stats(h: int) -> dict:

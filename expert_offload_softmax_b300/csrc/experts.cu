@@ -88,6 +88,35 @@ __device__ __forceinline__ void row_to_a(const RowWords<FMT>& r, uint32_t (&A)[8
     }
 }
 
+// FP4 tiled blobs: the 16 code bytes of lane quad q and the step scales of row
+// r (0-15) of a tile, for K-group j of G
+template <int FMT>
+__device__ __forceinline__ void load_tile_row(const uint8_t* tile, int G, int sbpg, int r, int j, int q, float mul,
+                                              RowWords<FMT>& x, float (&s)[8]) {
+    const int c = j / kChunkGroups, w = j % kChunkGroups;
+    const int ng = fp4_chunk_groups(G, c);
+    const uint8_t* chunk = tile + fp4_chunk_off(c, sbpg);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, r, w, q)));
+    x.w[0] = v.x; x.w[1] = v.y; x.w[2] = v.z; x.w[3] = v.w;
+    // the group's scale bytes sit where a row-major scale row would hold group 0
+    load_step_scales<FMT>(chunk + fp4_scale_off(ng, sbpg, r, w), 0, mul, s);
+}
+
+// both rows (M rows 0-7 and 8-15) of one lane for group j: BF16 from row
+// pointers ra/rb, FP4 from rows ta/tb of `tile`
+template <int FMT>
+__device__ __forceinline__ void load_pair(const uint8_t* ra, const uint8_t* rb, const uint8_t* tile, int ta, int tb,
+                                          int G, int sbpg, int j, int q, float mul, RowWords<FMT>& x, RowWords<FMT>& y,
+                                          float (&sa)[8], float (&sb)[8]) {
+    if constexpr (FMT == FMT_BF16) {
+        load_row<FMT>(ra, j, q, x);
+        load_row<FMT>(rb, j, q, y);
+    } else {
+        load_tile_row<FMT>(tile, G, sbpg, ta, j, q, mul, x, sa);
+        load_tile_row<FMT>(tile, G, sbpg, tb, j, q, mul, y, sb);
+    }
+}
+
 // 64-byte B run (32 activations of one column for one group) -> 16 words; zeros if p is null
 __device__ __forceinline__ void load_b(const uint16_t* p, uint32_t (&b)[16]) {
     if (p) {
@@ -140,8 +169,17 @@ __device__ __forceinline__ void mma_group(const RowWords<FMT>& ra, const RowWord
 // grid (I/8 unit tiles, max active experts), 4 warps split K = H by group
 // --------------------------------------------------------------------------
 
+// thread 0 of every CTA waits for the call's weights; false if the wait gave up
+__device__ __forceinline__ bool cta_wait_ready(const CallArgs& a) {
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) s_ok = wait_ready(a) ? 1 : 0;
+    __syncthreads();
+    return s_ok != 0;
+}
+
 template <int FMT, int NC>
 __global__ void __launch_bounds__(128) k_gu(CallArgs a) {
+    if (!cta_wait_ready(a)) return;
     const int u = blockIdx.y;
     if (u >= *a.n_active) return;
     __shared__ float red[4][NC][32][4];
@@ -152,11 +190,10 @@ __global__ void __launch_bounds__(128) k_gu(CallArgs a) {
     const int i0 = blockIdx.x * 8;
     const int rg = (i0 / 64) * 128 + (i0 % 64) + g;  // device gu row of gate unit i0+g
     const int ru = rg + 64;                           // and of its up unit
-    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(H) * 2 : static_cast<size_t>(H) / 2;
-    const uint8_t* row_g = blob + a.lay.gu + rg * rowbytes;
+    const size_t rowbytes = static_cast<size_t>(H) * 2;
+    const uint8_t* row_g = blob + a.lay.gu + rg * rowbytes;  // BF16
     const uint8_t* row_u = blob + a.lay.gu + ru * rowbytes;
-    const uint8_t* sc_g = blob + a.lay.gus + static_cast<size_t>(rg) * a.lay.gus_pitch;
-    const uint8_t* sc_u = blob + a.lay.gus + static_cast<size_t>(ru) * a.lay.gus_pitch;
+    const uint8_t* tile = blob + a.lay.gu + static_cast<size_t>(blockIdx.x) * a.lay.gu_tile;  // FP4
     float gs_gate = 1.0f, gs_up = 1.0f;
     if constexpr (FMT == FMT_NVFP4) {
         const float* gsc = reinterpret_cast<const float*>(blob + a.lay.gsc);
@@ -177,11 +214,8 @@ __global__ void __launch_bounds__(128) k_gu(CallArgs a) {
         }
         for (int j = warp; j < G; j += 4) {
             RowWords<FMT> ra, rb;
-            load_row<FMT>(row_g, j, q, ra);
-            load_row<FMT>(row_u, j, q, rb);
             float sa[8], sb[8];
-            load_step_scales<FMT>(sc_g, j, 1.0f, sa);
-            load_step_scales<FMT>(sc_u, j, 1.0f, sb);
+            load_pair<FMT>(row_g, row_u, tile, g, 8 + g, G, a.lay.sbpg, j, q, 1.0f, ra, rb, sa, sb);
             const uint16_t* bp[NC];
 #pragma unroll
             for (int c = 0; c < NC; ++c)
@@ -232,7 +266,7 @@ __global__ void __launch_bounds__(128) k_down_dec(CallArgs a) {
     const int H = a.H, I = a.I, T = a.T, GI = I / kGroupK;
     const int r0 = blockIdx.x * 16 + g;
     const int na = *a.n_active;
-    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
+    const size_t rowbytes = static_cast<size_t>(I) * 2;
         const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     for (int u = 0; u < na; ++u) {
@@ -240,17 +274,13 @@ __global__ void __launch_bounds__(128) k_down_dec(CallArgs a) {
         const int hr = g < T ? a.tok_row[u * kDecodeMaxT + g] : -1;
         float gsd = 1.0f;
         if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
-        const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
+        const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;  // BF16
         const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
-        const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * a.lay.ds_pitch;
-        const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * a.lay.ds_pitch;
+        const uint8_t* tile = blob + a.lay.d + static_cast<size_t>(blockIdx.x) * a.lay.d_tile;  // FP4
         for (int j = warp; j < GI; j += 4) {
             RowWords<FMT> ra, rb;
-            load_row<FMT>(rowa, j, q, ra);
-            load_row<FMT>(rowb, j, q, rb);
             float sa[8], sb[8];
-            load_step_scales<FMT>(sca, j, gsd, sa);
-            load_step_scales<FMT>(scb, j, gsd, sb);
+            load_pair<FMT>(rowa, rowb, tile, g, 8 + g, GI, a.lay.sbpg, j, q, gsd, ra, rb, sa, sb);
             const uint16_t* bp[1] = {hr >= 0 ? hb + static_cast<size_t>(hr) * I + j * 128 + 32 * q : nullptr};
             mma_group<FMT, 1>(ra, rb, sa, sb, bp, 1, acc);
         }
@@ -293,13 +323,12 @@ __global__ void __launch_bounds__(128) k_down_rows(CallArgs a) {
     const uint8_t* blob = a.act_ptr[u];
     const int row0 = a.act_row0[u], cnt = a.act_cnt[u];
     const int r0 = blockIdx.x * 16 + g;
-    const size_t rowbytes = FMT == FMT_BF16 ? static_cast<size_t>(I) * 2 : static_cast<size_t>(I) / 2;
+    const size_t rowbytes = static_cast<size_t>(I) * 2;
         float gsd = 1.0f;
     if constexpr (FMT == FMT_NVFP4) gsd = reinterpret_cast<const float*>(blob + a.lay.gsc)[2];
-    const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;
+    const uint8_t* rowa = blob + a.lay.d + r0 * rowbytes;  // BF16
     const uint8_t* rowb = blob + a.lay.d + (r0 + 8) * rowbytes;
-    const uint8_t* sca = blob + a.lay.ds + static_cast<size_t>(r0) * a.lay.ds_pitch;
-    const uint8_t* scb = blob + a.lay.ds + static_cast<size_t>(r0 + 8) * a.lay.ds_pitch;
+    const uint8_t* tile = blob + a.lay.d + static_cast<size_t>(blockIdx.x) * a.lay.d_tile;  // FP4
     const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
     __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(a.ybuf);
     for (int cb = 0; cb < cnt; cb += 8 * NC) {
@@ -309,11 +338,8 @@ __global__ void __launch_bounds__(128) k_down_rows(CallArgs a) {
         for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.0f;
         for (int j = warp; j < GI; j += 4) {
             RowWords<FMT> ra, rb;
-            load_row<FMT>(rowa, j, q, ra);
-            load_row<FMT>(rowb, j, q, rb);
             float sa[8], sb[8];
-            load_step_scales<FMT>(sca, j, gsd, sa);
-            load_step_scales<FMT>(scb, j, gsd, sb);
+            load_pair<FMT>(rowa, rowb, tile, g, 8 + g, GI, a.lay.sbpg, j, q, gsd, ra, rb, sa, sb);
             const uint16_t* bp[NC];
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
@@ -399,6 +425,7 @@ __device__ __forceinline__ float ldx(const void* p, size_t i) {
 
 template <int ACT>
 __global__ void __launch_bounds__(256) k_gu_f32(CallArgs a) {
+    if (!cta_wait_ready(a)) return;
     const int u = blockIdx.y;
     if (u >= *a.n_active) return;
     const int H = a.H, I = a.I;
@@ -523,6 +550,36 @@ cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
     }
     if (launches) *launches = n;
     return cudaGetLastError();
+}
+
+// Loads every expert kernel of this file now. The expert kernels of a call
+// wait on the device for the call's copies, which the service thread issues;
+// with lazy module loading, the first launch of a kernel behind a waiting one
+// would load its module while the wait runs and hold up those copies until the
+// wait gives up. Querying a kernel's attributes loads it.
+cudaError_t experts_preload() {
+    cudaFuncAttributes fa;
+    const void* fns[] = {
+        reinterpret_cast<const void*>(&k_gu<FMT_BF16, 1>), reinterpret_cast<const void*>(&k_gu<FMT_BF16, 8>),
+        reinterpret_cast<const void*>(&k_gu<FMT_NVFP4, 1>), reinterpret_cast<const void*>(&k_gu<FMT_NVFP4, 8>),
+        reinterpret_cast<const void*>(&k_gu<FMT_MXFP4, 1>), reinterpret_cast<const void*>(&k_gu<FMT_MXFP4, 8>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_BF16, ACT_BF16>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_BF16, ACT_FP32>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_NVFP4, ACT_BF16>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_NVFP4, ACT_FP32>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_MXFP4, ACT_BF16>),
+        reinterpret_cast<const void*>(&k_down_dec<FMT_MXFP4, ACT_FP32>),
+        reinterpret_cast<const void*>(&k_down_rows<FMT_BF16, 8>), reinterpret_cast<const void*>(&k_down_rows<FMT_NVFP4, 8>),
+        reinterpret_cast<const void*>(&k_down_rows<FMT_MXFP4, 8>),
+        reinterpret_cast<const void*>(&k_combine<ACT_BF16>), reinterpret_cast<const void*>(&k_combine<ACT_FP32>),
+        reinterpret_cast<const void*>(&k_gu_f32<ACT_BF16>), reinterpret_cast<const void*>(&k_gu_f32<ACT_FP32>),
+        reinterpret_cast<const void*>(&k_down_f32<ACT_BF16>), reinterpret_cast<const void*>(&k_down_f32<ACT_FP32>),
+    };
+    for (const void* f : fns) {
+        const cudaError_t e = cudaFuncGetAttributes(&fa, f);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -20,28 +20,61 @@ enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 
 // Device layout of one expert ("blob"), identical in the pinned host bank and
 // in a pool slot, so that a miss is one contiguous copy.
-//   gu  : gate/up rows [2I][H]. Rows come in blocks of 128: 64 gate rows then
-//         the 64 up rows of the same intermediate units (FP32: plain [gate I][up I]).
-//   d   : down rows [H][I].
-//   gus, ds: per-row block scales of gu and d (FP4 formats), canonical order;
-//         each scale row is padded to gus_pitch / ds_pitch bytes (multiples of
-//         16, so that any 16-byte aligned run of a row can be bulk-copied).
-//   gsc : float[4] per-tensor scales (gate, up, down, 1) — NVFP4; else 1.
-// Within every row, K is stored in "device order" (FP32 excepted): each group
-// of 128 consecutive elements is reordered so that position 32q + 4s + i holds
+//
+// Within every weight row, K is stored in "device order": each group of 128
+// consecutive elements is reordered so that position 32q + 4s + i holds
 // element 16s + 4q + i of the group (q < 4, s < 8, i < 4). A warp lane with
 // quad index q then finds, in one contiguous 16-byte (FP4) or 64-byte (BF16)
 // run, its operands for the eight m16n8k16 MMA steps s of the group, and step s
 // covers exactly one 16-element NVFP4 scale block (half of an MXFP4 block).
 // Activations fed to the same MMAs are stored in the same order.
+//
+// BF16 / FP32 blobs:
+//   gu : gate/up rows [2I][H]. Rows come in blocks of 128: 64 gate rows then
+//        the 64 up rows of the same intermediate units (FP32: plain [gate I][up I]).
+//   d  : down rows [H][I].
+// FP4 blobs (NVFP4, MXFP4) are tiled for streaming: the gu region is I/8 tiles
+// (tile u: rows 0-7 = gate units 8u..8u+7, rows 8-15 = their up units), the d
+// region H/16 tiles (tile r: down rows 16r..16r+15); a tile is a run of chunks
+// of up to 8 K-groups (1024 elements), and chunk c with ng groups is
+//   codes  [16 rows][ng * 64 bytes]   (16-byte units of row r XOR-swizzled,
+//                                      see fp4_code_off)
+//   scales [16 rows][ng * sbpg bytes] (sbpg = 8 E4M3 (NVFP4) or 4 E8M0 (MXFP4)
+//                                      bytes per group, canonical order)
+// so that one 16-row x 1024-K slice of a projection is one contiguous run.
+//   gsc: float[4] per-tensor scales (gate, up, down, 1) - NVFP4; else 1.
 struct BlobLayout {
-    size_t gu, d, gus, ds, gsc, bytes;
-    size_t gus_pitch, ds_pitch;
+    size_t gu, d, gsc, bytes;
+    size_t gu_tile, d_tile;  // FP4: bytes of one tile of each region
+    int sbpg;                // FP4: scale bytes per 128-element group
 };
+
+constexpr int kTileRows = 16;
+constexpr int kChunkGroups = 8;
+
+// FP4 tiles: offset of chunk c (all earlier chunks are full)
+__host__ __device__ inline size_t fp4_chunk_off(int c, int sbpg) {
+    return static_cast<size_t>(kTileRows) * kChunkGroups * c * (64 + sbpg);
+}
+__host__ __device__ inline int fp4_chunk_groups(int G, int c) {
+    return G - kChunkGroups * c < kChunkGroups ? G - kChunkGroups * c : kChunkGroups;
+}
+// offset, inside its chunk (ng groups), of the 16 code bytes of row r, group w,
+// lane quad q. Rows of an even-ng chunk are 512-byte multiples apart, so the
+// odd rows swap the two halves of each 128-byte bank window: the 8 lanes of a
+// quarter-warp (rows 2m, 2m+1, quads 0-3) then hit 8 distinct 16-byte bank groups.
+__host__ __device__ inline int fp4_code_off(int ng, int r, int w, int q) {
+    const int x = ((r & 1) && !(ng & 1)) ? 4 : 0;
+    return r * ng * 64 + (((w * 4 + q) ^ x) * 16);
+}
+__host__ __device__ inline int fp4_scale_off(int ng, int sbpg, int r, int w) {
+    return kTileRows * ng * 64 + r * ng * sbpg + w * sbpg;
+}
 
 // Written by the cache kernel into mapped host memory; read by the host after
 // the cache kernel completes.
 struct CallInfo {
+    unsigned long long done;  // the call's sequence number, written last by the routing kernel
     int32_t status;          // 0 ok, else a negative moe_status
     int32_t n_uniq;
     int32_t n_hit, n_miss;   // demand batch
@@ -60,6 +93,22 @@ struct CallInfo {
     int32_t ev_evicted[2 * kMaxExperts];
     int32_t ev_prefetch[2 * kMaxExperts];
 };
+
+// Decode plan: what the decode expert kernel needs about each active expert,
+// written by the routing kernel into one contiguous buffer (a 128-byte header
+// with the number of active experts, then one 128-byte record per expert) so
+// that the expert kernel fetches it with a single bulk copy.
+struct DecExpert {
+    const uint8_t* ptr;          // blob (pool slot or shared-expert area)
+    int32_t row0, cnt;           // first h row, rows (tokens) of the expert
+    int32_t tok[kDecodeMaxT];    // token of the expert's row n (n < cnt), else -1
+    int32_t hrow[kDecodeMaxT];   // h row of token t, else -1
+    float gate[kDecodeMaxT];     // routing gate of the expert's row n
+    float gs[3];                 // per-tensor scales (filled by the expert kernel)
+    int32_t pad;
+};
+static_assert(sizeof(DecExpert) == 128, "decode plan record");
+constexpr int kDecPlanHeader = 128;
 
 struct CallArgs {
     // shape
@@ -92,6 +141,7 @@ struct CallArgs {
     int32_t* dev_err;      // [1] sticky device error word (bounded waits that gave up)
     int32_t* route_done;   // [1] routing CTAs finished in this call (0 between calls)
     unsigned int* grid_bar;  // [2] grid barrier of the decode expert kernel: arrivals, generation
+    unsigned char* dplan;  // decode plan: header + (E + n_shared) records
     int32_t* n_uniq;       // [1]
     int32_t* n_active;     // [1]
     void* hbuf;            // [rows][I] intermediate (f16 / bf16 / f32)
@@ -104,15 +154,48 @@ struct CallArgs {
     const uint8_t* pool;   // S * blob bytes
     const uint8_t* shared_base;  // this layer's shared experts (n_shared blobs)
     BlobLayout lay;
-    CallInfo* info;        // mapped host memory (device pointer)
+    CallInfo* info;        // mapped host memory (device pointer): this call's record
+    // miss pipeline: the expert kernels of call `seq` start once *ready >= seq.
+    // The routing kernel releases the call itself when it has no demand misses
+    // and self_release is set; otherwise the host writes seq after the copies.
+    unsigned long long* ready;
+    unsigned long long seq;
+    int self_release;
+    unsigned long long wait_ns;  // bound of every device-side wait
 };
+
+// Bounded wait of the expert kernels for their call's weights (one thread);
+// false (and the device error word set) if the bound ran out.
+__device__ __forceinline__ bool wait_ready(const CallArgs& a) {
+    const volatile unsigned long long* r = a.ready;
+    if (*r >= a.seq) {
+        __threadfence();
+        return true;
+    }
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        if (*r >= a.seq) {
+            __threadfence();
+            return true;
+        }
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > a.wait_ns) {
+            atomicExch(a.dev_err, 4);  // MOE_DEVERR_TIMEOUT_READY
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
 
 // device error codes written to CallArgs::dev_err
 enum DevErr {
     DEVERR_NONE = 0,
     MOE_DEVERR_TIMEOUT_PRODUCER = 1,
     MOE_DEVERR_TIMEOUT_MMA = 2,
-    MOE_DEVERR_TIMEOUT_EPILOGUE = 3
+    MOE_DEVERR_TIMEOUT_EPILOGUE = 3,
+    MOE_DEVERR_TIMEOUT_READY = 4
 };
 
 // an opaque CUtensorMap (128 bytes, 64-byte aligned)
@@ -150,6 +233,8 @@ cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
 bool decode_fp4_supported(int fmt, int T);
 cudaError_t decode_fp4_set_attributes();
 cudaError_t launch_decode_fp4(const CallArgs& a, int num_sms, cudaStream_t s);
+// loads every expert kernel (called once by moe_init)
+cudaError_t experts_preload();
 // true when a prefill call of this shape takes the tensor-core path
 inline bool prefill_uses_umma(int fmt, int T) { return fmt == FMT_BF16 && T > kDecodeMaxT; }
 

@@ -81,11 +81,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
 
+// waits for the phase of parity `parity` for up to ~20 us (the thread is
+// suspended, not spinning, and resumes as soon as the phase completes)
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n"
         "selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(su32(b)), "r"(parity)
@@ -269,7 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued_phase[C::kStages];
 #pragma unroll
             for (int s = 0; s < C::kStages; ++s) issued_phase[s] = -1;
-            bool ok = true;
+            // the call's expert weights must have landed in the pool
+            bool ok = MODE == MODE_DOWN || wait_ready(a);
+            if (!ok) *abort_flag = 1;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const int u = find_expert(ts, na, t);
                 const int local = t - ts.start[u];
@@ -515,8 +519,12 @@ bool umma_map_3d(UmmaMap* m, const void* base, uint64_t slots, uint64_t slot_byt
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// also loads the gather kernel (see experts_preload for why every kernel is loaded up front)
 cudaError_t umma_set_attributes() {
     cudaError_t e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32>)))) return e;
     if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfg<MODE_GU>::kSmem)))
         return e;

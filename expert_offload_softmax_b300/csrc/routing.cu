@@ -30,7 +30,7 @@ namespace moe {
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kPrefillTokTile = 8;  // tokens per phase-A CTA (prefill)
-constexpr int kPrefillEpw = 2;      // experts per warp per pass (prefill)
+constexpr int kPrefillEpw = 4;      // experts per warp per pass (prefill)
 
 // --------------------------------------------------------------------------
 // activation loads
@@ -66,24 +66,25 @@ __device__ __forceinline__ void ld_act8(const void* p, size_t i, float (&v)[8]) 
 }
 
 // --------------------------------------------------------------------------
-// activations -> device K-order (f16 for FP4 weights, bf16 for BF16 weights)
-// for rows [t0, t1); work split over `nthr` threads starting at `tid`
+// activations -> device K-order (f16 for FP4 weights, bf16 for BF16 weights),
+// from the token rows already staged in shared memory: xs holds rows
+// [t0, t0 + nt); work split over `nthr` threads starting at `tid`
 // --------------------------------------------------------------------------
 
 template <int ACT>
-__device__ void xprep_rows(const void* __restrict__ hidden, void* __restrict__ xh, int fmt, int H, int t0,
-                           int t1, size_t tid, size_t nthr) {
+__device__ void xprep_rows(const unsigned char* xs, void* __restrict__ xh, int fmt, int H, int t0, int nt,
+                           size_t tid, size_t nthr) {
     if (fmt == FMT_FP32) return;
     const bool f16 = fmt != FMT_BF16;
     const int h4 = H / 4;
-    const size_t n4 = static_cast<size_t>(t1 - t0) * h4;
+    const size_t n4 = static_cast<size_t>(nt) * h4;
     for (size_t idx = tid; idx < n4; idx += nthr) {
-        const int t = t0 + static_cast<int>(idx / h4);
+        const int t = static_cast<int>(idx / h4);
         const int p = 4 * static_cast<int>(idx % h4);   // device position
         const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
         const size_t src = static_cast<size_t>(t) * H + 128 * j + 16 * s + 4 * q;
-        const float v0 = ld_act<ACT>(hidden, src), v1 = ld_act<ACT>(hidden, src + 1);
-        const float v2 = ld_act<ACT>(hidden, src + 2), v3 = ld_act<ACT>(hidden, src + 3);
+        const float v0 = ld_act<ACT>(xs, src), v1 = ld_act<ACT>(xs, src + 1);
+        const float v2 = ld_act<ACT>(xs, src + 2), v3 = ld_act<ACT>(xs, src + 3);
         uint2 o;
         if (f16) {
             __half2 a = __floats2half2_rn(v0, v1), b = __floats2half2_rn(v2, v3);
@@ -94,7 +95,27 @@ __device__ void xprep_rows(const void* __restrict__ hidden, void* __restrict__ x
             o.x = *reinterpret_cast<uint32_t*>(&a);
             o.y = *reinterpret_cast<uint32_t*>(&b);
         }
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xh) + static_cast<size_t>(t) * H + p) = o;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(xh) + static_cast<size_t>(t0 + t) * H + p) = o;
+    }
+}
+
+// global -> shared copy of n 16-byte vectors; each thread issues up to 8 loads
+// before its first store, so the copy costs one memory round trip per 8 vectors
+__device__ __forceinline__ void copy_g2s(unsigned char* dst, const unsigned char* src, size_t n) {
+    constexpr int kB = 8;
+    const size_t nthr = blockDim.x;
+    for (size_t i0 = threadIdx.x; i0 < n; i0 += nthr * kB) {
+        uint4 v[kB];
+#pragma unroll
+        for (int i = 0; i < kB; ++i) {
+            const size_t k = i0 + i * nthr;
+            if (k < n) v[i] = __ldg(reinterpret_cast<const uint4*>(src) + k);
+        }
+#pragma unroll
+        for (int i = 0; i < kB; ++i) {
+            const size_t k = i0 + i * nthr;
+            if (k < n) reinterpret_cast<uint4*>(dst)[k] = v[i];
+        }
     }
 }
 
@@ -104,38 +125,116 @@ __device__ void xprep_rows(const void* __restrict__ hidden, void* __restrict__ x
 //   accumulates its chunks in increasing h with fused multiply-adds from 0;
 //   the 32 lane sums then combine by xor-butterfly (o = 16, 8, 4, 2, 1).
 // EPW experts (rows e0.. of router_w, e >= E contributes nothing) x nt tokens
-// whose rows sit in shared memory; every lane returns the finished sums.
+// whose rows sit in shared memory; every lane returns the finished sums. Each
+// lane first loads NB of its chunks (all independent), then runs its FMA
+// chain over them in order, so a batch costs one memory round trip. Pairs of
+// experts go through the packed fma.rn.f32x2, two IEEE fused multiply-adds
+// with round-to-nearest-even, i.e. the same result as two separate ones.
 // --------------------------------------------------------------------------
 
-template <int ACT, int EPW>
+template <int ACT>
+struct RawChunk {
+    uint4 v[ACT == ACT_BF16 ? 1 : 2];
+};
+
+template <int ACT>
+__device__ __forceinline__ void ld_chunk(const void* p, size_t i, RawChunk<ACT>& r) {
+    const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(p) +
+                                                    i * (ACT == ACT_BF16 ? 2 : 4));
+    r.v[0] = __ldg(q);
+    if constexpr (ACT != ACT_BF16) r.v[1] = __ldg(q + 1);
+}
+
+template <int ACT>
+__device__ __forceinline__ void cvt_chunk(const RawChunk<ACT>& r, float (&v)[8]) {
+    if constexpr (ACT == ACT_BF16) {
+        const uint32_t w[4] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = __uint_as_float(w[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    } else {
+        const uint32_t w[8] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(w[j]);
+    }
+}
+
+// (c0, c1) = (fma(a, b0, c0), fma(a, b1, c1)), both rounded to nearest even
+__device__ __forceinline__ void fma2(float a, float b0, float b1, float& c0, float& c1) {
+    unsigned long long A, B, C;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a), "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c0), "f"(c1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(C) : "l"(A), "l"(B));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(C));
+}
+
+// the first batch of a warp's router chunks (lane's chunks lane, lane+32, ...)
+template <int ACT, int EPW, int NB>
+__device__ __forceinline__ void router_batch(const void* __restrict__ router_w, int H, int E, int e0, int cb,
+                                             RawChunk<ACT> (&raw)[NB][EPW]) {
+    const int nchunk = H / 8;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        const int c = cb + 32 * i;
+#pragma unroll
+        for (int e = 0; e < EPW; ++e)
+            if (c < nchunk && e0 + e < E) ld_chunk<ACT>(router_w, static_cast<size_t>(e0 + e) * H + 8 * c, raw[i][e]);
+    }
+}
+
+// pre: this lane's first batch, already loaded with router_batch (or null)
+template <int ACT, int EPW, int NB>
 __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, const unsigned char* xs, int H,
-                                            int E, int e0, int nt, int lane, float (&acc)[EPW][8]) {
+                                            int E, int e0, int nt, int lane, float (&acc)[EPW][8],
+                                            const RawChunk<ACT> (*pre)[EPW] = nullptr) {
 #pragma unroll
     for (int e = 0; e < EPW; ++e)
 #pragma unroll
         for (int t = 0; t < 8; ++t) acc[e][t] = 0.0f;
     const int nchunk = H / 8;
-#pragma unroll 2
-    for (int c = lane; c < nchunk; c += 32) {
-        float wv[EPW][8];
+    for (int cb = lane; cb < nchunk; cb += 32 * NB) {
+        RawChunk<ACT> raw[NB][EPW];
+        if (pre && cb == lane) {
 #pragma unroll
-        for (int e = 0; e < EPW; ++e) {
-            if (e0 + e < E) {
-                ld_act8<ACT>(router_w, static_cast<size_t>(e0 + e) * H + 8 * c, wv[e]);
-            } else {
+            for (int i = 0; i < NB; ++i)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) wv[e][i] = 0.0f;
-            }
+                for (int e = 0; e < EPW; ++e) raw[i][e] = pre[i][e];
+        } else {
+            router_batch<ACT, EPW, NB>(router_w, H, E, e0, cb, raw);
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (t < nt) {
-                float xv[8];
-                ld_act8<ACT>(xs, static_cast<size_t>(t) * H + 8 * c, xv);
+        for (int i = 0; i < NB; ++i) {
+            const int c = cb + 32 * i;
+            if (c >= nchunk) break;
+            float wv[EPW][8];
 #pragma unroll
-                for (int e = 0; e < EPW; ++e)
+            for (int e = 0; e < EPW; ++e) {
+                if (e0 + e < E) {
+                    cvt_chunk<ACT>(raw[i][e], wv[e]);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[e][t] = __fmaf_rn(xv[i], wv[e][i], acc[e][t]);
+                    for (int j = 0; j < 8; ++j) wv[e][j] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t < nt) {
+                    float xv[8];
+                    ld_act8<ACT>(xs, static_cast<size_t>(t) * H + 8 * c, xv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if constexpr (EPW % 2 == 0) {
+#pragma unroll
+                            for (int e = 0; e < EPW; e += 2) fma2(xv[j], wv[e][j], wv[e + 1][j], acc[e][t], acc[e + 1][t]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < EPW; ++e) acc[e][t] = __fmaf_rn(xv[j], wv[e][j], acc[e][t]);
+                        }
+                    }
+                }
             }
         }
     }
@@ -157,58 +256,74 @@ __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, c
 //   divided by their sum. Lane j < k returns selection j.
 // --------------------------------------------------------------------------
 
-template <bool GLOBAL>
-__device__ __forceinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate) {
-    constexpr int kPer = kMaxExperts / 32;
-    const int per = (E + 31) / 32;
-    float v[kPer];
-    float mx = -INFINITY;
+// float -> unsigned with the same order (NaN never reaches it)
+__device__ __forceinline__ uint32_t ord_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// KPER: logits per lane the code is unrolled for (E <= 32 * KPER). Each round
+// takes the lane-local best untaken logit, then the warp maximum and the
+// lowest expert index holding it with two warp-wide reductions.
+template <bool GLOBAL, int KPER>
+__device__ __forceinline__ void warp_topk_n(const float* lrow, int E, int k, int lane, int& sel, float& gate) {
+    float v[KPER];
+    uint32_t key[KPER];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        v[i] = -INFINITY;
+    for (int i = 0; i < KPER; ++i) {
         const int e = lane + 32 * i;
-        if (i < per && e < E) {
-            float x = GLOBAL ? __ldcg(lrow + e) : lrow[e];
-            if (x != x) x = -INFINITY;
-            v[i] = x;
-            mx = fmaxf(mx, x);
-        }
+        float x = -INFINITY;
+        if (e < E) x = GLOBAL ? __ldcg(lrow + e) : lrow[e];
+        if (x != x) x = -INFINITY;
+        v[i] = x;
+        key[i] = ord_key(x);
     }
+    uint32_t kmax = 0u;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int i = 0; i < KPER; ++i) kmax = key[i] > kmax ? key[i] : kmax;
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    const uint32_t mu = (kmax & 0x80000000u) ? (kmax & 0x7FFFFFFFu) : ~kmax;
+    const float mx = __uint_as_float(mu);
     float den = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i)
-        if (i < per && v[i] != -INFINITY) den += expf(v[i] - mx);
+    for (int i = 0; i < KPER; ++i)
+        if (v[i] != -INFINITY) den += expf(v[i] - mx);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     uint32_t taken = 0;
-    float psum = 0.0f, pj = 0.0f;
     int ej = 0;
+    float bvj = -INFINITY;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        uint32_t bk = 0u;
         int be = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i < KPER; ++i) {
             const int e = lane + 32 * i;
-            if (i < per && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-                bv = v[i];
-                be = e;
-            }
+            if (e < E && !((taken >> i) & 1u) && key[i] > bk) { bk = key[i]; be = e; }
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        // lanes whose local best is below the warp best offer no index
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const int we = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<uint32_t>(bk == wk ? be : 0x7fffffff)));
+        if ((we & 31) == lane) taken |= 1u << (we >> 5);
+        if (lane == j) {
+            ej = we;
+            const uint32_t u = (wk & 0x80000000u) ? (wk & 0x7FFFFFFFu) : ~wk;
+            bvj = __uint_as_float(u);
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        const float p = bv == -INFINITY ? 0.0f : expf(bv - mx) / den;
-        psum += p;
-        if (lane == j) { pj = p; ej = be; }
     }
+    // lane j < k holds selection j; gates = its probability / sum over the k
+    const float pj = (lane < k && bvj != -INFINITY) ? expf(bvj - mx) / den : 0.0f;
+    float psum = lane < k ? pj : 0.0f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
     sel = ej;
     gate = pj / psum;
+}
+
+template <bool GLOBAL>
+__device__ __forceinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate) {
+    if (E <= 256) warp_topk_n<GLOBAL, 8>(lrow, E, k, lane, sel, gate);
+    else warp_topk_n<GLOBAL, kMaxExperts / 32>(lrow, E, k, lane, sel, gate);
 }
 
 // --------------------------------------------------------------------------
@@ -235,11 +350,13 @@ struct LruShared {
     unsigned long long clock;
 };
 
-// phase-B shared memory; the keys / per-warp count area follows it
+// phase-B shared memory; the work area follows it
 struct RouteShared {
     int32_t cnt[kMaxExperts];
     int32_t off[kMaxExperts];
     int32_t members[kMaxExperts];
+    int32_t e2u[kMaxExperts];
+    int32_t trow[2][kMaxExperts];  // LRU table rows of this layer and of layer+1
     int32_t topk[kDecodeMaxT * kMaxTopK];
     float gates[kDecodeMaxT * kMaxTopK];
     int32_t scan_a[kRouteWarps], scan_b[kRouteWarps];
@@ -248,6 +365,41 @@ struct RouteShared {
 };
 
 constexpr size_t kRouteSharedBytes = (sizeof(RouteShared) + 15) / 16 * 16;
+// pools up to this many slots keep their stamps and owners in shared memory during phase B
+constexpr int kLruCachedSlots = 4096;
+
+// The LRU state phase B works on: global arrays, with shared-memory copies
+// (loaded once at the start of phase B) of the stamps and owners of a small
+// pool and of the table rows of this layer and the next. Every write goes to
+// both.
+struct LruView {
+    const CallArgs* a;
+    int32_t* trow0;               // table row of a.layer
+    int32_t* trow1;               // table row of a.layer + 1 (prefill prefetch)
+    unsigned long long* st_s;     // [S] stamps, or null
+    int32_t* own_s;               // [S] owners, or null
+    __device__ int table(int layer, int e) const {
+        if (layer == a->layer) return trow0[e];
+        if (trow1 && layer == a->layer + 1) return trow1[e];
+        return a->table[layer * a->E + e];
+    }
+    __device__ void set_table(int key, int v) const {
+        a->table[key] = v;
+        const int l = key / a->E, e = key % a->E;
+        if (l == a->layer) trow0[e] = v;
+        else if (trow1 && l == a->layer + 1) trow1[e] = v;
+    }
+    __device__ unsigned long long stamp(int s) const { return st_s ? st_s[s] : a->stamp[s]; }
+    __device__ void set_stamp(int s, unsigned long long v) const {
+        a->stamp[s] = v;
+        if (st_s) st_s[s] = v;
+    }
+    __device__ int owner(int s) const { return own_s ? own_s[s] : a->owner[s]; }
+    __device__ void set_owner(int s, int v) const {
+        a->owner[s] = v;
+        if (own_s) own_s[s] = v;
+    }
+};
 
 __device__ __forceinline__ unsigned long long slot_key(unsigned long long stamp, int s) {
     return (stamp << 14) | static_cast<unsigned long long>(s);
@@ -255,22 +407,22 @@ __device__ __forceinline__ unsigned long long slot_key(unsigned long long stamp,
 
 // members: the batch's experts (ascending), or nullptr for 0..n-1.
 // Returns the number of misses, or -1 (not enough slots; nothing changed).
-__device__ int lru_batch(const CallArgs& a, LruShared& sm, unsigned long long* keys, int layer,
+__device__ int lru_batch(const CallArgs& a, const LruView& lv, LruShared& sm, unsigned long long* keys, int layer,
                          const int32_t* members, int n, const int32_t* protect, int n_protect, int protect_layer) {
-    const int tid = threadIdx.x, nthr = blockDim.x, S = a.S, E = a.E;
+    const int tid = threadIdx.x, nthr = blockDim.x, S = a.S;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     for (int i = tid; i < (S + 31) / 32; i += nthr) sm.blocked[i] = 0u;
     if (tid == 0) sm.n_free = 0;
     __syncthreads();
     for (int p = tid; p < n; p += nthr) {
         const int e = members ? members[p] : p;
-        const int s = a.table[layer * E + e];
+        const int s = lv.table(layer, e);
         sm.member_slot[p] = s;
         sm.member_old[p] = -1;
         if (s >= 0) atomicOr(&sm.blocked[s >> 5], 1u << (s & 31));
     }
     for (int q = tid; q < n_protect; q += nthr) {
-        const int s = a.table[protect_layer * E + protect[q]];
+        const int s = lv.table(protect_layer, protect[q]);
         if (s >= 0) atomicOr(&sm.blocked[s >> 5], 1u << (s & 31));
     }
     __syncthreads();
@@ -301,22 +453,17 @@ __device__ int lru_batch(const CallArgs& a, LruShared& sm, unsigned long long* k
     __syncthreads();
     const int m = running;
     if (m > sm.n_free) return -1;
-    if (tid == 0) {
-        sm.clock = *a.clock + 1;
-        *a.clock = sm.clock;
-    }
-    __syncthreads();
-    const unsigned long long c = sm.clock;
+    const unsigned long long c = sm.clock + 1;
     // hits restamp
     for (int p = tid; p < n; p += nthr)
-        if (sm.member_slot[p] >= 0) a.stamp[sm.member_slot[p]] = (c << 16) | static_cast<unsigned long long>(p);
+        if (sm.member_slot[p] >= 0) lv.set_stamp(sm.member_slot[p], (c << 16) | static_cast<unsigned long long>(p));
     if (m > 0) {
         // keys of the candidate slots; blocked slots never win
         int P = 1;
         while (P < S) P <<= 1;
         const int span = m <= 32 ? S : P;
         for (int s = tid; s < span; s += nthr)
-            keys[s] = (s < S && !((sm.blocked[s >> 5] >> (s & 31)) & 1u)) ? slot_key(a.stamp[s], s) : ~0ull;
+            keys[s] = (s < S && !((sm.blocked[s >> 5] >> (s & 31)) & 1u)) ? slot_key(lv.stamp(s), s) : ~0ull;
         __syncthreads();
         if (m <= 32) {
             // m rounds of a block-wide minimum; slot s is only ever read by thread s mod nthr
@@ -353,19 +500,24 @@ __device__ int lru_batch(const CallArgs& a, LruShared& sm, unsigned long long* k
         }
         __syncthreads();
     }
-    // fill the victims
+    // fill the victims (distinct slots; the evicted keys are not members)
     for (int r = tid; r < m; r += nthr) {
         const int p = sm.miss_p[r];
         const int v = sm.victim[r];
         const int e = members ? members[p] : p;
-        const int32_t key = layer * E + e;
-        const int32_t old = a.owner[v];
-        if (old >= 0) a.table[old] = -1;
-        a.owner[v] = key;
-        a.table[key] = v;
-        a.stamp[v] = (c << 16) | static_cast<unsigned long long>(p);
+        const int32_t key = layer * a.E + e;
+        const int32_t old = lv.owner(v);
+        if (old >= 0) lv.set_table(old, -1);
+        lv.set_owner(v, key);
+        lv.set_table(key, v);
+        lv.set_stamp(v, (c << 16) | static_cast<unsigned long long>(p));
         sm.member_slot[p] = v;
         sm.member_old[p] = old;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        sm.clock = c;
+        *a.clock = c;
     }
     __syncthreads();
     return m;
@@ -397,14 +549,86 @@ __device__ __forceinline__ void block_scan2(int va, int vb, int& ea, int& eb, in
     __syncthreads();
 }
 
+// layout of the work area behind RouteShared: [keys | per-warp counts] (a union:
+// the permutation is done before the cache lookup), then the stamp and owner
+// copies of a small pool
+__host__ __device__ inline size_t route_area_union(int S, int E) {
+    size_t P = 1;
+    while (P < static_cast<size_t>(S)) P <<= 1;
+    const size_t keys = P * 8, wc = static_cast<size_t>(kRouteWarps) * E * 4;
+    return (keys > wc ? keys : wc);
+}
+
+__host__ __device__ inline size_t route_area_bytes(int S, int E) {
+    return route_area_union(S, E) + (S <= kLruCachedSlots ? static_cast<size_t>(S) * 12 : 0);
+}
+
 // --------------------------------------------------------------------------
 // phase B: everything after the logits (and, for prefill, the top-k)
 // --------------------------------------------------------------------------
 
 __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char* area, bool decode) {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.T, E = a.E, k = a.k, n = T * k;
+    const int T = a.T, E = a.E, k = a.k, n = T * k, S = a.S;
     CallInfo* info = a.info;
+    LruShared& sm = rs.lru;
+    // start every independent load of the cache state now: one round trip
+    const bool pf_possible = a.prefetch && T > kDecodeMaxT && a.layer + 1 < a.L;
+    const bool cached = S <= kLruCachedSlots;
+    LruView lv;
+    lv.a = &a;
+    lv.trow0 = rs.trow[0];
+    lv.trow1 = pf_possible ? rs.trow[1] : nullptr;
+    unsigned long long* st_s = reinterpret_cast<unsigned long long*>(area + route_area_union(S, E));
+    int32_t* own_s = reinterpret_cast<int32_t*>(st_s + S);
+    lv.st_s = cached ? st_s : nullptr;
+    lv.own_s = cached ? own_s : nullptr;
+    {
+        // every thread issues all its loads before its first store
+        constexpr int kB = 8;
+        const unsigned long long clock = tid == 0 ? *a.clock : 0ull;
+        for (int e0 = tid; e0 < E; e0 += nthr * 2) {
+            int32_t v[2][2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = e0 + i * nthr;
+                if (e < E) {
+                    v[i][0] = a.table[a.layer * E + e];
+                    v[i][1] = pf_possible ? a.table[(a.layer + 1) * E + e] : -1;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = e0 + i * nthr;
+                if (e < E) {
+                    rs.trow[0][e] = v[i][0];
+                    rs.trow[1][e] = v[i][1];
+                }
+            }
+        }
+        if (cached)
+            for (int s0 = tid; s0 < S; s0 += nthr * kB) {
+                unsigned long long sv[kB];
+                int32_t ov[kB];
+#pragma unroll
+                for (int i = 0; i < kB; ++i) {
+                    const int s = s0 + i * nthr;
+                    if (s < S) {
+                        sv[i] = a.stamp[s];
+                        ov[i] = a.owner[s];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kB; ++i) {
+                    const int s = s0 + i * nthr;
+                    if (s < S) {
+                        st_s[s] = sv[i];
+                        own_s[s] = ov[i];
+                    }
+                }
+            }
+        if (tid == 0) sm.clock = clock;
+    }
     // decode: top-k of every token (one warp each)
     if (decode) {
         if (warp < T) {
@@ -426,7 +650,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     auto gate_at = [&](int i) -> float { return decode ? rs.gates[i] : __ldcg(a.gates + i); };
     for (int i = tid; i < n; i += nthr) atomicAdd(&rs.cnt[topk_at(i)], 1);
     __syncthreads();
-    // offsets (exclusive) and the active list: each thread owns experts 2*tid, 2*tid+1, ...
+    // offsets (exclusive) and the active list: each thread owns `per` consecutive experts
     const int per = (E + nthr - 1) / nthr;
     {
         int sc = 0, sz = 0;
@@ -441,6 +665,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
             if (e < E) {
                 const int c = rs.cnt[e];
                 rs.off[e] = ec;
+                rs.e2u[e] = c > 0 ? ez : -1;
                 a.offsets[e] = ec;
                 a.counts[e] = c;
                 a.e2u[e] = c > 0 ? ez : -1;
@@ -449,6 +674,11 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
                     a.act_expert[ez] = e;
                     a.act_row0[ez] = ec;
                     a.act_cnt[ez] = c;
+                    if (decode) {
+                        DecExpert* d = reinterpret_cast<DecExpert*>(a.dplan + kDecPlanHeader) + ez;
+                        d->row0 = ec;
+                        d->cnt = c;
+                    }
                 }
                 ec += c;
                 ez += c > 0;
@@ -468,6 +698,16 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         const int chunk = (n + nwarps - 1) / nwarps;
         const int a0 = min(n, warp * chunk), a1 = min(n, a0 + chunk);
         for (int i = tid; i < nwarps * E; i += nthr) wc[i] = 0;
+        if (decode) {
+            // plan token tables of the routed experts: empty until the permutation fills them
+            DecExpert* dp = reinterpret_cast<DecExpert*>(a.dplan + kDecPlanHeader);
+            for (int i = tid; i < rs.nu * kDecodeMaxT; i += nthr) {
+                DecExpert& d = dp[i / kDecodeMaxT];
+                d.tok[i % kDecodeMaxT] = -1;
+                d.hrow[i % kDecodeMaxT] = -1;
+                d.gate[i % kDecodeMaxT] = 0.0f;
+            }
+        }
         __syncthreads();
         for (int i = a0 + lane; i < a1; i += 32) atomicAdd(&wc[warp * E + topk_at(i)], 1);
         __syncthreads();
@@ -497,25 +737,34 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
                 a.inv_perm[i] = row;
                 a.row_tok[row] = t;
                 a.row_gate[row] = gate_at(i);
-                if (decode) a.tok_row[a.e2u[e] * kDecodeMaxT + t] = row;
+                if (decode) {
+                    const int u = rs.e2u[e];
+                    a.tok_row[u * kDecodeMaxT + t] = row;
+                    DecExpert& d = reinterpret_cast<DecExpert*>(a.dplan + kDecPlanHeader)[u];
+                    d.tok[row - rs.off[e]] = t;
+                    d.gate[row - rs.off[e]] = gate_at(i);
+                    d.hrow[t] = row;
+                }
             }
         }
     }
     __syncthreads();
     // LRU: demand batch of this layer's experts
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(area);
-    LruShared& sm = rs.lru;
     const int nu = rs.nu;
-    const int m = lru_batch(a, sm, keys, a.layer, rs.members, nu, nullptr, 0, 0);
+    const int m = lru_batch(a, lv, sm, keys, a.layer, rs.members, nu, nullptr, 0, 0);
     if (m < 0) {
         if (tid == 0) {
             info->n_uniq = nu;
             info->n_hit = info->n_miss = info->n_pf = info->n_pf_hit = info->n_pf_miss = 0;
             info->n_events = 0;
             info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
-            *a.n_active = 0;
-            __threadfence_system();
             info->status = -4;  // MOE_ERR_CAPACITY
+            *a.n_active = 0;
+            if (decode) *reinterpret_cast<int32_t*>(a.dplan) = 0;
+            if (a.self_release) *a.ready = a.seq;
+            __threadfence_system();
+            info->done = a.seq;
         }
         return;
     }
@@ -523,10 +772,13 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         const int s = sm.member_slot[p];
         a.act_ptr[p] = a.pool + static_cast<size_t>(s) * a.lay.bytes;
         a.act_slot[p] = s;
+        if (decode) reinterpret_cast<DecExpert*>(a.dplan + kDecPlanHeader)[p].ptr = a.act_ptr[p];
+    }
+    for (int p = tid; p < nu; p += nthr) {
         info->ev_layer[p] = a.layer;
         info->ev_expert[p] = rs.members[p];
         info->ev_hit[p] = 1;
-        info->ev_slot[p] = s;
+        info->ev_slot[p] = sm.member_slot[p];
         info->ev_evicted[p] = sm.member_old[p];
         info->ev_prefetch[p] = 0;
     }
@@ -540,9 +792,9 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     }
     __syncthreads();
     int n_pf = 0, m_pf = 0;
-    const bool do_pf = a.prefetch && T > kDecodeMaxT && a.layer + 1 < a.L && a.S >= nu + E;
+    const bool do_pf = pf_possible && a.S >= nu + E;
     if (do_pf) {
-        m_pf = lru_batch(a, sm, keys, a.layer + 1, nullptr, E, rs.members, nu, a.layer);
+        m_pf = lru_batch(a, lv, sm, keys, a.layer + 1, nullptr, E, rs.members, nu, a.layer);
         n_pf = E;
         if (m_pf < 0) { m_pf = 0; n_pf = 0; }  // cannot happen when S >= nu + E
         for (int p = tid; p < n_pf; p += nthr) {
@@ -577,7 +829,20 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
             a.row_gate[T * k + s * T + t] = 1.0f;
             if (decode) a.tok_row[u * kDecodeMaxT + t] = T * k + s * T + t;
         }
+        if (decode && tid < kDecodeMaxT) {
+            DecExpert& d = reinterpret_cast<DecExpert*>(a.dplan + kDecPlanHeader)[u];
+            const int t = tid;
+            d.tok[t] = t < T ? t : -1;
+            d.hrow[t] = t < T ? T * k + s * T + t : -1;
+            d.gate[t] = t < T ? 1.0f : 0.0f;
+            if (t == 0) {
+                d.ptr = a.shared_base + static_cast<size_t>(s) * a.lay.bytes;
+                d.row0 = T * k + s * T;
+                d.cnt = T;
+            }
+        }
     }
+    if (decode && tid == 0) *reinterpret_cast<int32_t*>(a.dplan) = nu + a.n_shared;
     __syncthreads();
     if (tid == 0) {
         *a.n_active = nu + a.n_shared;
@@ -589,8 +854,10 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         info->n_pf_miss = m_pf;
         info->n_events = nu + n_pf;
         info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
-        __threadfence_system();
         info->status = 0;
+        if (a.self_release && m == 0) *a.ready = a.seq;
+        __threadfence_system();
+        info->done = a.seq;
     }
 }
 
@@ -607,20 +874,17 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
     // ---------------- phase A
     if constexpr (DECODE) {
-        // x rows [T][H] in shared memory; warp w: expert blockIdx.x * 16 + w
-        {
-            const size_t bytes = static_cast<size_t>(T) * H * esz;
-            const uint4* src = reinterpret_cast<const uint4*>(a.hidden);
-            uint4* dst = reinterpret_cast<uint4*>(route_smem);
-            for (size_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) dst[i] = src[i];
-        }
-        xprep_rows<ACT>(a.hidden, a.xh, a.fmt, H, 0, T, static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x,
-                        static_cast<size_t>(gridDim.x) * blockDim.x);
-        __syncthreads();
+        // warp w: expert blockIdx.x * 16 + w. Its first router chunks are loaded
+        // before the x rows [T][H] are staged, so both share one round trip.
+        constexpr int NB = ACT == ACT_BF16 ? 8 : 4;  // chunks per lane per round trip
         const int e0 = blockIdx.x * kRouteWarps + warp;
+        RawChunk<ACT> pre[NB][1];
+        router_batch<ACT, 1, NB>(a.router_w, H, E, e0, lane, pre);
+        copy_g2s(route_smem, reinterpret_cast<const unsigned char*>(a.hidden), static_cast<size_t>(T) * H * esz / 16);
+        __syncthreads();
         if (e0 < E) {
             float acc[1][8];
-            warp_logits<ACT, 1>(a.router_w, route_smem, H, E, e0, T, lane, acc);
+            warp_logits<ACT, 1, NB>(a.router_w, route_smem, H, E, e0, T, lane, acc, pre);
             if (lane < T) {
                 float v = acc[0][0];
 #pragma unroll
@@ -628,26 +892,23 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
                 a.logits[static_cast<size_t>(lane) * E + e0] = v;
             }
         }
+        xprep_rows<ACT>(route_smem, a.xh, a.fmt, H, 0, T, static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                        static_cast<size_t>(gridDim.x) * blockDim.x);
     } else {
         // 8 tokens per CTA, all experts; logits [8][E] in shared memory, then top-k
         const int t0 = blockIdx.x * kPrefillTokTile;
         const int nt = min(kPrefillTokTile, T - t0);
         float* lg = reinterpret_cast<float*>(route_smem + static_cast<size_t>(kPrefillTokTile) * H * esz);
-        {
-            const size_t bytes = static_cast<size_t>(nt) * H * esz;
-            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(a.hidden) +
-                                                              static_cast<size_t>(t0) * H * esz);
-            uint4* dst = reinterpret_cast<uint4*>(route_smem);
-            for (size_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) dst[i] = src[i];
-        }
-        if (a.fmt != FMT_BF16) xprep_rows<ACT>(a.hidden, a.xh, a.fmt, H, t0, t0 + nt, threadIdx.x, blockDim.x);
+        copy_g2s(route_smem, reinterpret_cast<const unsigned char*>(a.hidden) + static_cast<size_t>(t0) * H * esz,
+                 static_cast<size_t>(nt) * H * esz / 16);
         __syncthreads();
+        if (a.fmt != FMT_BF16) xprep_rows<ACT>(route_smem, a.xh, a.fmt, H, t0, nt, threadIdx.x, blockDim.x);
         constexpr int kPass = kRouteWarps * kPrefillEpw;
         for (int eb = 0; eb < E; eb += kPass) {
             const int e0 = eb + warp * kPrefillEpw;
             if (e0 < E) {
                 float acc[kPrefillEpw][8];
-                warp_logits<ACT, kPrefillEpw>(a.router_w, route_smem, H, E, e0, nt, lane, acc);
+                warp_logits<ACT, kPrefillEpw, 1>(a.router_w, route_smem, H, E, e0, nt, lane, acc);
                 if (lane == 0) {
 #pragma unroll
                     for (int e = 0; e < kPrefillEpw; ++e)
@@ -690,10 +951,7 @@ static size_t route_smem_bytes(const CallArgs& a, bool decode) {
     const size_t phase_a = decode ? static_cast<size_t>(a.T) * a.H * esz
                                   : static_cast<size_t>(kPrefillTokTile) * a.H * esz +
                                         static_cast<size_t>(kPrefillTokTile) * a.E * 4;
-    size_t P = 1;
-    while (P < static_cast<size_t>(a.S)) P <<= 1;
-    const size_t area = std::max(P * 8, static_cast<size_t>(kRouteWarps) * a.E * 4);
-    return std::max(phase_a, kRouteSharedBytes + area);
+    return std::max(phase_a, kRouteSharedBytes + route_area_bytes(a.S, a.E));
 }
 
 // the opt-in per-block limit is 227 KB including static shared memory

@@ -7,14 +7,35 @@
 // PCIe, and prefill streams the next layer's experts while the current layer
 // computes. Cache resizing happens at a safe point (moe_cache_config), as the
 // same page describes for the scheduler's safe points.
+//
+// Miss pipeline. moe_layer_forward only enqueues work: the routing kernel (which
+// also runs the cache lookup) and the expert kernels of call number `seq` go on
+// the caller's stream back to back, and the expert kernels wait on the device
+// until a "ready" word reaches seq. The routing kernel writes the call's record
+// (hits, misses with their slots, events) into a ring of mapped host memory. A
+// service thread per handle reads the records in call order; for a call with
+// misses it issues one cudaMemcpyAsync per missed expert (pinned bank -> pool
+// slot) on the copy stream and then writes `ready = seq` on the same stream, so
+// the expert kernels start once the copies have landed. A call whose experts
+// all hit releases itself from inside the routing kernel, and the host is not
+// on its critical path at all. Prefill prefetch copies of layer+1 go on the
+// copy stream after the call's own release, and the next call is then released
+// by the service thread behind them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <condition_variable>
 #include <cstdio>
-#include <deque>
+#include <cstdlib>
 #include <cstring>
+#include <deque>
+#include <mutex>
 #include <new>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "../../include/moe.h"
@@ -28,12 +49,28 @@ using moe::BlobLayout;
 using moe::CallArgs;
 using moe::CallInfo;
 
+namespace {
+
+constexpr int kRing = 16;  // calls in flight between the caller and the service thread
+typedef CUresult (*WriteValue64Fn)(CUstream, CUdeviceptr, cuuint64_t, unsigned int);
+
+}  // namespace
+
 // CUDA events of one timed forward call
 struct TimedCall {
+    uint64_t seq = 0;
     cudaEvent_t r0 = nullptr, r1 = nullptr, f0 = nullptr, f1 = nullptr, f2 = nullptr, f3 = nullptr;
     cudaEvent_t c0 = nullptr, c1 = nullptr;
-    bool has_copy = false, has_combine = false;
+    bool has_copy = false, has_combine = false, had_miss = false;
     uint64_t gu_bytes = 0, down_bytes = 0, combine_bytes = 0, copy_bytes = 0;
+};
+
+// one enqueued call, as the service thread sees it
+struct PendingCall {
+    uint64_t seq = 0;
+    int layer = 0, T = 0;
+    bool self_release = true;
+    TimedCall* tc = nullptr;
 };
 
 struct moe_handle {
@@ -59,21 +96,42 @@ struct moe_handle {
     moe::UmmaMaps maps{};
     int num_sms = 148;
     CallArgs base{};
+    // call records (mapped ring) and the ready word
     CallInfo* info_h = nullptr;
     CallInfo* info_d = nullptr;
+    unsigned long long* ready = nullptr;       // device
+    unsigned long long* ready_vals = nullptr;  // pinned host [kRing] (used without cuStreamWriteValue64)
+    WriteValue64Fn write64 = nullptr;
+    unsigned long long wait_ns = 5000000000ull;
+    // host-side fault injection (MOE_FAULT=drop_release): the service thread
+    // skips the release of the first call that has misses, so that its expert
+    // kernels run into their bounded wait
+    bool fault_drop_release = false;
+    bool log = false;  // MOE_LOG: one stderr line per serviced call
     // streams / events
     cudaStream_t stream = nullptr, copy = nullptr;
-    cudaEvent_t ev_cache = nullptr, ev_copy = nullptr, ev_prefetch = nullptr;
-    bool prefetch_pending = false;
-    // last call
+    // enqueue side (caller's thread)
+    uint64_t submitted = 0;
+    bool prefetch_may_be_pending = false;
     int last_T = 0;
     cudaStream_t last_stream = nullptr;
+    // service thread
+    std::thread svc;
+    std::mutex mu;
+    std::condition_variable cv, done_cv;
+    std::deque<PendingCall> queue;
+    std::atomic<uint64_t> serviced{0};
+    bool stop = false;
+    // errors found while servicing, reported by the next call (mu)
+    int pending_err = MOE_OK;
+    std::string pending_msg;
+    bool sticky_timeout = false;
     // timing
     bool timing = false;
     moe_timing_t tm{};
     std::deque<TimedCall*> pending;
     std::vector<TimedCall*> spare;
-    // stats
+    // stats (mu)
     moe_stats_t st{};
     std::vector<moe_event> events;
     std::string err;
@@ -129,21 +187,19 @@ BlobLayout layout_for(const moe_model_desc& d) {
         case moe::FMT_FP32:
             L.gu = 0; o = 2 * I * H * 4;
             L.d = align_up(o, 256); o = L.d + H * I * 4;
-            L.gus = L.ds = L.gsc = align_up(o, 256); o = L.gsc + 16;
+            L.gsc = align_up(o, 256); o = L.gsc + 16;
             break;
         case moe::FMT_BF16:
             L.gu = 0; o = 2 * I * H * 2;
             L.d = align_up(o, 256); o = L.d + H * I * 2;
-            L.gus = L.ds = L.gsc = align_up(o, 256); o = L.gsc + 16;
+            L.gsc = align_up(o, 256); o = L.gsc + 16;
             break;
         default: {
-            const size_t blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
-            L.gus_pitch = align_up(H / blk, 16);
-            L.ds_pitch = align_up(I / blk, 16);
-            L.gu = 0; o = 2 * I * H / 2;
-            L.d = align_up(o, 256); o = L.d + H * I / 2;
-            L.gus = align_up(o, 256); o = L.gus + 2 * I * L.gus_pitch;
-            L.ds = align_up(o, 256); o = L.ds + H * L.ds_pitch;
+            L.sbpg = d.weight_fmt == moe::FMT_NVFP4 ? 8 : 4;
+            L.gu_tile = static_cast<size_t>(moe::kTileRows) * (H / moe::kGroupK) * (64 + L.sbpg);
+            L.d_tile = static_cast<size_t>(moe::kTileRows) * (I / moe::kGroupK) * (64 + L.sbpg);
+            L.gu = 0; o = (I / 8) * L.gu_tile;
+            L.d = align_up(o, 256); o = L.d + (H / moe::kTileRows) * L.d_tile;
             L.gsc = align_up(o, 256); o = L.gsc + 16;
         }
     }
@@ -210,24 +266,36 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
             break;
         }
         default: {
+            // device-order rows, scattered into 16-row tiles of 1024-element chunks
             const int blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
-            uint8_t* gu = blob + L.gu;
-            uint8_t* gus = blob + L.gus;
+            const int sbpg = L.sbpg;
+            std::vector<uint8_t> drow(std::max(H, I) / 2);
+            auto put_row = [&](uint8_t* tile, int r, const uint8_t* codes, const uint8_t* scales, int K) {
+                reorder_row_fp4(codes, drow.data(), K);
+                const int G = K / moe::kGroupK;
+                for (int c = 0; c * moe::kChunkGroups < G; ++c) {
+                    const int ng = moe::fp4_chunk_groups(G, c);
+                    uint8_t* chunk = tile + moe::fp4_chunk_off(c, sbpg);
+                    for (int w = 0; w < ng; ++w) {
+                        const int j = c * moe::kChunkGroups + w;
+                        for (int q = 0; q < 4; ++q)
+                            std::memcpy(chunk + moe::fp4_code_off(ng, r, w, q), drow.data() + j * 64 + 16 * q, 16);
+                        std::memcpy(chunk + moe::fp4_scale_off(ng, sbpg, r, w), scales + static_cast<size_t>(j) * (128 / blk),
+                                    128 / blk);
+                    }
+                }
+            };
             for (int which = 0; which < 2; ++which) {
                 const uint8_t* src = static_cast<const uint8_t*>(ts[which]->data);
                 const uint8_t* sc = ts[which]->scales;
-                for (int i = 0; i < I; ++i) {
-                    const size_t dr = gu_row(i, which);
-                    reorder_row_fp4(src + static_cast<size_t>(i) * H / 2, gu + dr * H / 2, H);
-                    std::memcpy(gus + dr * L.gus_pitch, sc + static_cast<size_t>(i) * (H / blk), H / blk);
-                }
+                for (int i = 0; i < I; ++i)
+                    put_row(blob + L.gu + static_cast<size_t>(i / 8) * L.gu_tile, 8 * which + i % 8,
+                            src + static_cast<size_t>(i) * H / 2, sc + static_cast<size_t>(i) * (H / blk), H);
             }
             const uint8_t* src = static_cast<const uint8_t*>(w->down.data);
             for (int r = 0; r < H; ++r)
-                reorder_row_fp4(src + static_cast<size_t>(r) * I / 2, blob + L.d + static_cast<size_t>(r) * I / 2, I);
-            for (int r = 0; r < H; ++r)
-                std::memcpy(blob + L.ds + static_cast<size_t>(r) * L.ds_pitch, w->down.scales + static_cast<size_t>(r) * (I / blk),
-                            I / blk);
+                put_row(blob + L.d + static_cast<size_t>(r / moe::kTileRows) * L.d_tile, r % moe::kTileRows,
+                        src + static_cast<size_t>(r) * I / 2, w->down.scales + static_cast<size_t>(r) * (I / blk), I);
             if (d.weight_fmt == moe::FMT_NVFP4) {
                 gsc[0] = w->gate.global_scale;
                 gsc[1] = w->up.global_scale;
@@ -251,7 +319,8 @@ TimedCall* acquire_timed(moe_handle* h) {
     if (!h->spare.empty()) {
         TimedCall* t = h->spare.back();
         h->spare.pop_back();
-        t->has_copy = t->has_combine = false;
+        t->has_copy = t->has_combine = t->had_miss = false;
+        t->gu_bytes = t->down_bytes = t->combine_bytes = t->copy_bytes = 0;
         return t;
     }
     TimedCall* t = new (std::nothrow) TimedCall();
@@ -271,10 +340,12 @@ float elapsed(cudaEvent_t a, cudaEvent_t b) {
     return ms;
 }
 
-// folds finished timed calls into the totals; wait = block until all finished
+// folds finished (and serviced) timed calls into the totals; wait = block until all finished
 void harvest(moe_handle* h, bool wait) {
+    const uint64_t done = h->serviced.load(std::memory_order_acquire);
     while (!h->pending.empty()) {
         TimedCall* t = h->pending.front();
+        if (t->seq > done) break;
         cudaEvent_t last = t->has_combine ? t->f3 : t->f2;
         if (wait) {
             cudaEventSynchronize(last);
@@ -285,13 +356,17 @@ void harvest(moe_handle* h, bool wait) {
         }
         h->tm.calls++;
         h->tm.route_ms += elapsed(t->r0, t->r1);
-        h->tm.gate_up_ms += elapsed(t->f0, t->f1);
-        h->tm.down_ms += elapsed(t->f1, t->f2);
-        if (t->has_combine) h->tm.combine_ms += elapsed(t->f2, t->f3);
+        if (!t->had_miss) {
+            // expert kernels of calls without demand misses: pure kernel time
+            h->tm.resident_calls++;
+            h->tm.gate_up_ms += elapsed(t->f0, t->f1);
+            h->tm.down_ms += elapsed(t->f1, t->f2);
+            if (t->has_combine) h->tm.combine_ms += elapsed(t->f2, t->f3);
+            h->tm.gate_up_bytes += t->gu_bytes;
+            h->tm.down_bytes += t->down_bytes;
+            h->tm.combine_bytes += t->combine_bytes;
+        }
         if (t->has_copy) h->tm.copy_ms += elapsed(t->c0, t->c1);
-        h->tm.gate_up_bytes += t->gu_bytes;
-        h->tm.down_bytes += t->down_bytes;
-        h->tm.combine_bytes += t->combine_bytes;
         h->tm.copy_bytes += t->copy_bytes;
         h->pending.pop_front();
         h->spare.push_back(t);
@@ -309,6 +384,190 @@ void free_timed(moe_handle* h) {
     for (auto* t : h->spare) kill(t);
     h->pending.clear();
     h->spare.clear();
+}
+
+inline void cpu_relax() {
+#if defined(__x86_64__) || defined(__i386__)
+    __builtin_ia32_pause();
+#endif
+}
+
+void record_error(moe_handle* h, int code, const std::string& msg) {
+    std::lock_guard<std::mutex> lk(h->mu);
+    if (code == MOE_ERR_TIMEOUT) h->sticky_timeout = true;
+    if (h->pending_err == MOE_OK || code == MOE_ERR_TIMEOUT) {
+        h->pending_err = code;
+        h->pending_msg = msg;
+    }
+}
+
+// writes `ready = seq` on the copy stream, behind every copy issued before it
+cudaError_t post_ready(moe_handle* h, uint64_t seq) {
+    if (h->write64) {
+        const CUresult r = h->write64(reinterpret_cast<CUstream>(h->copy), reinterpret_cast<CUdeviceptr>(h->ready),
+                                      static_cast<cuuint64_t>(seq), 0);
+        return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+    }
+    unsigned long long* v = h->ready_vals + (seq % kRing);
+    *v = seq;
+    return cudaMemcpyAsync(h->ready, v, 8, cudaMemcpyHostToDevice, h->copy);
+}
+
+// the service thread's work for one call
+void service_call(moe_handle* h, const PendingCall& pc) {
+    volatile CallInfo* inf = h->info_h + (pc.seq % kRing);
+    // wait for the call's routing kernel: spin while it is near, then back off
+    const auto t0 = std::chrono::steady_clock::now();
+    uint64_t spins = 0;
+    while (inf->done != pc.seq) {
+        if (++spins < 200000) {
+            cpu_relax();
+            continue;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(120)) {
+            record_error(h, MOE_ERR_TIMEOUT, "the routing kernel of a call did not report back");
+            return;
+        }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    const int status = inf->status;
+    const int nm = inf->n_miss, npm = inf->n_pf_miss, nu = inf->n_uniq;
+    const bool kernel_released = pc.self_release && nm == 0;
+    if (status == MOE_ERR_CAPACITY)
+        record_error(h, MOE_ERR_CAPACITY, "the layer's experts do not fit in the expert pool");
+    else if (status != 0)
+        record_error(h, MOE_ERR_CUDA, "the routing kernel reported an unknown status");
+    if (inf->dev_err != 0)
+        record_error(h, MOE_ERR_TIMEOUT, "a kernel gave up a bounded wait (device error " +
+                                             std::to_string(inf->dev_err) + "); call moe_cache_config to reset");
+    const size_t B = h->lay.bytes;
+    TimedCall* tc = pc.tc;
+    cudaError_t ce = cudaSuccess;
+    if (tc && nm + npm > 0) {
+        cudaEventRecord(tc->c0, h->copy);
+        tc->has_copy = true;
+    }
+    for (int i = 0; i < nm && ce == cudaSuccess; ++i) {
+        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
+        ce = cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
+                             cudaMemcpyHostToDevice, h->copy);
+    }
+    if (ce == cudaSuccess && !kernel_released) {
+        if (h->fault_drop_release && nm > 0) h->fault_drop_release = false;
+        else ce = post_ready(h, pc.seq);
+    }
+    for (int i = nm; i < nm + npm && ce == cudaSuccess; ++i) {
+        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
+        ce = cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
+                             cudaMemcpyHostToDevice, h->copy);
+    }
+    if (tc && tc->has_copy) cudaEventRecord(tc->c1, h->copy);
+    if (h->log)
+        std::fprintf(stderr, "[moe] call %llu layer %d T %d status %d uniq %d miss %d pf_miss %d self_release %d "
+                             "kernel_released %d copy_err %d dev_err %d\n",
+                     static_cast<unsigned long long>(pc.seq), pc.layer, pc.T, status, nu, nm, npm,
+                     pc.self_release ? 1 : 0, kernel_released ? 1 : 0, static_cast<int>(ce), inf->dev_err);
+    if (ce != cudaSuccess) {
+        record_error(h, MOE_ERR_CUDA, std::string("expert copy: ") + cudaGetErrorString(ce));
+        cudaGetLastError();
+    }
+    if (tc) {
+        // algorithmic bytes of this call
+        const uint64_t H = h->d.hidden, I = h->d.inter, k = h->d.top_k, ns = h->d.num_shared, T = pc.T;
+        const uint64_t na = static_cast<uint64_t>(nu) + ns;
+        const uint64_t rows = T * (k + ns);
+        const uint64_t ea = h->d.act_dtype == moe::ACT_BF16 ? 2 : 4;
+        const uint64_t he = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
+        uint64_t wgu, wd;
+        switch (h->d.weight_fmt) {
+            case moe::FMT_FP32: wgu = 2 * I * H * 4; wd = H * I * 4; break;
+            case moe::FMT_BF16: wgu = 2 * I * H * 2; wd = H * I * 2; break;
+            default: {
+                const uint64_t blk = h->d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
+                wgu = 2 * I * H / 2 + 2 * I * H / blk;
+                wd = H * I / 2 + H * I / blk;
+            }
+        }
+        tc->had_miss = nm > 0;
+        tc->gu_bytes = na * wgu + T * H * ea + rows * I * he;
+        tc->down_bytes = na * wd + rows * I * he + (tc->has_combine ? rows * H * 2 : T * H * ea);
+        tc->combine_bytes = tc->has_combine ? rows * H * 2 + T * H * ea : 0;
+        tc->copy_bytes = static_cast<uint64_t>(nm + npm) * B;
+    }
+    std::lock_guard<std::mutex> lk(h->mu);
+    h->st.calls++;
+    (pc.T <= moe::kDecodeMaxT ? h->st.decode_calls : h->st.prefill_calls)++;
+    if (status == 0) {
+        h->st.hits += inf->n_hit;
+        h->st.misses += nm;
+        h->st.prefetch_hits += inf->n_pf_hit;
+        h->st.prefetch_misses += npm;
+        h->st.copies_h2d += nm + npm;
+        h->st.bytes_h2d += static_cast<uint64_t>(nm + npm) * B;
+        const int nev = inf->n_events;
+        for (int i = 0; i < nev; ++i) {
+            if (inf->ev_evicted[i] >= 0) h->st.evictions++;
+            if (h->flags & MOE_CACHE_LOG_EVENTS) {
+                moe_event ev{inf->ev_layer[i], inf->ev_expert[i], inf->ev_hit[i], inf->ev_slot[i], inf->ev_evicted[i],
+                             inf->ev_prefetch[i]};
+                h->events.push_back(ev);
+            }
+        }
+    } else {
+        h->st.device_errors++;
+    }
+    if (inf->dev_err != 0) h->st.device_errors++;
+}
+
+void service_loop(moe_handle* h) {
+    cudaSetDevice(h->d.device);
+    for (;;) {
+        PendingCall pc;
+        {
+            std::unique_lock<std::mutex> lk(h->mu);
+            h->cv.wait(lk, [&] { return h->stop || !h->queue.empty(); });
+            if (h->queue.empty()) return;  // stopping, and every call has been serviced
+            pc = h->queue.front();
+        }
+        service_call(h, pc);
+        {
+            std::lock_guard<std::mutex> lk(h->mu);
+            h->queue.pop_front();
+            h->serviced.store(pc.seq, std::memory_order_release);
+        }
+        h->done_cv.notify_all();
+    }
+}
+
+// waits until the service thread has handled every enqueued call
+void drain(moe_handle* h) {
+    std::unique_lock<std::mutex> lk(h->mu);
+    h->done_cv.wait(lk, [&] { return h->serviced.load(std::memory_order_acquire) >= h->submitted; });
+}
+
+// error found by the service thread for an earlier call; capacity errors are
+// reported once, bounded-wait timeouts until moe_cache_config
+int take_error(moe_handle* h) {
+    std::lock_guard<std::mutex> lk(h->mu);
+    if (h->pending_err == MOE_OK) return MOE_OK;
+    const int e = h->pending_err;
+    h->err = h->pending_msg;
+    if (!h->sticky_timeout) {
+        h->pending_err = MOE_OK;
+        h->pending_msg.clear();
+    }
+    return e;
+}
+
+void stop_service(moe_handle* h) {
+    if (!h->svc.joinable()) return;
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        h->stop = true;
+    }
+    h->cv.notify_all();
+    h->svc.join();
 }
 
 }  // namespace
@@ -335,14 +594,29 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     h->d = *desc;
     h->max_tokens = desc->max_tokens > 0 ? desc->max_tokens : 4096;
     h->lay = layout_for(h->d);
+    if (const char* f = std::getenv("MOE_FAULT")) h->fault_drop_release = std::strcmp(f, "drop_release") == 0;
+    h->log = std::getenv("MOE_LOG") != nullptr;
+    if (const char* w = std::getenv("MOE_WAIT_MS")) {
+        const long ms = std::strtol(w, nullptr, 10);
+        if (ms > 0) h->wait_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
     auto bail = [&](int code) { moe_destroy(h); return code; };
     cudaError_t e = cudaSetDevice(desc->device);
     if (e != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::routing_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::umma_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::decode_fp4_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (moe::experts_preload() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, desc->device) != cudaSuccess)
         return bail(MOE_ERR_CUDA);
+    {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue64", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            h->write64 = reinterpret_cast<WriteValue64Fn>(p);
+        cudaGetLastError();
+    }
     const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared, k = h->d.top_k;
     const size_t H = h->d.hidden, I = h->d.inter, Tm = h->max_tokens;
     h->bank.assign(L, nullptr);
@@ -379,6 +653,8 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {4, reinterpret_cast<void**>(&a.dev_err)},
         {4, reinterpret_cast<void**>(&a.route_done)},
         {8, reinterpret_cast<void**>(&a.grid_bar)},
+        {moe::kDecPlanHeader + static_cast<size_t>(E + ns) * sizeof(moe::DecExpert), reinterpret_cast<void**>(&a.dplan)},
+        {8, reinterpret_cast<void**>(&a.ready)},
         {4, reinterpret_cast<void**>(&a.n_uniq)},
         {4, reinterpret_cast<void**>(&a.n_active)},
         {rows * I * hes, &a.hbuf},
@@ -393,6 +669,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         *p.dst = static_cast<uint8_t*>(h->scratch) + off;
         off += align_up(p.bytes, 256);
     }
+    h->ready = a.ready;
     if (umma) {
         // TMA descriptors over the gathered activations, h, and the resident shared experts
         bool ok = moe::umma_map_2d(&h->maps.x, a.xperm, rows, H, 128) && moe::umma_map_2d(&h->maps.h, a.hbuf, rows, I, 128);
@@ -405,21 +682,26 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         if (!ok) return bail(MOE_ERR_CUDA);
         h->maps.have_io = true;
     }
-    if (cudaHostAlloc(reinterpret_cast<void**>(&h->info_h), sizeof(CallInfo), cudaHostAllocMapped) != cudaSuccess)
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->info_h), sizeof(CallInfo) * kRing, cudaHostAllocMapped) !=
+        cudaSuccess)
         return bail(MOE_ERR_OOM);
-    std::memset(h->info_h, 0, sizeof(CallInfo));
+    std::memset(h->info_h, 0, sizeof(CallInfo) * kRing);
     if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->info_d), h->info_h, 0) != cudaSuccess)
         return bail(MOE_ERR_CUDA);
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->ready_vals), 8 * kRing, cudaHostAllocDefault) != cudaSuccess)
+        return bail(MOE_ERR_OOM);
     if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
-    if (cudaEventCreateWithFlags(&h->ev_cache, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
-    if (cudaEventCreateWithFlags(&h->ev_copy, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
-    if (cudaEventCreateWithFlags(&h->ev_prefetch, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ERR_CUDA);
     a.E = E; a.k = k; a.H = static_cast<int>(H); a.I = static_cast<int>(I); a.n_shared = ns; a.L = L;
     a.fmt = h->d.weight_fmt; a.act = h->d.act_dtype; a.mode = h->d.act_mode;
     a.lay = h->lay;
-    a.info = h->info_d;
+    a.wait_ns = h->wait_ns;
+    try {
+        h->svc = std::thread(service_loop, h);
+    } catch (...) {
+        return bail(MOE_ERR_OOM);
+    }
     *out = h;
     return MOE_OK;
 }
@@ -459,6 +741,7 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     if (capacity_slots < h->d.top_k) return fail(h, MOE_ERR_CAPACITY, "capacity below top_k");
     if (capacity_slots > moe::kMaxSlots) return fail(h, MOE_ERR_INVALID, "capacity above 16384 slots");
     CK(h, cudaSetDevice(h->d.device));
+    drain(h);
     CK(h, cudaDeviceSynchronize());
     free_pool(h);
     const int L = h->d.num_layers, E = h->d.num_experts;
@@ -482,6 +765,9 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     CK(h, cudaMemset(h->base.dev_err, 0, 4));
     CK(h, cudaMemset(h->base.route_done, 0, 4));
     CK(h, cudaMemset(h->base.grid_bar, 0, 8));
+    // the ready word continues from the last serviced call
+    const unsigned long long rv = h->submitted;
+    CK(h, cudaMemcpy(h->ready, &rv, 8, cudaMemcpyHostToDevice));
     CK(h, cudaDeviceSynchronize());
     h->maps.have_pool = false;
     if (h->maps.have_io) {
@@ -497,9 +783,16 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
         }
         h->maps.have_pool = true;
     }
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        h->pending_err = MOE_OK;
+        h->pending_msg.clear();
+        h->sticky_timeout = false;
+        h->events.clear();
+    }
     h->S = capacity_slots;
     h->flags = flags;
-    h->prefetch_pending = false;
+    h->prefetch_may_be_pending = false;
     CallArgs& a = h->base;
     a.table = h->table; a.owner = h->owner; a.stamp = h->stamp; a.clock = h->clock;
     a.pool = h->pool; a.S = h->S;
@@ -511,6 +804,7 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
 int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, int layer_id, int T, void* out,
                       void* stream) {
     if (!h) return MOE_ERR_INVALID;
+    if (const int e = take_error(h)) return e;
     if (!h->pool) return fail(h, MOE_ERR_STATE, "moe_cache_config has not been called");
     const int L = h->d.num_layers, E = h->d.num_experts;
     if (layer_id < 0 || layer_id >= L) return fail(h, MOE_ERR_INVALID, "layer out of range");
@@ -530,6 +824,14 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
                 return fail(h, MOE_ERR_STATE, "next layer has unloaded experts");
     CK(h, cudaSetDevice(h->d.device));
     cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+    const uint64_t seq = h->submitted + 1;
+    // the record slot of call seq - kRing must have been read
+    if (seq > static_cast<uint64_t>(kRing) && h->serviced.load(std::memory_order_acquire) < seq - kRing) {
+        std::unique_lock<std::mutex> lk(h->mu);
+        h->done_cv.wait(lk, [&] { return h->serviced.load(std::memory_order_acquire) >= seq - kRing; });
+    }
+    CallInfo* rec = h->info_h + (seq % kRing);
+    reinterpret_cast<volatile unsigned long long*>(&rec->done)[0] = 0;
     CallArgs a = h->base;
     a.T = T;
     a.layer = layer_id;
@@ -538,117 +840,79 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     a.out = out;
     a.shared_base = h->shared_dev ? h->shared_dev + static_cast<size_t>(layer_id) * h->d.num_shared * h->lay.bytes
                                   : nullptr;
-    h->info_h->status = 1;
+    a.info = h->info_d + (seq % kRing);
+    a.seq = seq;
+    a.self_release = h->prefetch_may_be_pending ? 0 : 1;
     TimedCall* tc = nullptr;
     if (h->timing) {
         harvest(h, false);
         tc = acquire_timed(h);
         if (!tc) return fail(h, MOE_ERR_OOM, "timing events");
+        tc->seq = seq;
         CK(h, cudaEventRecord(tc->r0, s));
     }
     CK(h, moe::launch_route(a, s));
-    h->st.kernel_launches += 1;
-    if (tc) CK(h, cudaEventRecord(tc->r1, s));
-    CK(h, cudaEventRecord(h->ev_cache, s));
-    CK(h, cudaEventSynchronize(h->ev_cache));
-    volatile CallInfo* inf = h->info_h;
-    h->last_T = T;
-    h->last_stream = s;
-    if (inf->status == MOE_ERR_CAPACITY) {
-        h->st.device_errors++;
-        return fail(h, MOE_ERR_CAPACITY, "the layer's experts do not fit in the expert pool");
+    if (tc) {
+        CK(h, cudaEventRecord(tc->r1, s));
+        CK(h, cudaEventRecord(tc->f0, s));
     }
-    if (inf->status != 0) return fail(h, MOE_ERR_CUDA, "cache kernel did not complete");
-    if (inf->dev_err != 0) {
-        h->st.device_errors++;
-        return fail(h, MOE_ERR_TIMEOUT, "an expert kernel gave up a bounded wait (device error " +
-                                            std::to_string(inf->dev_err) + "); call moe_cache_config to reset");
-    }
-    const int nm = inf->n_miss, npm = inf->n_pf_miss;
-    const size_t B = h->lay.bytes;
-    if (tc && nm + npm > 0) {
-        CK(h, cudaEventRecord(tc->c0, h->copy));
-        tc->has_copy = true;
-    }
-    // demand misses: copy, then make the compute stream wait for them
-    for (int i = 0; i < nm; ++i) {
-        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
-        CK(h, cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
-                              cudaMemcpyHostToDevice, h->copy));
-    }
-    if (nm > 0) {
-        CK(h, cudaEventRecord(h->ev_copy, h->copy));
-        CK(h, cudaStreamWaitEvent(s, h->ev_copy, 0));
-    }
-    // experts prefetched by an earlier call must have landed before they are used
-    if (h->prefetch_pending) {
-        CK(h, cudaStreamWaitEvent(s, h->ev_prefetch, 0));
-        h->prefetch_pending = false;
-    }
-    // prefetch of the next layer: streams behind this layer's compute
-    for (int i = nm; i < nm + npm; ++i) {
-        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
-        CK(h, cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
-                              cudaMemcpyHostToDevice, h->copy));
-    }
-    if (npm > 0) {
-        CK(h, cudaEventRecord(h->ev_prefetch, h->copy));
-        h->prefetch_pending = true;
-    }
-    if (tc && tc->has_copy) CK(h, cudaEventRecord(tc->c1, h->copy));
-    if (tc) CK(h, cudaEventRecord(tc->f0, s));
     int nl = 0;
-    CK(h, moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &h->maps, h->num_sms, &nl));
-    h->st.kernel_launches += nl;
+    const cudaError_t le =
+        moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &h->maps, h->num_sms, &nl);
     if (tc) {
         tc->has_combine = !decode && h->d.weight_fmt != moe::FMT_FP32;
         if (tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
-        // algorithmic bytes of this call
-        const uint64_t H = h->d.hidden, I = h->d.inter, k = h->d.top_k, ns = h->d.num_shared;
-        const uint64_t na = static_cast<uint64_t>(inf->n_uniq) + ns;
-        const uint64_t rows = static_cast<uint64_t>(T) * (k + ns);
-        const uint64_t ea = h->d.act_dtype == moe::ACT_BF16 ? 2 : 4;
-        const uint64_t he = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
-        uint64_t wgu, wd;
-        switch (h->d.weight_fmt) {
-            case moe::FMT_FP32: wgu = 2 * I * H * 4; wd = H * I * 4; break;
-            case moe::FMT_BF16: wgu = 2 * I * H * 2; wd = H * I * 2; break;
-            default: {
-                const uint64_t blk = h->d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
-                wgu = 2 * I * H / 2 + 2 * I * H / blk;
-                wd = H * I / 2 + H * I / blk;
-            }
-        }
-        tc->gu_bytes = na * wgu + T * H * ea + rows * I * he;
-        tc->down_bytes = na * wd + rows * I * he + (tc->has_combine ? rows * H * 2 : T * H * ea);
-        tc->combine_bytes = tc->has_combine ? rows * H * 2 + T * H * ea : 0;
-        tc->copy_bytes = static_cast<uint64_t>(nm + npm) * B;
-        h->pending.push_back(tc);
     }
-    // bookkeeping
-    h->st.calls++;
-    (decode ? h->st.decode_calls : h->st.prefill_calls)++;
-    h->st.hits += inf->n_hit;
-    h->st.misses += nm;
-    h->st.prefetch_hits += inf->n_pf_hit;
-    h->st.prefetch_misses += npm;
-    h->st.copies_h2d += nm + npm;
-    h->st.bytes_h2d += static_cast<uint64_t>(nm + npm) * B;
-    const int nev = inf->n_events;
-    for (int i = 0; i < nev; ++i) {
-        if (inf->ev_evicted[i] >= 0) h->st.evictions++;
-        if (h->flags & MOE_CACHE_LOG_EVENTS) {
-            moe_event ev{inf->ev_layer[i], inf->ev_expert[i], inf->ev_hit[i], inf->ev_slot[i], inf->ev_evicted[i],
-                         inf->ev_prefetch[i]};
-            h->events.push_back(ev);
-        }
+    // the call is enqueued from here on (the routing kernel is in flight): hand
+    // it to the service thread even if the expert launch failed, so that its
+    // record is consumed in order
+    h->submitted = seq;
+    h->prefetch_may_be_pending = want_pf;
+    h->last_T = T;
+    h->last_stream = s;
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        PendingCall pc;
+        pc.seq = seq;
+        pc.layer = layer_id;
+        pc.T = T;
+        pc.self_release = a.self_release != 0;
+        pc.tc = tc;
+        h->queue.push_back(pc);
+        h->st.kernel_launches += 1 + nl;
+        if (tc) h->pending.push_back(tc);
     }
+    h->cv.notify_one();
+    if (le != cudaSuccess) return cuda_fail(h, le, "expert kernel launch");
     return MOE_OK;
+}
+
+int moe_sync(moe_handle* h) {
+    if (!h) return MOE_ERR_INVALID;
+    CK(h, cudaSetDevice(h->d.device));
+    drain(h);
+    if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
+    CK(h, cudaStreamSynchronize(h->copy));
+    // a bounded wait that gave up after the call's routing kernel had reported
+    int32_t dev_err = 0;
+    CK(h, cudaMemcpy(&dev_err, h->base.dev_err, 4, cudaMemcpyDeviceToHost));
+    if (h->log) {
+        unsigned long long rv = 0;
+        cudaMemcpy(&rv, h->ready, 8, cudaMemcpyDeviceToHost);
+        std::fprintf(stderr, "[moe] sync: submitted %llu serviced %llu ready %llu dev_err %d write64 %d\n",
+                     static_cast<unsigned long long>(h->submitted),
+                     static_cast<unsigned long long>(h->serviced.load()), rv, dev_err, h->write64 ? 1 : 0);
+    }
+    if (dev_err != 0)
+        record_error(h, MOE_ERR_TIMEOUT, "a kernel gave up a bounded wait (device error " + std::to_string(dev_err) +
+                                             "); call moe_cache_config to reset");
+    return take_error(h);
 }
 
 int moe_timing_enable(moe_handle* h, int enable) {
     if (!h) return MOE_ERR_INVALID;
     CK(h, cudaSetDevice(h->d.device));
+    drain(h);
     harvest(h, true);
     h->tm = moe_timing_t{};
     h->timing = enable != 0;
@@ -658,6 +922,7 @@ int moe_timing_enable(moe_handle* h, int enable) {
 int moe_timing(moe_handle* h, moe_timing_t* t) {
     if (!h || !t) return MOE_ERR_INVALID;
     CK(h, cudaSetDevice(h->d.device));
+    drain(h);
     harvest(h, true);
     *t = h->tm;
     return MOE_OK;
@@ -665,12 +930,16 @@ int moe_timing(moe_handle* h, moe_timing_t* t) {
 
 int moe_stats(moe_handle* h, moe_stats_t* s) {
     if (!h || !s) return MOE_ERR_INVALID;
+    drain(h);
+    std::lock_guard<std::mutex> lk(h->mu);
     *s = h->st;
     return MOE_OK;
 }
 
 int moe_stats_reset(moe_handle* h) {
     if (!h) return MOE_ERR_INVALID;
+    drain(h);
+    std::lock_guard<std::mutex> lk(h->mu);
     h->st = moe_stats_t{};
     h->events.clear();
     return MOE_OK;
@@ -678,6 +947,8 @@ int moe_stats_reset(moe_handle* h) {
 
 int moe_stats_events(moe_handle* h, moe_event* buf, int cap, int* n) {
     if (!h || !n || cap < 0 || (cap > 0 && !buf)) return MOE_ERR_INVALID;
+    drain(h);
+    std::lock_guard<std::mutex> lk(h->mu);
     const int m = std::min<int>(cap, static_cast<int>(h->events.size()));
     for (int i = 0; i < m; ++i) buf[i] = h->events[i];
     h->events.erase(h->events.begin(), h->events.begin() + m);
@@ -689,6 +960,7 @@ int moe_debug_routing(moe_handle* h, int32_t* topk_idx, float* gates, int32_t* p
                       int32_t* uniq, int32_t* n_uniq) {
     if (!h) return MOE_ERR_INVALID;
     CK(h, cudaSetDevice(h->d.device));
+    drain(h);
     if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
     const size_t n = static_cast<size_t>(h->last_T) * h->d.top_k;
     const CallArgs& a = h->base;
@@ -707,6 +979,7 @@ int moe_debug_lru_table(moe_handle* h, int32_t* table) {
     if (!h || !table) return MOE_ERR_INVALID;
     if (!h->table) return fail(h, MOE_ERR_STATE, "moe_cache_config has not been called");
     CK(h, cudaSetDevice(h->d.device));
+    drain(h);
     if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
     CK(h, cudaMemcpy(table, h->table, static_cast<size_t>(h->d.num_layers) * h->d.num_experts * 4,
                      cudaMemcpyDeviceToHost));
@@ -718,6 +991,7 @@ const char* moe_last_error(const moe_handle* h) { return h ? h->err.c_str() : "N
 void moe_destroy(moe_handle* h) {
     if (!h) return;
     cudaSetDevice(h->d.device);
+    stop_service(h);
     cudaDeviceSynchronize();
     free_timed(h);
     free_pool(h);
@@ -726,9 +1000,7 @@ void moe_destroy(moe_handle* h) {
     cudaFree(h->shared_dev);
     cudaFree(h->scratch);
     if (h->info_h) cudaFreeHost(h->info_h);
-    if (h->ev_cache) cudaEventDestroy(h->ev_cache);
-    if (h->ev_copy) cudaEventDestroy(h->ev_copy);
-    if (h->ev_prefetch) cudaEventDestroy(h->ev_prefetch);
+    if (h->ready_vals) cudaFreeHost(h->ready_vals);
     if (h->stream) cudaStreamDestroy(h->stream);
     if (h->copy) cudaStreamDestroy(h->copy);
     delete h;

@@ -23,6 +23,14 @@
  * MOE_CACHE_PREFETCH_NEXT_LAYER also stream all experts of layer+1 into the
  * pool while this layer computes, when the pool has room for both.
  *
+ * Calls are asynchronous: moe_layer_forward enqueues the call's kernels and
+ * returns. A service thread owned by the handle reads each call's cache result
+ * from mapped host memory, issues the miss copies and then releases the call's
+ * expert kernels, which wait for that release on the device (bounded). A call
+ * whose experts all hit releases itself on the device. Errors that the device
+ * side of a call finds (capacity, bounded-wait timeouts) are reported by the
+ * next moe_layer_forward or moe_sync.
+ *
  * Conventions
  *  - Every call returns MOE_OK (0) or a negative moe_status. Nothing throws and
  *    nothing aborts. moe_last_error() gives a human-readable reason.
@@ -118,12 +126,16 @@ typedef struct moe_stats_t {
  * written. */
 typedef struct moe_timing_t {
     uint64_t calls;
-    double route_ms;      /* activation prep, router, top-k, permutation, cache kernels */
-    double gate_up_ms;    /* gate/up projection + SwiGLU */
+    double route_ms;      /* routing kernel: router, top-k, permutation, cache lookup (all calls) */
+    double gate_up_ms;    /* gate/up projection + SwiGLU (decode with FP4 weights: the whole
+                             expert kernel, gate/up and down+combine) */
     double down_ms;       /* down projection (+ combine, decode) */
     double combine_ms;    /* prefill combine */
-    double copy_ms;       /* expert copies (misses and prefetch) on the copy stream */
+    double copy_ms;       /* expert copies (misses and prefetch) on the copy stream (all calls) */
     uint64_t gate_up_bytes, down_bytes, combine_bytes, copy_bytes;
+    uint64_t resident_calls;  /* calls without demand misses: gate_up/down/combine ms and bytes
+                                 cover only these (the expert kernels of a call with misses
+                                 include the wait for its copies) */
 } moe_timing_t;
 
 typedef struct moe_event {
@@ -149,9 +161,10 @@ int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
  * layout. The caller's buffers may be freed on return. Synchronous. */
 int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host* w);
 
-/* A safe point: waits until the device is idle, then (re)builds the expert
- * pool with capacity_slots slots shared by all layers, and empties the LRU
- * table. flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS. Every
+/* A safe point: waits until every enqueued call has finished, then (re)builds
+ * the expert pool with capacity_slots slots shared by all layers, empties the
+ * LRU table and the event log, and clears errors of earlier calls (including a
+ * bounded-wait timeout). flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS. Every
  * routed expert must have been loaded before the first forward call.
  * capacity_slots < top_k gives MOE_ERR_CAPACITY. */
 int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
@@ -159,13 +172,20 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
 /* One call of MoE layer `layer_id` on T tokens (0 <= T <= max_tokens):
  * hidden [T, H], router_w [E, H], out [T, H], all device memory in the handle's
  * act_dtype, row-major. Enqueued on `stream` (a cudaStream_t; NULL = the
- * handle's own stream). The call blocks the host until this layer's routing
- * and cache lookup have run on the device (the misses must be known to issue
- * their copies); the expert FFN work itself is left running on `stream`.
- * MOE_ERR_CAPACITY if the layer's experts exceed the pool (the cache is left
- * unchanged and out is not written). */
+ * handle's own stream) and returns without waiting for the device; the host
+ * blocks only when 16 calls are already waiting for the service thread. out is
+ * complete once `stream` has passed the call. A call whose layer's experts
+ * exceed the pool leaves the cache unchanged and out unwritten; the next
+ * moe_layer_forward or moe_sync returns MOE_ERR_CAPACITY for it. Errors found
+ * for earlier calls are returned before anything is enqueued. */
 int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, int layer_id,
                       int T, void* out, void* stream);
+
+/* Waits until every call enqueued so far has been serviced and has finished on
+ * the device (its stream and the copy stream), then returns the first error
+ * found for any of them (MOE_ERR_CAPACITY once; MOE_ERR_TIMEOUT until the next
+ * moe_cache_config), or MOE_OK. */
+int moe_sync(moe_handle* h);
 
 /* Cumulative counters since moe_init (or the last moe_stats_reset). */
 int moe_stats(moe_handle* h, moe_stats_t* s);

@@ -63,6 +63,7 @@ class GpuStack:
         out = self.out_buf(T)
         self.torch.cuda.synchronize(self.dev)
         self.forward_dev(layer, x, out, T)
+        moe.moe_sync(self.h)
         self.stream.synchronize()
         o = out.float().cpu().numpy()
         r = moe.moe_debug_routing(self.h, T, self.shape.k, self.shape.E)
