@@ -38,10 +38,13 @@ METRIC = "MoE-layer tokens/s (decode T=1, prefill T=4096); % of HBM / FP4 tensor
 UNIT = "tokens/s"
 
 WORKLOADS = {
-    # name: (shape, T, pool fraction, cache flags, layers used)
-    "decode": (synth.DECODE_NVFP4, 1, 0.25, 0, 40),
-    "decode8": (synth.DECODE_NVFP4, 8, 0.25, 0, 40),
-    "prefill": (synth.PREFILL_BF16, 4096, 0.5, 1, 8),
+    # name: (shape, T, pool fraction, cache flags, layers used, step reuse probability)
+    "decode": (synth.DECODE_NVFP4, 1, 0.25, 0, 40, 0.0),
+    "decode8": (synth.DECODE_NVFP4, 8, 0.25, 0, 40, 0.0),
+    "prefill": (synth.PREFILL_BF16, 4096, 0.5, 1, 40, 0.0),
+    "large": (synth.LARGE_MXFP4, 1, 0.2, 0, 24, 0.0),
+    "large_prefill": (synth.LARGE_MXFP4, 2048, 0.2, 0, 24, 0.0),
+    "stress": (synth.STRESS_NVFP4, 1, 0.10, 0, 16, 0.7),
 }
 
 L2_BYTES = 126 * 1024 * 1024
@@ -182,7 +185,7 @@ def run_ours(args, rank, world, dist):
     local = _env_int("LOCAL_RANK", 0)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    shape, T, frac, flags, L = WORKLOADS[args.workload]
+    shape, T, frac, flags, L, reuse = WORKLOADS[args.workload]
     if args.layers:
         L = min(L, args.layers)
     if args.pool_frac:
@@ -197,11 +200,15 @@ def run_ours(args, rank, world, dist):
         r = synth.router_weights(shape, 0, l)
         router.append(torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16))
     nsteps = args.warmup + args.steps
-    # per (step, layer) hidden states, distinct across ranks
+    # per (step, layer) hidden states, distinct across ranks; with step reuse,
+    # a step repeats the previous step's hidden states in every layer
     hid = np.empty((nsteps, L, T, shape.H), np.uint16)
+    flags_r = synth.reuse_flags(rank, nsteps, reuse) if reuse > 0 else np.zeros(nsteps, bool)
+    src = 0
     for st in range(nsteps):
+        src = src if flags_r[st] else st
         for l in range(L):
-            hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + st)
+            hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + src)
     x_dev = torch.from_numpy(hid.view(np.int16)).to(dev).view(torch.bfloat16)
     out_dev = torch.empty((L, T, shape.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -284,36 +291,57 @@ def run_ours(args, rank, world, dist):
             "down": (timing["down_ms"], timing["down_bytes"])}
     if timing["combine_ms"] > 0:
         kern["combine"] = (timing["combine_ms"], timing["combine_bytes"])
+    fused_decode = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4)
+    if fused_decode:
+        # one kernel does gate/up, down and the combine
+        kern = {"gate_up": (timing["gate_up_ms"], timing["gate_up_bytes"] + timing["down_bytes"])}
     dom = max(kern, key=lambda n: kern[n][0])
     dms, dbytes = kern[dom]
     calls = max(1, timing["resident_calls"])
-    fused_decode = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4)
     kernel_name = {"gate_up": "k_dec_fp4 (gate/up + down + combine)" if fused_decode else "gate/up + SwiGLU",
                    "down": "down projection", "combine": "combine"}[dom]
     achieved = dbytes / (dms * 1e-3) / 1e9 if dms > 0 else 0.0
     peak = peaks.get("hbm_gbs", 6400.0)
     traffic = _traffic_for(dom, args.workload)
+    roof = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+            else "fallback 6.4 TB/s",
+            "algorithmic_bytes_per_launch": int(dbytes // calls),
+            "avg_launch_us": round(dms * 1e3 / calls, 3),
+            "traffic": traffic}
+    if T > 8:
+        # prefill: the expert GEMMs are a dense contraction; gate/up is 2*2*I*H flops per routed row
+        rows = T * (shape.k + shape.shared)
+        gu_flops = 4.0 * shape.I * shape.H * rows
+        tf = gu_flops / (timing["gate_up_ms"] / calls * 1e-3) / 1e12 if timing["gate_up_ms"] > 0 else 0.0
+        tpeak = peaks.get("bf16_tflops", 1800.0)
+        roof = {"bound": "tensor", "kernel": "gate/up + SwiGLU grouped GEMM"
+                + (" (tcgen05, TMA, TMEM)" if shape.fmt == synth.FMT_BF16 else " (mma.sync)"),
+                "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+                "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json)",
+                "algorithmic_flops_per_launch": gu_flops,
+                "avg_launch_us": round(timing["gate_up_ms"] * 1e3 / calls, 3),
+                "hbm": {"achieved_gbs": round(achieved, 1) if dom == "gate_up" else None,
+                        "frac": round(achieved / peak, 4) if dom == "gate_up" else None},
+                "traffic": traffic}
     cpu = cpu_baseline(shape, T, L, budget_s=args.cpu_budget) if world == 1 else None
     cap_hits = stats["hits"] + stats["misses"]
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 weights x f16 activations, fp32 accumulate"
-        if shape.fmt == synth.FMT_NVFP4 else "bf16 x bf16, fp32 accumulate",
+        "vs_baseline": None, "dtype": {synth.FMT_NVFP4: "nvfp4 weights x f16 activations, fp32 accumulate",
+                                       synth.FMT_MXFP4: "mxfp4 weights x f16 activations, fp32 accumulate"}.get(
+            shape.fmt, "bf16 x bf16, fp32 accumulate"),
         "data": "synthetic (seeded; random weights of the stated shape)",
-        "config": {"workload": shape.name if T == 1 or args.workload != "decode8" else shape.name,
+        "config": {"workload": shape.name,
                    "T": T, "layers": L, "pool_slots": S, "pool_frac": frac,
-                   "router_zipf_s": shape.zipf_s, "cache_flags": flags,
+                   "router_zipf_s": shape.zipf_s, "cache_flags": flags, "step_reuse_p": reuse,
+                   "shared_experts": shape.shared,
                    "l2": "per-step working set (active experts' weights, %d MB) exceeds the 126 MB L2"
                          % ((timing["gate_up_bytes"] + timing["down_bytes"]) // max(1, K) // (1 << 20)),
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
-                     else "fallback 6.4 TB/s",
-                     "algorithmic_bytes_per_launch": int(dbytes // calls),
-                     "avg_launch_us": round(dms * 1e3 / calls, 3),
-                     "traffic": traffic},
+        "roofline": roof,
         "kernels_us_per_call": {"route+cache": round(timing["route_ms"] * 1e3 / max(1, timing["calls"]), 2),
                                 "gate_up": round(timing["gate_up_ms"] * 1e3 / calls, 2),
                                 "down": round(timing["down_ms"] * 1e3 / calls, 2),
@@ -378,7 +406,7 @@ def cpu_baseline(shape, T, L, budget_s=15.0):
 
 
 def run_reference(args):
-    shape, T, frac, flags, L = WORKLOADS[args.workload]
+    shape, T, frac, flags, L, reuse = WORKLOADS[args.workload]
     budget = float(os.environ.get("MOE_REF_STEP_BUDGET_S", "1.0"))
     for _ in range(args.warmup):
         oracle_layer_seconds(shape, T, L, 0.0)

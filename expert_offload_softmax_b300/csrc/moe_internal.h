@@ -140,6 +140,14 @@ struct CallArgs {
     void* xperm;           // [T*k + T*n_shared][H] bf16 gathered activations, device K-order (prefill, BF16)
     int32_t* dev_err;      // [1] sticky device error word (bounded waits that gave up)
     int32_t* route_done;   // [1] routing CTAs finished in this call (0 between calls)
+    // prefill permutation, computed in parts: each routing CTA b (8 tokens)
+    // ranks its assignments among those of the same expert and adds its
+    // per-expert counts; the column scans give every CTA its base row per expert
+    int32_t* cacc;         // [E] per-expert assignment counts (0 between calls)
+    int16_t* cntT;         // [E][nb] per-CTA counts of each expert (nb = ceil(max_tokens / 8))
+    int32_t* baseT;        // [E][nb] rows of expert e before CTA b's (exclusive scan over b)
+    int16_t* lrank;        // [T*k] rank of assignment a among its CTA's assignments to the same expert
+    int nb_max;            // column stride of cntT / baseT
     unsigned int* grid_bar;  // [2] grid barrier of the decode expert kernel: arrivals, generation
     unsigned char* dplan;  // decode plan: header + (E + n_shared) records
     int32_t* n_uniq;       // [1]

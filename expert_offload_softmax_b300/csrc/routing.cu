@@ -127,9 +127,7 @@ __device__ __forceinline__ void copy_g2s(unsigned char* dst, const unsigned char
 // EPW experts (rows e0.. of router_w, e >= E contributes nothing) x nt tokens
 // whose rows sit in shared memory; every lane returns the finished sums. Each
 // lane first loads NB of its chunks (all independent), then runs its FMA
-// chain over them in order, so a batch costs one memory round trip. Pairs of
-// experts go through the packed fma.rn.f32x2, two IEEE fused multiply-adds
-// with round-to-nearest-even, i.e. the same result as two separate ones.
+// chain over them in order, so a batch costs one memory round trip.
 // --------------------------------------------------------------------------
 
 template <int ACT>
@@ -161,16 +159,6 @@ __device__ __forceinline__ void cvt_chunk(const RawChunk<ACT>& r, float (&v)[8])
     }
 }
 
-// (c0, c1) = (fma(a, b0, c0), fma(a, b1, c1)), both rounded to nearest even
-__device__ __forceinline__ void fma2(float a, float b0, float b1, float& c0, float& c1) {
-    unsigned long long A, B, C;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a), "f"(a));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c0), "f"(c1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(C) : "l"(A), "l"(B));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(C));
-}
-
 // the first batch of a warp's router chunks (lane's chunks lane, lane+32, ...)
 template <int ACT, int EPW, int NB>
 __device__ __forceinline__ void router_batch(const void* __restrict__ router_w, int H, int E, int e0, int cb,
@@ -185,8 +173,9 @@ __device__ __forceinline__ void router_batch(const void* __restrict__ router_w, 
     }
 }
 
-// pre: this lane's first batch, already loaded with router_batch (or null)
-template <int ACT, int EPW, int NB>
+// pre: this lane's first batch, already loaded with router_batch (or null);
+// XT: element type of the token rows in shared memory
+template <int ACT, int EPW, int NB, int XT = ACT>
 __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, const unsigned char* xs, int H,
                                             int E, int e0, int nt, int lane, float (&acc)[EPW][8],
                                             const RawChunk<ACT> (*pre)[EPW] = nullptr) {
@@ -223,17 +212,11 @@ __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, c
             for (int t = 0; t < 8; ++t) {
                 if (t < nt) {
                     float xv[8];
-                    ld_act8<ACT>(xs, static_cast<size_t>(t) * H + 8 * c, xv);
+                    ld_act8<XT>(xs, static_cast<size_t>(t) * H + 8 * c, xv);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if constexpr (EPW % 2 == 0) {
+                    for (int j = 0; j < 8; ++j)
 #pragma unroll
-                            for (int e = 0; e < EPW; e += 2) fma2(xv[j], wv[e][j], wv[e + 1][j], acc[e][t], acc[e + 1][t]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < EPW; ++e) acc[e][t] = __fmaf_rn(xv[j], wv[e][j], acc[e][t]);
-                        }
-                    }
+                        for (int e = 0; e < EPW; ++e) acc[e][t] = __fmaf_rn(xv[j], wv[e][j], acc[e][t]);
                 }
             }
         }
@@ -644,12 +627,22 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         }
         for (int i = tid; i < (E + a.n_shared) * kDecodeMaxT; i += nthr) a.tok_row[i] = -1;
     }
-    for (int e = tid; e < E; e += nthr) rs.cnt[e] = 0;
+    if (decode) {
+        for (int e = tid; e < E; e += nthr) rs.cnt[e] = 0;
+    } else {
+        // the routing CTAs added their counts; reset the accumulator for the next call
+        for (int e = tid; e < E; e += nthr) {
+            rs.cnt[e] = __ldcg(a.cacc + e);
+            a.cacc[e] = 0;
+        }
+    }
     __syncthreads();
-    auto topk_at = [&](int i) -> int { return decode ? rs.topk[i] : __ldcg(a.topk + i); };
-    auto gate_at = [&](int i) -> float { return decode ? rs.gates[i] : __ldcg(a.gates + i); };
-    for (int i = tid; i < n; i += nthr) atomicAdd(&rs.cnt[topk_at(i)], 1);
-    __syncthreads();
+    auto topk_at = [&](int i) -> int { return rs.topk[i]; };
+    auto gate_at = [&](int i) -> float { return rs.gates[i]; };
+    if (decode) {
+        for (int i = tid; i < n; i += nthr) atomicAdd(&rs.cnt[topk_at(i)], 1);
+        __syncthreads();
+    }
     // offsets (exclusive) and the active list: each thread owns `per` consecutive experts
     const int per = (E + nthr - 1) / nthr;
     {
@@ -691,8 +684,67 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         }
     }
     __syncthreads();
-    // stable permutation: warp w owns the contiguous assignment range [w*chunk, (w+1)*chunk)
-    {
+    if (!decode) {
+        // prefill: rows of expert e before CTA b = exclusive scan of its count
+        // column over b; a follow-up kernel places the assignments
+        const int nwarps = nthr >> 5;
+        const int nb = (T + kPrefillTokTile - 1) / kPrefillTokTile;
+        // 16 consecutive columns per lane, read as two 16-byte vectors (nb_max is a
+        // multiple of 16; columns past nb hold stale counts and are masked)
+        constexpr int kPerLane = 16, kBatch = 4;
+        for (int e0 = warp * kBatch; e0 < E; e0 += nwarps * kBatch) {
+            int carry[kBatch] = {0, 0, 0, 0};
+            for (int b0 = 0; b0 < nb; b0 += 32 * kPerLane) {
+                int v[kBatch][kPerLane];
+                const int bl = b0 + lane * kPerLane;
+                uint4 raw[kBatch][2];
+#pragma unroll
+                for (int x = 0; x < kBatch; ++x)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        raw[x][h] = (e0 + x < E && bl < nb)
+                                        ? __ldcg(reinterpret_cast<const uint4*>(a.cntT + static_cast<size_t>(e0 + x) * a.nb_max + bl) + h)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int x = 0; x < kBatch; ++x)
+#pragma unroll
+                    for (int i = 0; i < kPerLane; ++i) {
+                        const uint4 r = raw[x][i / 8];
+                        const uint32_t w = (i % 8) < 2 ? r.x : (i % 8) < 4 ? r.y : (i % 8) < 6 ? r.z : r.w;
+                        const int c = static_cast<int>((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+                        v[x][i] = bl + i < nb ? c : 0;
+                    }
+#pragma unroll
+                for (int x = 0; x < kBatch; ++x) {
+                    int tot = 0;
+#pragma unroll
+                    for (int i = 0; i < kPerLane; ++i) tot += v[x][i];
+                    int incl = tot;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    int run = carry[x] + incl - tot;
+                    if (e0 + x < E && bl < nb) {
+                        int o[kPerLane];
+#pragma unroll
+                        for (int i = 0; i < kPerLane; ++i) {
+                            o[i] = run;
+                            run += v[x][i];
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(a.baseT + static_cast<size_t>(e0 + x) * a.nb_max + bl);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            dst[h] = make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+                    }
+                    carry[x] += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+        }
+    }
+    // decode: stable permutation, warp w owns the contiguous assignment range [w*chunk, (w+1)*chunk)
+    if (decode) {
         int32_t* wc = reinterpret_cast<int32_t*>(area);  // [kRouteWarps][E]
         const int nwarps = nthr >> 5;
         const int chunk = (n + nwarps - 1) / nwarps;
@@ -895,12 +947,17 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         xprep_rows<ACT>(route_smem, a.xh, a.fmt, H, 0, T, static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x,
                         static_cast<size_t>(gridDim.x) * blockDim.x);
     } else {
-        // 8 tokens per CTA, all experts; logits [8][E] in shared memory, then top-k
+        // 8 tokens per CTA, all experts; logits [8][E] in shared memory, then
+        // top-k, then this CTA's share of the permutation (ranks, counts)
         const int t0 = blockIdx.x * kPrefillTokTile;
         const int nt = min(kPrefillTokTile, T - t0);
+        const int k = a.k;
         float* lg = reinterpret_cast<float*>(route_smem + static_cast<size_t>(kPrefillTokTile) * H * esz);
+        int32_t* s_tk = reinterpret_cast<int32_t*>(lg + static_cast<size_t>(kPrefillTokTile) * E);
+        int32_t* s_cnt = s_tk + kPrefillTokTile * kMaxTopK;
         copy_g2s(route_smem, reinterpret_cast<const unsigned char*>(a.hidden) + static_cast<size_t>(t0) * H * esz,
                  static_cast<size_t>(nt) * H * esz / 16);
+        for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
         __syncthreads();
         if (a.fmt != FMT_BF16) xprep_rows<ACT>(route_smem, a.xh, a.fmt, H, t0, nt, threadIdx.x, blockDim.x);
         constexpr int kPass = kRouteWarps * kPrefillEpw;
@@ -922,12 +979,39 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         if (warp < nt) {
             int sel;
             float g;
-            warp_topk<false>(lg + warp * E, E, a.k, lane, sel, g);
-            if (lane < a.k) {
-                const size_t o = static_cast<size_t>(t0 + warp) * a.k + lane;
+            warp_topk<false>(lg + warp * E, E, k, lane, sel, g);
+            if (lane < k) {
+                const size_t o = static_cast<size_t>(t0 + warp) * k + lane;
                 a.topk[o] = sel;
                 a.gates[o] = g;
+                s_tk[warp * k + lane] = sel;
             }
+        }
+        __syncthreads();
+        // ranks among this CTA's assignments to the same expert (ascending
+        // assignment order), per-expert counts: the stable permutation then
+        // puts assignment a at offsets[e] + (rows of e in earlier CTAs) + rank
+        if (warp == 0) {
+            const int na = nt * k;
+            const uint32_t lt = (1u << lane) - 1u;
+            for (int base = 0; base < na; base += 32) {
+                const int i = base + lane;
+                const bool valid = i < na;
+                const int e = valid ? s_tk[i] : -1 - lane;
+                const uint32_t peers = __match_any_sync(0xffffffffu, e);
+                int r = 0;
+                if (valid) r = s_cnt[e] + __popc(peers & lt);
+                __syncwarp();
+                if (valid && lane == 31 - __clz(peers)) s_cnt[e] += __popc(peers);
+                __syncwarp();
+                if (valid) a.lrank[static_cast<size_t>(t0) * k + i] = static_cast<int16_t>(r);
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int c = s_cnt[e];
+            a.cntT[static_cast<size_t>(e) * a.nb_max + blockIdx.x] = static_cast<int16_t>(c);
+            if (c) atomicAdd(&a.cacc[e], c);
         }
     }
     // ---------------- hand-off: the last CTA to finish runs phase B
@@ -945,12 +1029,29 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     if (threadIdx.x == 0) *a.route_done = 0;
 }
 
+// prefill: places every assignment of routing CTA b (8 tokens) at
+// offsets[e] + rows of e in earlier CTAs + its rank among CTA b's assignments to e
+__global__ void __launch_bounds__(256) k_perm_rows(CallArgs a) {
+    const int b = blockIdx.x, k = a.k;
+    const int t0 = b * kPrefillTokTile, nt = min(kPrefillTokTile, a.T - t0);
+    const int i = threadIdx.x;
+    if (i >= nt * k) return;
+    const int asg = t0 * k + i;
+    const int e = a.topk[asg];
+    const int row = a.offsets[e] + a.baseT[static_cast<size_t>(e) * a.nb_max + b] + a.lrank[asg];
+    a.perm[row] = asg;
+    a.inv_perm[asg] = row;
+    a.row_tok[row] = asg / k;
+    a.row_gate[row] = a.gates[asg];
+}
+
 // dynamic shared memory of one k_route launch
 static size_t route_smem_bytes(const CallArgs& a, bool decode) {
     const size_t esz = a.act == ACT_BF16 ? 2 : 4;
     const size_t phase_a = decode ? static_cast<size_t>(a.T) * a.H * esz
                                   : static_cast<size_t>(kPrefillTokTile) * a.H * esz +
-                                        static_cast<size_t>(kPrefillTokTile) * a.E * 4;
+                                        static_cast<size_t>(kPrefillTokTile) * a.E * 4 +
+                                        static_cast<size_t>(kPrefillTokTile) * kMaxTopK * 4 + static_cast<size_t>(a.E) * 4;
     return std::max(phase_a, kRouteSharedBytes + route_area_bytes(a.S, a.E));
 }
 
@@ -969,6 +1070,7 @@ cudaError_t launch_route(const CallArgs& a, cudaStream_t s) {
         const int grid = (a.T + kPrefillTokTile - 1) / kPrefillTokTile;
         if (a.act == ACT_BF16) k_route<ACT_BF16, false><<<grid, kRouteThreads, smem, s>>>(a);
         else k_route<ACT_FP32, false><<<grid, kRouteThreads, smem, s>>>(a);
+        k_perm_rows<<<grid, 256, 0, s>>>(a);
     }
     return cudaGetLastError();
 }
@@ -976,6 +1078,8 @@ cudaError_t launch_route(const CallArgs& a, cudaStream_t s) {
 // dynamic shared memory limits are raised once per process
 cudaError_t routing_set_attributes() {
     cudaError_t e;
+    cudaFuncAttributes fa;  // loads the kernel now (see experts_preload)
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_perm_rows)))) return e;
     const int big = static_cast<int>(route_smem_limit());
     if ((e = cudaFuncSetAttribute(k_route<ACT_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, big))) return e;
     if ((e = cudaFuncSetAttribute(k_route<ACT_BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, big))) return e;

@@ -489,7 +489,7 @@ void service_call(moe_handle* h, const PendingCall& pc) {
                 wd = H * I / 2 + H * I / blk;
             }
         }
-        tc->had_miss = nm > 0;
+        tc->had_miss = nm > 0 || !pc.self_release;  // the kernels waited for copies
         tc->gu_bytes = na * wgu + T * H * ea + rows * I * he;
         tc->down_bytes = na * wd + rows * I * he + (tc->has_combine ? rows * H * 2 : T * H * ea);
         tc->combine_bytes = tc->has_combine ? rows * H * 2 + T * H * ea : 0;
@@ -628,6 +628,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     // scratch carve-up
     const size_t rows = Tm * (k + ns);
     const size_t hes = h->d.weight_fmt == moe::FMT_FP32 ? 4 : 2;
+    const size_t nb_max = align_up((Tm + 7) / 8, 16);  // routing CTAs of a prefill call, padded to 16
     const bool umma = moe::prefill_uses_umma(h->d.weight_fmt, static_cast<int>(Tm));
     struct Part { size_t bytes; void** dst; };
     CallArgs& a = h->base;
@@ -652,6 +653,10 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {umma ? rows * H * 2 : 16, &a.xperm},
         {4, reinterpret_cast<void**>(&a.dev_err)},
         {4, reinterpret_cast<void**>(&a.route_done)},
+        {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.cacc)},
+        {static_cast<size_t>(E) * nb_max * 2, reinterpret_cast<void**>(&a.cntT)},
+        {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
+        {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
         {8, reinterpret_cast<void**>(&a.grid_bar)},
         {moe::kDecPlanHeader + static_cast<size_t>(E + ns) * sizeof(moe::DecExpert), reinterpret_cast<void**>(&a.dplan)},
         {8, reinterpret_cast<void**>(&a.ready)},
@@ -694,6 +699,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ERR_CUDA);
     a.E = E; a.k = k; a.H = static_cast<int>(H); a.I = static_cast<int>(I); a.n_shared = ns; a.L = L;
+    a.nb_max = static_cast<int>(nb_max);
     a.fmt = h->d.weight_fmt; a.act = h->d.act_dtype; a.mode = h->d.act_mode;
     a.lay = h->lay;
     a.wait_ns = h->wait_ns;
@@ -879,7 +885,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         pc.self_release = a.self_release != 0;
         pc.tc = tc;
         h->queue.push_back(pc);
-        h->st.kernel_launches += 1 + nl;
+        h->st.kernel_launches += (decode ? 1 : 2) + nl;
         if (tc) h->pending.push_back(tc);
     }
     h->cv.notify_one();

@@ -133,9 +133,9 @@ typedef struct moe_timing_t {
     double combine_ms;    /* prefill combine */
     double copy_ms;       /* expert copies (misses and prefetch) on the copy stream (all calls) */
     uint64_t gate_up_bytes, down_bytes, combine_bytes, copy_bytes;
-    uint64_t resident_calls;  /* calls without demand misses: gate_up/down/combine ms and bytes
-                                 cover only these (the expert kernels of a call with misses
-                                 include the wait for its copies) */
+    uint64_t resident_calls;  /* calls whose expert kernels did not wait for copies (no demand
+                                 misses, no prefetch of an earlier call outstanding):
+                                 gate_up/down/combine ms and bytes cover only these */
 } moe_timing_t;
 
 typedef struct moe_event {
