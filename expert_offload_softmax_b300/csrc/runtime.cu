@@ -109,7 +109,11 @@ struct moe_handle {
     bool fault_drop_release = false;
     bool log = false;  // MOE_LOG: one stderr line per serviced call
     // streams / events
-    cudaStream_t stream = nullptr, copy = nullptr;
+    // miss copies alternate between two copy streams (the copy engines overlap
+    // one copy's setup with another's transfer); `copy` joins `copy2` before
+    // every release, so a release always follows all of its call's copies
+    cudaStream_t stream = nullptr, copy = nullptr, copy2 = nullptr;
+    cudaEvent_t ev_join = nullptr;
     // enqueue side (caller's thread)
     uint64_t submitted = 0;
     bool prefetch_may_be_pending = false;
@@ -448,20 +452,25 @@ void service_call(moe_handle* h, const PendingCall& pc) {
         cudaEventRecord(tc->c0, h->copy);
         tc->has_copy = true;
     }
-    for (int i = 0; i < nm && ce == cudaSuccess; ++i) {
-        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
-        ce = cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
-                             cudaMemcpyHostToDevice, h->copy);
-    }
+    auto copy_range = [&](int i0, int i1) -> cudaError_t {
+        cudaError_t r = cudaSuccess;
+        for (int i = i0; i < i1 && r == cudaSuccess; ++i) {
+            const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
+            r = cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
+                                cudaMemcpyHostToDevice, ((i - i0) & 1) ? h->copy2 : h->copy);
+        }
+        if (r == cudaSuccess && i1 - i0 > 1) {
+            r = cudaEventRecord(h->ev_join, h->copy2);
+            if (r == cudaSuccess) r = cudaStreamWaitEvent(h->copy, h->ev_join, 0);
+        }
+        return r;
+    };
+    ce = copy_range(0, nm);
     if (ce == cudaSuccess && !kernel_released) {
         if (h->fault_drop_release && nm > 0) h->fault_drop_release = false;
         else ce = post_ready(h, pc.seq);
     }
-    for (int i = nm; i < nm + npm && ce == cudaSuccess; ++i) {
-        const int l = inf->miss_layer[i], e = inf->miss_expert[i], sl = inf->miss_slot[i];
-        ce = cudaMemcpyAsync(h->pool + static_cast<size_t>(sl) * B, h->bank[l] + static_cast<size_t>(e) * B, B,
-                             cudaMemcpyHostToDevice, h->copy);
-    }
+    if (ce == cudaSuccess) ce = copy_range(nm, nm + npm);
     if (tc && tc->has_copy) cudaEventRecord(tc->c1, h->copy);
     if (h->log)
         std::fprintf(stderr, "[moe] call %llu layer %d T %d status %d uniq %d miss %d pf_miss %d self_release %d "
@@ -697,6 +706,8 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         return bail(MOE_ERR_OOM);
     if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaStreamCreateWithFlags(&h->copy2, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ERR_CUDA);
     a.E = E; a.k = k; a.H = static_cast<int>(H); a.I = static_cast<int>(I); a.n_shared = ns; a.L = L;
     a.nb_max = static_cast<int>(nb_max);
@@ -899,6 +910,7 @@ int moe_sync(moe_handle* h) {
     drain(h);
     if (h->last_stream) CK(h, cudaStreamSynchronize(h->last_stream));
     CK(h, cudaStreamSynchronize(h->copy));
+    CK(h, cudaStreamSynchronize(h->copy2));
     // a bounded wait that gave up after the call's routing kernel had reported
     int32_t dev_err = 0;
     CK(h, cudaMemcpy(&dev_err, h->base.dev_err, 4, cudaMemcpyDeviceToHost));
@@ -1009,6 +1021,8 @@ void moe_destroy(moe_handle* h) {
     if (h->ready_vals) cudaFreeHost(h->ready_vals);
     if (h->stream) cudaStreamDestroy(h->stream);
     if (h->copy) cudaStreamDestroy(h->copy);
+    if (h->copy2) cudaStreamDestroy(h->copy2);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     delete h;
 }
 
