@@ -317,7 +317,8 @@ def run_ours(args, rank, world, dist):
         tf = gu_flops / (timing["gate_up_ms"] / calls * 1e-3) / 1e12 if timing["gate_up_ms"] > 0 else 0.0
         tpeak = peaks.get("bf16_tflops", 1800.0)
         roof = {"bound": "tensor", "kernel": "gate/up + SwiGLU grouped GEMM"
-                + (" (tcgen05, TMA, TMEM)" if shape.fmt == synth.FMT_BF16 else " (mma.sync)"),
+                + (" (tcgen05, TMA, TMEM)" if shape.fmt == synth.FMT_BF16
+                   else " (tcgen05, TMEM; FP4 A tiles widened to BF16 in shared memory)"),
                 "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
                 "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json)",
                 "algorithmic_flops_per_launch": gu_flops,
@@ -330,9 +331,10 @@ def run_ours(args, rank, world, dist):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {synth.FMT_NVFP4: "nvfp4 weights x f16 activations, fp32 accumulate",
-                                       synth.FMT_MXFP4: "mxfp4 weights x f16 activations, fp32 accumulate"}.get(
-            shape.fmt, "bf16 x bf16, fp32 accumulate"),
+        "vs_baseline": None, "dtype": ("bf16 x bf16, fp32 accumulate" if shape.fmt == synth.FMT_BF16 else
+                                       "%s weights widened %s x %s activations, fp32 accumulate" % (
+                                           "nvfp4" if shape.fmt == synth.FMT_NVFP4 else "mxfp4",
+                                           "to f16" if T <= 8 else "to bf16", "f16" if T <= 8 else "bf16")),
         "data": "synthetic (seeded; random weights of the stated shape)",
         "config": {"workload": shape.name,
                    "T": T, "layers": L, "pool_slots": S, "pool_frac": frac,

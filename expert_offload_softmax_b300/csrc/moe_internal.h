@@ -244,6 +244,6 @@ cudaError_t launch_decode_fp4(const CallArgs& a, int num_sms, cudaStream_t s);
 // loads every expert kernel (called once by moe_init)
 cudaError_t experts_preload();
 // true when a prefill call of this shape takes the tensor-core path
-inline bool prefill_uses_umma(int fmt, int T) { return fmt == FMT_BF16 && T > kDecodeMaxT; }
+inline bool prefill_uses_umma(int fmt, int T) { return fmt != FMT_FP32 && T > kDecodeMaxT; }
 
 }  // namespace moe

@@ -35,6 +35,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "mma_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -43,17 +44,20 @@ namespace {
 constexpr int BM = 128;  // weight rows per accumulator (MMA M)
 constexpr int BN = 128;  // tokens per tile (MMA N at most)
 constexpr int BK = 64;   // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;                   // BF16 weights: producer, MMA, 4 epilogue warps
+constexpr int kXformWarps = 8;                  // FP4 weights: + warps that widen the A tiles to BF16
+constexpr int kThreadsFp4 = kThreads + 32 * kXformWarps;
 constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand tile
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum { MODE_GU = 0, MODE_DOWN = 1 };
 
-template <int MODE>
+template <int MODE, bool FP4 = false>
 struct Cfg {
     static constexpr int kATiles = MODE == MODE_GU ? 2 : 1;           // gate + up, or down
     static constexpr int kStageBytes = (kATiles + 1) * kTileBytes;   // A tiles + B tile
-    static constexpr int kStages = MODE == MODE_GU ? 4 : 6;
+    // FP4: 4 stages, each written by two transform warps (see xform_rows)
+    static constexpr int kStages = (MODE == MODE_GU || FP4) ? 4 : 6;
     static constexpr int kAccCols = kATiles * BN;                    // TMEM columns per accumulator set
     static constexpr int kTmemCols = 2 * kAccCols;                   // double-buffered: 512 / 256
     static constexpr int kSmem = kStages * kStageBytes + 1024;       // + alignment slack
@@ -62,12 +66,6 @@ struct Cfg {
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
@@ -196,14 +194,101 @@ __device__ __forceinline__ int find_expert(const TileSched& ts, int na, int t) {
     return lo;
 }
 
+// FP4 weights (NVFP4 / MXFP4): the A tile of a pipeline stage (one 64-element
+// K block of 128 weight rows, or 2 x 128 for gate/up) is written by two
+// transform warps, each owning half of its rows. Warp w serves stage w mod 4
+// and only that stage, so it is never more than one use ahead of the MMA (an
+// mbarrier parity wait cannot tell use n from use n-2). A warp loads its rows'
+// codes and block scales from the tiled blob (one position ahead, into a second
+// register buffer), widens code x scale to BF16 (exact: an E2M1 value times an
+// E4M3 or E8M0 scale has at most 6 significant bits) and stores them in the
+// layout a TMA load with 128-byte swizzling would have produced (row r at
+// r*128 bytes, its 16-byte chunk c at position c ^ (r mod 8)).
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+struct XRows {
+    static constexpr int kRows = MODE == MODE_GU ? 4 : 2;  // rows per lane: 128 / 32 or 64 / 32
+    uint4 codes[kRows][2];
+    uint2 sc[kRows];
+};
+
+// loads, for K block kb of M tile mt of the expert at blob, the rows of part
+// `part` (GU: 0 = gate, 1 = up; DOWN: rows 64*part ..) that this lane owns
+template <int FMT, int MODE>
+__device__ __forceinline__ void xload(const CallArgs& a, const uint8_t* blob, int mt, int kb, int part, int lane,
+                                      XRows<MODE>& x) {
+    constexpr int kSbpg = FMT == FMT_NVFP4 ? 8 : 4;
+    const int G = (MODE == MODE_GU ? a.H : a.I) / kGroupK;
+    const int j = kb >> 1, h = kb & 1;  // K group, half of it
+    const int c = j / kChunkGroups, w = j % kChunkGroups, ng = fp4_chunk_groups(G, c);
+#pragma unroll
+    for (int i = 0; i < XRows<MODE>::kRows; ++i) {
+        const uint8_t* tile;
+        int trow;
+        if constexpr (MODE == MODE_GU) {
+            const int unit = mt * BM + lane + 32 * i;
+            tile = blob + a.lay.gu + static_cast<size_t>(unit / 8) * a.lay.gu_tile;
+            trow = 8 * part + unit % 8;  // gate rows 0-7, up rows 8-15 of the unit tile
+        } else {
+            const int row = mt * BM + 64 * part + lane + 32 * i;
+            tile = blob + a.lay.d + static_cast<size_t>(row / kTileRows) * a.lay.d_tile;
+            trow = row % kTileRows;
+        }
+        const uint8_t* chunk = tile + fp4_chunk_off(c, kSbpg);
+        x.codes[i][0] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h)));
+        x.codes[i][1] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h + 1)));
+        if constexpr (FMT == FMT_NVFP4)
+            x.sc[i] = __ldg(reinterpret_cast<const uint2*>(chunk + fp4_scale_off(ng, kSbpg, trow, w)));
+        else
+            x.sc[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(chunk + fp4_scale_off(ng, kSbpg, trow, w))), 0u);
+    }
+}
+
+// widens the loaded rows into the stage's A tile
+template <int FMT, int MODE>
+__device__ __forceinline__ void xstore(const XRows<MODE>& x, unsigned char* st, int part, int lane) {
+#pragma unroll
+    for (int i = 0; i < XRows<MODE>::kRows; ++i) {
+        float s8[8];
+        if constexpr (FMT == FMT_NVFP4) {
+            e4m3x8_to_f32(x.sc[i], s8);
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) s8[2 * b] = s8[2 * b + 1] = e8m0_to_f32((x.sc[i].x >> (8 * b)) & 0xFFu);
+        }
+        const int r = (MODE == MODE_GU ? 0 : 64 * part) + lane + 32 * i;  // row of the 128-row A tile
+        unsigned char* rowp = st + (MODE == MODE_GU ? part * kTileBytes : 0) + r * 128;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t wv[4] = {x.codes[i][u].x, x.codes[i][u].y, x.codes[i][u].z, x.codes[i][u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // 4 code bytes -> 8 elements -> one 16-byte chunk
+                uint32_t f[4];
+                fp4x8_to_f16x2(wv[q], f);
+                uint32_t o[4];
+#pragma unroll
+                for (int y = 0; y < 4; ++y) {
+                    const float sv = s8[(4 * q + y) >> 1];  // byte b of a unit holds K steps b/2
+                    const __half2 hv = *reinterpret_cast<const __half2*>(&f[y]);
+                    __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(hv) * sv, __high2float(hv) * sv);
+                    o[y] = *reinterpret_cast<uint32_t*>(&bv);
+                }
+                const int c16 = 4 * u + q;
+                *reinterpret_cast<uint4*>(rowp + ((c16 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
     k_umma_grouped(const __grid_constant__ CUtensorMap map_pool, const __grid_constant__ CUtensorMap map_shared,
                    const __grid_constant__ CUtensorMap map_b, CallArgs a) {
-    using C = Cfg<MODE>;
+    constexpr bool kFp4 = FMT != FMT_BF16;
+    using C = Cfg<MODE, kFp4>;
     extern __shared__ unsigned char dyn_raw[];
     __shared__ TileSched ts;
-    __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
+    __shared__ const uint8_t* s_ptr[kFp4 ? kMaxExperts + 1 : 1];  // blob of each active expert (FP4)
+    __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_afull[C::kStages];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -218,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_afull[s], 2);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_tfull[s], 1);
@@ -251,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) ts.start[na] = carry;
     }
+    if constexpr (kFp4)
+        for (int u = threadIdx.x; u < na; u += blockDim.x) s_ptr[u] = a.act_ptr[u];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -290,8 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     unsigned char* st = smem + stage * C::kStageBytes;
-                    mbar_expect_tx(&bar_full[stage], C::kStageBytes);
-                    if constexpr (MODE == MODE_GU) {
+                    mbar_expect_tx(&bar_full[stage], kFp4 ? kTileBytes : C::kStageBytes);
+                    if constexpr (kFp4) {
+                        // A tiles come from the transform warps
+                    } else if constexpr (MODE == MODE_GU) {
                         // gate rows of units [128 mt, 128 mt + 128) sit in two 64-row blocks
                         // 128 rows apart; the up rows follow each block
                         const int r0 = (mt * BM / 64) * 128;
@@ -344,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem + acc * C::kAccCols;
                 for (int kb = 0; kb < n_kb; ++kb) {
-                    if (!mbar_wait(&bar_full[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&bar_full[stage], phase, abort_flag) ||
+                        (kFp4 && !mbar_wait(&bar_afull[stage], phase, abort_flag))) {
                         fail(MOE_DEVERR_TIMEOUT_MMA);
                         ok = false;
                         break;
@@ -371,6 +462,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bar_drain);
             const uint64_t t0 = gtimer();
             while (!mbar_test(&bar_drain, 0) && gtimer() - t0 < kWaitNs) {
+            }
+        }
+    } else if (warp >= 6) {
+        // ---------------- A-tile transform (FP4 weights, warps 6-13)
+        if constexpr (kFp4) {
+            const int xw = warp - 6;
+            const int sidx = xw % C::kStages, part = xw / C::kStages;
+            bool ok = true;
+            if (lane == 0 && !wait_ready(a)) *abort_flag = 1;
+            __syncwarp();
+            if (*abort_flag) ok = false;
+            // this warp's positions: sidx, sidx + 4, ... over this CTA's tiles (n_kb each)
+            const int my_tiles = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+            const long long npos = static_cast<long long>(my_tiles) * n_kb;
+            auto where = [&](long long P, const uint8_t*& blob, int& mt, int& kb) {
+                const int i = static_cast<int>(P / n_kb);
+                kb = static_cast<int>(P % n_kb);
+                const int t = blockIdx.x + i * gridDim.x;
+                const int u = find_expert(ts, na, t);
+                const int local = t - ts.start[u];
+                const int n_nt = (a.act_cnt[u] + BN - 1) / BN;
+                mt = local / n_nt;
+                blob = s_ptr[u];
+            };
+            auto process = [&](long long P, const XRows<MODE>& x) -> bool {
+                const uint32_t ph = static_cast<uint32_t>((P / C::kStages) & 1);
+                int got = 1;
+                if (lane == 0) got = mbar_wait(&bar_empty[sidx], ph ^ 1u, abort_flag) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    if (lane == 0) fail(MOE_DEVERR_TIMEOUT_PRODUCER);
+                    return false;
+                }
+                xstore<FMT, MODE>(x, smem + sidx * C::kStageBytes, part, lane);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_afull[sidx]);
+                return true;
+            };
+            XRows<MODE> xa, xb;
+            const uint8_t* blob;
+            int mt, kb;
+            long long P = sidx;
+            if (ok && P < npos) {
+                where(P, blob, mt, kb);
+                xload<FMT, MODE>(a, blob, mt, kb, part, lane, xa);
+            }
+            while (ok && P < npos) {
+                const long long P1 = P + C::kStages;
+                if (P1 < npos) {
+                    where(P1, blob, mt, kb);
+                    xload<FMT, MODE>(a, blob, mt, kb, part, lane, xb);
+                }
+                ok = process(P, xa);
+                if (!ok || P1 >= npos) break;
+                const long long P2 = P1 + C::kStages;
+                if (P2 < npos) {
+                    where(P2, blob, mt, kb);
+                    xload<FMT, MODE>(a, blob, mt, kb, part, lane, xa);
+                }
+                ok = process(P1, xb);
+                P = P2;
             }
         }
     } else {
@@ -525,12 +678,17 @@ cudaError_t umma_set_attributes() {
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16>)))) return e;
     if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32>)))) return e;
-    if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE_GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<MODE_GU>::kSmem)))
+#define MOE_UMMA_ATTR(MODE, FMT)                                                                         \
+    if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                  Cfg<MODE, FMT != FMT_BF16>::kSmem)))                                   \
         return e;
-    if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<MODE_DOWN>::kSmem)))
-        return e;
+    MOE_UMMA_ATTR(MODE_GU, FMT_BF16)
+    MOE_UMMA_ATTR(MODE_DOWN, FMT_BF16)
+    MOE_UMMA_ATTR(MODE_GU, FMT_NVFP4)
+    MOE_UMMA_ATTR(MODE_DOWN, FMT_NVFP4)
+    MOE_UMMA_ATTR(MODE_GU, FMT_MXFP4)
+    MOE_UMMA_ATTR(MODE_DOWN, FMT_MXFP4)
+#undef MOE_UMMA_ATTR
     return cudaSuccess;
 }
 
@@ -538,6 +696,19 @@ static CUtensorMap as_map(const UmmaMap& m) {
     CUtensorMap t;
     std::memcpy(&t, m.bytes, sizeof(t));
     return t;
+}
+
+template <int FMT>
+static void launch_gemms(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s, cudaEvent_t ev_gu) {
+    constexpr int threads = FMT == FMT_BF16 ? kThreads : kThreadsFp4;
+    // FP4 weights do not use the pool / shared tensor maps (their A tiles are built in shared memory)
+    const CUtensorMap pg = as_map(FMT == FMT_BF16 ? maps.pool_gu : maps.x);
+    const CUtensorMap sg = as_map(FMT == FMT_BF16 ? maps.shared_gu : maps.x);
+    const CUtensorMap pd = as_map(FMT == FMT_BF16 ? maps.pool_d : maps.x);
+    const CUtensorMap sd = as_map(FMT == FMT_BF16 ? maps.shared_d : maps.x);
+    k_umma_grouped<MODE_GU, FMT><<<num_sms, threads, Cfg<MODE_GU, FMT != FMT_BF16>::kSmem, s>>>(pg, sg, as_map(maps.x), a);
+    if (ev_gu) cudaEventRecord(ev_gu, s);
+    k_umma_grouped<MODE_DOWN, FMT><<<num_sms, threads, Cfg<MODE_DOWN, FMT != FMT_BF16>::kSmem, s>>>(pd, sd, as_map(maps.h), a);
 }
 
 // gather, gate/up + SwiGLU, down; the combine is launched by the caller
@@ -548,11 +719,12 @@ cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num
     const int gb = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(num_sms) * 16));
     if (a.act == ACT_BF16) k_gather_x<ACT_BF16><<<gb, 256, 0, s>>>(a, rows);
     else k_gather_x<ACT_FP32><<<gb, 256, 0, s>>>(a, rows);
-    k_umma_grouped<MODE_GU><<<num_sms, kThreads, Cfg<MODE_GU>::kSmem, s>>>(as_map(maps.pool_gu), as_map(maps.shared_gu),
-                                                                          as_map(maps.x), a);
-    if (ev_gu) cudaEventRecord(ev_gu, s);
-    k_umma_grouped<MODE_DOWN><<<num_sms, kThreads, Cfg<MODE_DOWN>::kSmem, s>>>(as_map(maps.pool_d),
-                                                                              as_map(maps.shared_d), as_map(maps.h), a);
+    switch (a.fmt) {
+        case FMT_BF16: launch_gemms<FMT_BF16>(a, maps, num_sms, s, ev_gu); break;
+        case FMT_NVFP4: launch_gemms<FMT_NVFP4>(a, maps, num_sms, s, ev_gu); break;
+        case FMT_MXFP4: launch_gemms<FMT_MXFP4>(a, maps, num_sms, s, ev_gu); break;
+        default: return cudaErrorInvalidValue;
+    }
     if (launches) *launches = 3;
     return cudaGetLastError();
 }

@@ -959,7 +959,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
                  static_cast<size_t>(nt) * H * esz / 16);
         for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
         __syncthreads();
-        if (a.fmt != FMT_BF16) xprep_rows<ACT>(route_smem, a.xh, a.fmt, H, t0, nt, threadIdx.x, blockDim.x);
         constexpr int kPass = kRouteWarps * kPrefillEpw;
         for (int eb = 0; eb < E; eb += kPass) {
             const int e0 = eb + warp * kPrefillEpw;

@@ -687,7 +687,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (umma) {
         // TMA descriptors over the gathered activations, h, and the resident shared experts
         bool ok = moe::umma_map_2d(&h->maps.x, a.xperm, rows, H, 128) && moe::umma_map_2d(&h->maps.h, a.hbuf, rows, I, 128);
-        if (ok && ns > 0) {
+        if (ok && ns > 0 && h->d.weight_fmt == moe::FMT_BF16) {
             ok = moe::umma_map_3d(&h->maps.shared_gu, h->shared_dev + h->lay.gu, static_cast<uint64_t>(L) * ns,
                                   h->lay.bytes, 2 * I, H, 64) &&
                  moe::umma_map_3d(&h->maps.shared_d, h->shared_dev + h->lay.d, static_cast<uint64_t>(L) * ns,
@@ -787,7 +787,9 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     CK(h, cudaMemcpy(h->ready, &rv, 8, cudaMemcpyHostToDevice));
     CK(h, cudaDeviceSynchronize());
     h->maps.have_pool = false;
-    if (h->maps.have_io) {
+    if (h->maps.have_io && h->d.weight_fmt != moe::FMT_BF16) {
+        h->maps.have_pool = true;  // FP4 prefill builds its weight tiles in shared memory: no pool maps
+    } else if (h->maps.have_io) {
         const uint64_t H = h->d.hidden, I = h->d.inter;
         if (!moe::umma_map_3d(&h->maps.pool_gu, h->pool + h->lay.gu, S, h->lay.bytes, 2 * I, H, 64) ||
             !moe::umma_map_3d(&h->maps.pool_d, h->pool + h->lay.d, S, h->lay.bytes, H, I, 128)) {
