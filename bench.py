@@ -66,7 +66,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -79,7 +79,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -186,6 +186,8 @@ def run_ours(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     shape, T, frac, flags, L, reuse = WORKLOADS[args.workload]
+    if args.sync_misses:
+        flags |= moe.MOE_CACHE_SYNC_MISSES
     if args.layers:
         L = min(L, args.layers)
     if args.pool_frac:
@@ -201,11 +203,14 @@ def run_ours(args, rank, world, dist):
         router.append(torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16))
     nsteps = args.warmup + args.steps
     # per (step, layer) hidden states, distinct across ranks; with step reuse,
-    # a step repeats the previous step's hidden states in every layer
-    hid = np.empty((nsteps, L, T, shape.H), np.uint16)
-    flags_r = synth.reuse_flags(rank, nsteps, reuse) if reuse > 0 else np.zeros(nsteps, bool)
+    # a step repeats the previous step's hidden states in every layer. The
+    # end-to-end pass runs K further steps of new inputs, so that it does not
+    # replay the timed steps against a cache that has just seen them.
+    ntotal = nsteps + args.steps
+    hid = np.empty((ntotal, L, T, shape.H), np.uint16)
+    flags_r = synth.reuse_flags(rank, ntotal, reuse) if reuse > 0 else np.zeros(ntotal, bool)
     src = 0
-    for st in range(nsteps):
+    for st in range(ntotal):
         src = src if flags_r[st] else st
         for l in range(L):
             hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + src)
@@ -254,6 +259,7 @@ def run_ours(args, rank, world, dist):
     hid_pin = torch.from_numpy(hid.view(np.int16)).view(torch.bfloat16).pin_memory()
     out_pin = torch.empty((L, T, shape.H), dtype=torch.bfloat16).pin_memory()
     xin = torch.empty((L, T, shape.H), dtype=torch.bfloat16, device=dev)
+    x_dev = None
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
@@ -261,7 +267,7 @@ def run_ours(args, rank, world, dist):
     e1 = torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
     e0.record(stream)
-    for st in range(args.warmup, nsteps):
+    for st in range(nsteps, ntotal):
         with torch.cuda.stream(stream):
             xin.copy_(hid_pin[st], non_blocking=True)
         for l in range(L):
@@ -409,7 +415,8 @@ def cpu_baseline(shape, T, L, budget_s=15.0):
 
 def run_reference(args):
     shape, T, frac, flags, L, reuse = WORKLOADS[args.workload]
-    budget = float(os.environ.get("MOE_REF_STEP_BUDGET_S", "1.0"))
+    # each step is a bounded sample of oracle time: about a minute over all steps
+    budget = float(os.environ.get("MOE_REF_STEP_BUDGET_S", min(1.0, 60.0 / max(1, args.steps))))
     for _ in range(args.warmup):
         oracle_layer_seconds(shape, T, L, 0.0)
     secs = []
@@ -434,15 +441,25 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 300 decode, 3 prefill)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 300 decode, 3 prefill)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0, help="run only the first N layers of the stack (profiling)")
+    ap.add_argument("--sync-misses", action="store_true",
+                    help="service each call's misses before its expert kernels are launched "
+                         "(for profilers that serialise launches; not a bench setting)")
     ap.add_argument("--pool-frac", type=float, default=0.0,
                     help="expert pool as a fraction of the stack's experts (default: the workload's)")
     args = ap.parse_args()
+    decode = WORKLOADS[args.workload][1] <= 8
+    if args.steps is None:
+        args.steps = 300 if decode else 3
+    if args.warmup is None:
+        # decode: long enough for the LRU hit rate to settle (a cold 25% pool
+        # fills in ~10 steps; the Zipf-skewed hit rate keeps rising for ~100s)
+        args.warmup = 300 if decode else 3
     if args.warmup < 3:
         args.warmup = 3
     rank = _env_int("RANK", 0)

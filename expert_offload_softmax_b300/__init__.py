@@ -28,6 +28,7 @@ MOE_MODE_SWIGLU, MOE_MODE_LINEAR_TEST = 0, 1
 MOE_DECODE_MAX_T = 8
 MOE_CACHE_PREFETCH_NEXT_LAYER = 1
 MOE_CACHE_LOG_EVENTS = 2
+MOE_CACHE_SYNC_MISSES = 4
 
 # every symbol the header declares
 EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward", "moe_sync",

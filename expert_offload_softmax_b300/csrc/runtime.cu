@@ -757,6 +757,8 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     if (!h) return MOE_ERR_INVALID;
     if (capacity_slots < h->d.top_k) return fail(h, MOE_ERR_CAPACITY, "capacity below top_k");
     if (capacity_slots > moe::kMaxSlots) return fail(h, MOE_ERR_INVALID, "capacity above 16384 slots");
+    if (flags & ~(MOE_CACHE_PREFETCH_NEXT_LAYER | MOE_CACHE_LOG_EVENTS | MOE_CACHE_SYNC_MISSES))
+        return fail(h, MOE_ERR_INVALID, "unknown cache flag");
     CK(h, cudaSetDevice(h->d.device));
     drain(h);
     CK(h, cudaDeviceSynchronize());
@@ -874,16 +876,10 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     if (tc) {
         CK(h, cudaEventRecord(tc->r1, s));
         CK(h, cudaEventRecord(tc->f0, s));
-    }
-    int nl = 0;
-    const cudaError_t le =
-        moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &h->maps, h->num_sms, &nl);
-    if (tc) {
         tc->has_combine = !decode && h->d.weight_fmt != moe::FMT_FP32;
-        if (tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
     }
     // the call is enqueued from here on (the routing kernel is in flight): hand
-    // it to the service thread even if the expert launch failed, so that its
+    // it to the service thread even if the expert launch fails, so that its
     // record is consumed in order
     h->submitted = seq;
     h->prefetch_may_be_pending = want_pf;
@@ -898,10 +894,28 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         pc.self_release = a.self_release != 0;
         pc.tc = tc;
         h->queue.push_back(pc);
-        h->st.kernel_launches += (decode ? 1 : 2) + nl;
         if (tc) h->pending.push_back(tc);
     }
     h->cv.notify_one();
+    if (h->flags & MOE_CACHE_SYNC_MISSES) {
+        // the service thread reads the call's cache result, copies its misses and
+        // posts its release; once those copies have run, the expert kernels below
+        // find the release already there and never wait on the host
+        {
+            std::unique_lock<std::mutex> lk(h->mu);
+            h->done_cv.wait(lk, [&] { return h->serviced.load(std::memory_order_acquire) >= seq; });
+        }
+        CK(h, cudaStreamSynchronize(h->copy));
+        CK(h, cudaStreamSynchronize(h->copy2));
+    }
+    int nl = 0;
+    const cudaError_t le =
+        moe::launch_experts(a, s, tc ? tc->f1 : nullptr, tc ? tc->f2 : nullptr, &h->maps, h->num_sms, &nl);
+    if (tc && tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        h->st.kernel_launches += (decode ? 1 : 2) + nl;
+    }
     if (le != cudaSuccess) return cuda_fail(h, le, "expert kernel launch");
     return MOE_OK;
 }

@@ -77,6 +77,10 @@ typedef enum moe_act_mode { MOE_MODE_SWIGLU = 0, MOE_MODE_LINEAR_TEST = 1 } moe_
 #define MOE_DECODE_MAX_T 8                /* T <= 8: decode path; T > 8: prefill path */
 #define MOE_CACHE_PREFETCH_NEXT_LAYER 1u  /* prefill: stream layer+1 behind layer */
 #define MOE_CACHE_LOG_EVENTS 2u           /* keep a per-expert hit/miss event log */
+#define MOE_CACHE_SYNC_MISSES 4u          /* service each call's misses before its expert
+                                             kernels are launched (the calling thread waits
+                                             for the routing kernel and the copies); for
+                                             debugging and for tools that serialise launches */
 
 typedef struct moe_model_desc {
     int32_t num_layers;   /* L >= 1 */
@@ -164,7 +168,8 @@ int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host*
 /* A safe point: waits until every enqueued call has finished, then (re)builds
  * the expert pool with capacity_slots slots shared by all layers, empties the
  * LRU table and the event log, and clears errors of earlier calls (including a
- * bounded-wait timeout). flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS. Every
+ * bounded-wait timeout). flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS,
+ * MOE_CACHE_SYNC_MISSES; other bits give MOE_ERR_INVALID. Every
  * routed expert must have been loaded before the first forward call.
  * capacity_slots < top_k gives MOE_ERR_CAPACITY. */
 int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
@@ -173,7 +178,8 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
  * hidden [T, H], router_w [E, H], out [T, H], all device memory in the handle's
  * act_dtype, row-major. Enqueued on `stream` (a cudaStream_t; NULL = the
  * handle's own stream) and returns without waiting for the device; the host
- * blocks only when 16 calls are already waiting for the service thread. out is
+ * blocks only when 16 calls are already waiting for the service thread (with
+ * MOE_CACHE_SYNC_MISSES it also blocks until the call's misses have landed). out is
  * complete once `stream` has passed the call. A call whose layer's experts
  * exceed the pool leaves the cache unchanged and out unwritten; the next
  * moe_layer_forward or moe_sync returns MOE_ERR_CAPACITY for it. Errors found

@@ -105,6 +105,28 @@ def test_zipf_skewed_decode_many_steps():
     _run(s, 16, 4, 64, calls)
 
 
+def test_sync_misses_mode_matches_oracle():
+    """MOE_CACHE_SYNC_MISSES moves the miss copies before the expert launches;
+    the cache sequence and the outputs are those of the asynchronous path."""
+    s = synth.Shape("zipf", L=4, E=64, k=8, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16, zipf_s=1.0)
+    _run(s, 16, 4, 64, [(l, 1 + (st % 8), st) for st in range(3) for l in range(4)], flags=4)
+    s = synth.Shape("small", L=4, E=16, k=4, H=256, I=128, fmt=synth.FMT_MXFP4, act=synth.ACT_BF16)
+    _run(s, 13, 4, 40, [(l, 64, 0) for l in range(4)] + [(0, 3, 1)], flags=4 | 1)
+
+
+def test_unknown_cache_flag_is_rejected():
+    import expert_offload_softmax_b300 as moe
+    from moe_harness import GpuStack
+    s = synth.Shape("small", L=1, E=8, k=2, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
+    g = GpuStack(s, 3, 1, 8)
+    try:
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_cache_config(g.h, 8, 64)
+        assert ei.value.code == moe.MOE_ERR_INVALID
+    finally:
+        g.close()
+
+
 def test_capacity_error_leaves_cache_unchanged():
     import expert_offload_softmax_b300 as moe
     from moe_harness import GpuStack
