@@ -141,6 +141,40 @@ def _traffic_for(kernel, workload):
         return None
 
 
+# --------------------------------------------------------------------------- replicas
+
+def rank_hidden_states(shape, rank, nsteps, L, T, reuse):
+    """Hidden states [nsteps, L, T, H] (bf16 bits) of one rank. Every rank
+    draws its own steps (replicas share no inputs); with step reuse, a step
+    repeats the previous step's hidden states in every layer."""
+    hid = np.empty((nsteps, L, T, shape.H), np.uint16)
+    flags_r = synth.reuse_flags(rank, nsteps, reuse) if reuse > 0 else np.zeros(nsteps, bool)
+    src = 0
+    for st in range(nsteps):
+        src = src if flags_r[st] else st
+        for l in range(L):
+            hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + src)
+    return hid
+
+
+def max_over_ranks(dist, x, device=None):
+    """The largest x over all ranks (x itself without a process group). NCCL
+    reduces a device tensor, gloo a host tensor."""
+    if not dist:
+        return float(x)
+    import torch
+    on_dev = dist.get_backend() == "nccl"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if on_dev else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, steps, T, ms_max):
+    """Whole-job tokens/s: every rank runs `steps` steps of T tokens of its own;
+    the job takes as long as its slowest rank."""
+    return world * steps * T / (ms_max * 1e-3)
+
+
 # --------------------------------------------------------------------------- our arm
 
 def load_stack(moe, shape, L, capacity, flags, device, max_tokens, seed=0):
@@ -202,18 +236,10 @@ def run_ours(args, rank, world, dist):
         r = synth.router_weights(shape, 0, l)
         router.append(torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16))
     nsteps = args.warmup + args.steps
-    # per (step, layer) hidden states, distinct across ranks; with step reuse,
-    # a step repeats the previous step's hidden states in every layer. The
-    # end-to-end pass runs K further steps of new inputs, so that it does not
-    # replay the timed steps against a cache that has just seen them.
+    # the end-to-end pass runs K further steps of new inputs, so that it does
+    # not replay the timed steps against a cache that has just seen them
     ntotal = nsteps + args.steps
-    hid = np.empty((ntotal, L, T, shape.H), np.uint16)
-    flags_r = synth.reuse_flags(rank, ntotal, reuse) if reuse > 0 else np.zeros(ntotal, bool)
-    src = 0
-    for st in range(ntotal):
-        src = src if flags_r[st] else st
-        for l in range(L):
-            hid[st, l] = synth.hidden_states(shape, 0, l, T, step=1000003 * rank + src)
+    hid = rank_hidden_states(shape, rank, ntotal, L, T, reuse)
     x_dev = torch.from_numpy(hid.view(np.int16)).to(dev).view(torch.bfloat16)
     out_dev = torch.empty((L, T, shape.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -244,14 +270,10 @@ def run_ours(args, rank, world, dist):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(dist, ev0.elapsed_time(ev1), dev)
     timing = moe.moe_timing(h)
     moe.moe_timing_enable(h, False)
     stats = moe.moe_stats(h)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
 
     # end to end through the public call with host buffers: per step, copy the
     # step's hidden states from pinned host memory, run every layer, read the
@@ -277,12 +299,8 @@ def run_ours(args, rank, world, dist):
         stream.synchronize()
     e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
     e2e_wall = (time.perf_counter() - w0) * 1e3
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
     moe.moe_destroy(h)
 
     if rank != 0:
@@ -290,7 +308,7 @@ def run_ours(args, rank, world, dist):
     pcie = h2d_peak_gbs(torch, dev)
     peaks, peak_kind = _peaks()
     K = args.steps
-    value = world * K * T / (ms * 1e-3)
+    value = job_value(world, K, T, ms)
     # dominant library kernel by device time, over the calls without demand
     # misses (a call with misses also waits for its copies inside the kernel)
     kern = {"gate_up": (timing["gate_up_ms"], timing["gate_up_bytes"]),
