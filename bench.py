@@ -395,40 +395,78 @@ def run_ours(args, rank, world, dist):
 
 # --------------------------------------------------------------------------- oracle
 
+ORACLE_TOKEN_SAMPLE = 16  # above this many tokens a call is timed on samples
+ORACLE_DEQUANT_SAMPLE = 2  # experts dequantised per sampled call
+ORACLE_PAIR_SAMPLE = 8     # (token, expert) products per sampled call
+
+
 def oracle_layer_seconds(shape, T, L, budget_s, step0=0):
     """Times the oracle on layer calls of the workload (T tokens, cycling
-    through the layers) until ~budget_s of oracle time has elapsed. Expert
-    weights are generated untimed; routing, LRU, dequantisation and the expert
-    math are timed. Returns (seconds per layer call, calls)."""
+    through the layers) until ~budget_s of oracle time has elapsed; at least
+    one call. Expert weights are generated untimed.
+
+    Up to ORACLE_TOKEN_SAMPLE tokens the whole call is timed: routing, LRU,
+    dequantisation of the selected experts and the layer's expert math. Above
+    it (prefill; one call of the large stack takes many minutes on one core,
+    most of it dequantising 257 experts) each part is timed on a sample and
+    scaled to the full call: routing of evenly spaced tokens by T / tokens,
+    dequantisation of a few selected experts to every expert of the layer
+    (a prefill call of T*k >= 8*E assignments selects them all), and the
+    expert FFN on a few (token, expert) pairs to all T*(k + shared) pairs.
+    Returns (estimated seconds per full layer call, calls, tokens routed)."""
     import oracle
     from moe_harness import act_to_f32
     lru = oracle.LRU(L, shape.E, synth.capacity_slots(shape, 0.25))
     routers = {}
-    spent, calls = 0.0, 0
+    spent, est, calls = 0.0, 0.0, 0
+    sampled = T > ORACLE_TOKEN_SAMPLE
+    ns = ORACLE_TOKEN_SAMPLE if sampled else T
+    toks = np.linspace(0, T - 1, ns).round().astype(np.int64)
+    shared = list(range(shape.E, shape.E + shape.shared))
     while spent < budget_s or calls == 0:
         l = calls % L
         if l not in routers:
             routers[l] = act_to_f32(synth.router_weights(shape, 0, l), shape)
-        x = act_to_f32(synth.hidden_states(shape, 0, l, T, step=step0 + calls), shape)
+        x = act_to_f32(synth.hidden_states(shape, 0, l, T, step=step0 + calls), shape)[toks]
         t0 = time.perf_counter()
         r = oracle.route(x, routers[l], shape.k)
         lru.access(l, r["uniq"], T, False)
         t1 = time.perf_counter()
-        need = sorted(set(int(e) for e in np.unique(r["topk_idx"])) | set(range(shape.E, shape.E + shape.shared)))
+        need = sorted(set(int(e) for e in np.unique(r["topk_idx"])) | set(shared))
+        if sampled:
+            need = need[:ORACLE_DEQUANT_SAMPLE]
         raw = {e: synth.expert_weights(shape, 0, l, e) for e in need}
         t2 = time.perf_counter()
         ws = {e: oracle.dequant_expert(shape.fmt, raw[e], shape.H, shape.I) for e in need}
-        oracle.layer_tokens(x, r["topk_idx"], r["gates"], ws, shape.E, shape.shared, shape.act_mode, np.arange(T))
         t3 = time.perf_counter()
-        spent += (t1 - t0) + (t3 - t2)
+        if sampled:
+            for i in range(ORACLE_PAIR_SAMPLE):
+                oracle.expert_ffn(x[i % ns], *ws[need[i % len(need)]], shape.act_mode)
+        else:
+            oracle.layer_tokens(x, r["topk_idx"], r["gates"], ws, shape.E, shape.shared, shape.act_mode,
+                                np.arange(ns))
+        t4 = time.perf_counter()
+        spent += (t1 - t0) + (t4 - t2)
+        if sampled:
+            est += ((t1 - t0) * T / ns + (t3 - t2) * (shape.E + shape.shared) / len(need)
+                    + (t4 - t3) * T * (shape.k + shape.shared) / ORACLE_PAIR_SAMPLE)
+        else:
+            est += (t1 - t0) + (t4 - t2)
         calls += 1
-    return spent / calls, calls
+    return est / calls, calls, ns
 
 
 def cpu_baseline(shape, T, L, budget_s=15.0):
-    per_call, calls = oracle_layer_seconds(shape, T, L, budget_s)
-    return {"value": round(T / (per_call * L), 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{calls} layer calls (T={T}) of the {L}-layer stack; tokens/s = T / (L x mean s per call)"}
+    if budget_s <= 0:
+        return None
+    per_call, calls, ns = oracle_layer_seconds(shape, T, L, budget_s)
+    sample = f"{calls} layer calls (T={T}) of the {L}-layer stack; tokens/s = T / (L x mean s per call)"
+    if ns < T:
+        sample += (f"; each call timed on samples scaled to the full call: routing of {ns} evenly spaced "
+                   f"tokens, dequantisation of {ORACLE_DEQUANT_SAMPLE} of the {shape.E + shape.shared} "
+                   f"experts, the expert FFN on {ORACLE_PAIR_SAMPLE} of the {T * (shape.k + shape.shared)} "
+                   f"(token, expert) pairs")
+    return {"value": round(T / (per_call * L), 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
@@ -438,8 +476,9 @@ def run_reference(args):
     for _ in range(args.warmup):
         oracle_layer_seconds(shape, T, L, 0.0)
     secs = []
+    ns = T
     for st in range(args.steps):
-        per_call, _ = oracle_layer_seconds(shape, T, L, budget, step0=10007 * (st + 1))
+        per_call, _, ns = oracle_layer_seconds(shape, T, L, budget, step0=10007 * (st + 1))
         secs.append(per_call * L)
     ms = float(np.mean(secs)) * 1e3
     value = T / (ms * 1e-3)
@@ -451,7 +490,10 @@ def run_reference(args):
         "config": {"workload": shape.name, "T": T, "layers": L, "pool_frac": frac},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step: layer calls (T={T}) for ~{budget:.1f} s of oracle time, "
-                                   f"scaled to the {L}-layer stack"},
+                                   f"scaled to the {L}-layer stack"
+                                   + (f"; each call timed on samples ({ns} tokens routed, "
+                                      f"{ORACLE_DEQUANT_SAMPLE} experts dequantised, {ORACLE_PAIR_SAMPLE} "
+                                      f"expert FFNs) scaled to the full call" if ns < T else "")},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -41,3 +41,15 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_reference_arm_other_ranks_exit_quietly():
     assert _run({"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_cpu_baseline_samples_large_calls_and_times_small_ones_whole():
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    s = synth.Shape("cb", L=2, E=16, k=4, H=128, I=64, fmt=synth.FMT_MXFP4, act=synth.ACT_BF16, shared=1)
+    whole = bench.cpu_baseline(s, 4, 2, budget_s=0.01)
+    assert whole["kind"] == "oracle" and whole["value"] > 0 and "samples" not in whole["sample"]
+    part = bench.cpu_baseline(s, 256, 2, budget_s=0.01)
+    assert part["value"] > 0 and "samples" in part["sample"] and "1280" in part["sample"]
+    assert bench.cpu_baseline(s, 4, 2, budget_s=0) is None
