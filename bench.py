@@ -416,7 +416,7 @@ def oracle_layer_seconds(shape, T, L, budget_s, step0=0):
     Returns (estimated seconds per full layer call, calls, tokens routed)."""
     import oracle
     from moe_harness import act_to_f32
-    lru = oracle.LRU(L, shape.E, synth.capacity_slots(shape, 0.25))
+    lru = oracle.LRU(L, shape.E, max(shape.E, synth.capacity_slots(shape, 0.25)))
     routers = {}
     spent, est, calls = 0.0, 0.0, 0
     sampled = T > ORACLE_TOKEN_SAMPLE
