@@ -138,7 +138,11 @@ struct moe_handle {
     // stats (mu)
     moe_stats_t st{};
     std::vector<moe_event> events;
+    // message of the last failed call (err_mu: loaders may fail concurrently)
+    std::mutex err_mu;
     std::string err;
+    // host banks are allocated by whichever loader thread first needs them
+    std::mutex load_mu;
 };
 
 namespace {
@@ -146,7 +150,10 @@ namespace {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int fail(moe_handle* h, int code, const std::string& msg) {
-    if (h) h->err = msg;
+    if (h) {
+        std::lock_guard<std::mutex> lk(h->err_mu);
+        h->err = msg;
+    }
     return code;
 }
 
@@ -561,7 +568,10 @@ int take_error(moe_handle* h) {
     std::lock_guard<std::mutex> lk(h->mu);
     if (h->pending_err == MOE_OK) return MOE_OK;
     const int e = h->pending_err;
-    h->err = h->pending_msg;
+    {
+        std::lock_guard<std::mutex> lk2(h->err_mu);
+        h->err = h->pending_msg;
+    }
     if (!h->sticky_timeout) {
         h->pending_err = MOE_OK;
         h->pending_msg.clear();
@@ -739,15 +749,20 @@ int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host*
                          cudaMemcpyHostToDevice));
         return MOE_OK;
     }
-    if (!h->bank[layer]) {
-        void* p = nullptr;
-        if (cudaHostAlloc(&p, static_cast<size_t>(E) * B, cudaHostAllocDefault) != cudaSuccess) {
-            cudaGetLastError();
-            return fail(h, MOE_ERR_OOM, "pinned host bank allocation failed");
+    uint8_t* bank;
+    {
+        std::lock_guard<std::mutex> lk(h->load_mu);
+        if (!h->bank[layer]) {
+            void* p = nullptr;
+            if (cudaHostAlloc(&p, static_cast<size_t>(E) * B, cudaHostAllocDefault) != cudaSuccess) {
+                cudaGetLastError();
+                return fail(h, MOE_ERR_OOM, "pinned host bank allocation failed");
+            }
+            h->bank[layer] = static_cast<uint8_t*>(p);
         }
-        h->bank[layer] = static_cast<uint8_t*>(p);
+        bank = h->bank[layer];
     }
-    int r = repack_expert(h->d, h->lay, w, h->bank[layer] + static_cast<size_t>(expert) * B, &why);
+    int r = repack_expert(h->d, h->lay, w, bank + static_cast<size_t>(expert) * B, &why);
     if (r != MOE_OK) return fail(h, r, why);
     h->loaded[static_cast<size_t>(layer) * E + expert] = 1;
     return MOE_OK;

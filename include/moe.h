@@ -162,7 +162,10 @@ int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
 /* Copies one expert from the canonical host layout into the library's pinned
  * host bank (routed experts, expert < E) or into device-resident memory
  * (shared experts, E <= expert < E + num_shared), repacking it into the device
- * layout. The caller's buffers may be freed on return. Synchronous. */
+ * layout. The caller's buffers may be freed on return. Synchronous. Unlike the
+ * other calls, which expect one host thread at a time per handle, this one may
+ * run concurrently from several host threads (e.g. one per layer), as long as
+ * no forward call is in progress; each (layer, expert) is loaded by one thread. */
 int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host* w);
 
 /* A safe point: waits until every enqueued call has finished, then (re)builds
