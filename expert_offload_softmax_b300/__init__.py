@@ -31,7 +31,7 @@ MOE_CACHE_LOG_EVENTS = 2
 MOE_CACHE_SYNC_MISSES = 4
 
 # every symbol the header declares
-EXPORTS = ["moe_init", "moe_expert_bytes", "moe_load_expert", "moe_cache_config", "moe_layer_forward", "moe_sync",
+EXPORTS = ["moe_init", "moe_expert_bytes", "moe_repack_expert", "moe_load_expert", "moe_cache_config", "moe_layer_forward", "moe_sync",
            "moe_stats", "moe_stats_reset", "moe_stats_events", "moe_debug_routing", "moe_debug_lru_table",
            "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing", "moe_route_topk_noalloc"]
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
@@ -96,6 +96,7 @@ def load(path: str | None = None):
     P = ctypes.POINTER
     lib.moe_init.argtypes = [P(moe_model_desc), P(vp)]
     lib.moe_expert_bytes.argtypes = [P(moe_model_desc), P(ctypes.c_size_t)]
+    lib.moe_repack_expert.argtypes = [P(moe_model_desc), P(moe_expert_host), ctypes.c_void_p, ctypes.c_size_t]
     lib.moe_load_expert.argtypes = [vp, i32, i32, P(moe_expert_host)]
     lib.moe_cache_config.argtypes = [vp, i32, u32]
     lib.moe_layer_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp]
@@ -153,6 +154,20 @@ def _tensor(t: dict) -> moe_tensor_host:
     sc = np.ascontiguousarray(t["scales"]) if "scales" in t else None
     th = moe_tensor_host(data.ctypes.data, None if sc is None else sc.ctypes.data, float(t.get("gscale", 1.0)))
     return th, (data, sc)
+
+
+def moe_repack_expert(desc: moe_model_desc, w: dict) -> np.ndarray:
+    """The device-layout blob (uint8, moe_expert_bytes long) of canonical weights w. Host only."""
+    g, kg = _tensor(w["gate"])
+    u, ku = _tensor(w["up"])
+    d, kd = _tensor(w["down"])
+    eh = moe_expert_host(g, u, d)
+    blob = np.empty(moe_expert_bytes(desc), np.uint8)
+    rc = load().moe_repack_expert(ctypes.byref(desc), ctypes.byref(eh), blob.ctypes.data, blob.size)
+    del kg, ku, kd
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_repack_expert failed")
+    return blob
 
 
 def moe_load_expert(h: int, layer: int, expert: int, w: dict) -> None:

@@ -602,6 +602,16 @@ int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes) {
     return MOE_OK;
 }
 
+int moe_repack_expert(const moe_model_desc* desc, const moe_expert_host* w, void* blob, size_t blob_bytes) {
+    std::string why;
+    const int v = validate_desc(desc, &why);
+    if (v != MOE_OK) return v;
+    if (!w || !blob) return MOE_ERR_INVALID;
+    const BlobLayout L = layout_for(*desc);
+    if (blob_bytes < L.bytes) return MOE_ERR_INVALID;
+    return repack_expert(*desc, L, w, static_cast<uint8_t*>(blob), &why);
+}
+
 int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (!out) return MOE_ERR_INVALID;
     *out = nullptr;

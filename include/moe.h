@@ -159,6 +159,13 @@ int moe_init(const moe_model_desc* desc, moe_handle** out);
  * stores and copies). */
 int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
 
+/* Writes one expert, given in the canonical host layout, into `blob` (host
+ * memory of blob_bytes >= moe_expert_bytes) in the library's device layout:
+ * the bytes moe_load_expert keeps in its pinned bank and a cache slot holds.
+ * Host-only (no device is touched); for tools that prepare or inspect blobs.
+ * MOE_ERR_INVALID for a bad shape, NULL pointers or a short buffer. */
+int moe_repack_expert(const moe_model_desc* desc, const moe_expert_host* w, void* blob, size_t blob_bytes);
+
 /* Copies one expert from the canonical host layout into the library's pinned
  * host bank (routed experts, expert < E) or into device-resident memory
  * (shared experts, E <= expert < E + num_shared), repacking it into the device
