@@ -38,8 +38,9 @@
  *    alive until the work on `stream` has completed).
  *  - Host pointers: everything in moe_model_desc / moe_expert_host / result
  *    buffers; the library copies what it keeps before returning.
- *  - One handle is used by one host thread, and all forward calls on a handle
- *    are issued on one CUDA stream (the cache's slot reuse is ordered by it).
+ *  - One handle is used by one host thread at a time (moe_load_expert excepted:
+ *    see there), and all forward calls on a handle are issued on one CUDA
+ *    stream (the cache's slot reuse is ordered by it).
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
