@@ -351,6 +351,9 @@ def run_ours(args, rank, world, dist):
                         "frac": round(achieved / peak, 4) if dom == "gate_up" else None},
                 "traffic": traffic}
     cpu = cpu_baseline(shape, T, L, budget_s=args.cpu_budget) if world == 1 else None
+    blob = moe.moe_expert_bytes(moe.make_desc(1, shape.E, shape.k, shape.H, shape.I, shape.fmt, shape.act,
+                                              shared=shape.shared))
+    ws_bytes = (stats["hits"] + stats["misses"]) * blob // max(1, K)
     cap_hits = stats["hits"] + stats["misses"]
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -364,8 +367,8 @@ def run_ours(args, rank, world, dist):
                    "T": T, "layers": L, "pool_slots": S, "pool_frac": frac,
                    "router_zipf_s": shape.zipf_s, "cache_flags": flags, "step_reuse_p": reuse,
                    "shared_experts": shape.shared,
-                   "l2": "per-step working set (active experts' weights, %d MB) exceeds the 126 MB L2"
-                         % ((timing["gate_up_bytes"] + timing["down_bytes"]) // max(1, K) // (1 << 20)),
+                   "l2": "per-step working set (the weights of every expert a step selects, %d MB) exceeds "
+                         "the 126 MB L2" % (ws_bytes // (1 << 20)),
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roof,
         "kernels_us_per_call": {"route+cache": round(timing["route_ms"] * 1e3 / max(1, timing["calls"]), 2),
