@@ -306,6 +306,22 @@ def run_ours(args, rank, world, dist):
     if rank != 0:
         return None
     pcie = h2d_peak_gbs(torch, dev)
+    meas = {"ms": ms, "e2e_ms": e2e_ms, "e2e_wall": e2e_wall, "timing": timing, "stats": stats, "pcie": pcie,
+            "clk": clk, "t_load": t_load, "S": S, "frac": frac, "flags": flags, "L": L}
+    return make_line(args, world, meas, moe.moe_expert_bytes(moe.make_desc(
+        1, shape.E, shape.k, shape.H, shape.I, shape.fmt, shape.act, shared=shape.shared)))
+
+
+def make_line(args, world, meas, blob_bytes):
+    """The bench's JSON line from one run's measurements: meas holds the timed
+    and end-to-end durations (ms, max over ranks), the library's timing and
+    stats counters, the PCIe peak, the clock record and the run's stack
+    parameters; blob_bytes is one expert's size in the device layout."""
+    shape, T, _, _, _, reuse = WORKLOADS[args.workload]
+    ms, e2e_ms, e2e_wall = meas["ms"], meas["e2e_ms"], meas["e2e_wall"]
+    timing, stats, pcie, clk, t_load = meas["timing"], meas["stats"], meas["pcie"], meas["clk"], meas["t_load"]
+    S, frac, flags, L = meas["S"], meas["frac"], meas["flags"], meas["L"]
+    blob = blob_bytes
     peaks, peak_kind = _peaks()
     K = args.steps
     value = job_value(world, K, T, ms)
@@ -351,8 +367,6 @@ def run_ours(args, rank, world, dist):
                         "frac": round(achieved / peak, 4) if dom == "gate_up" else None},
                 "traffic": traffic}
     cpu = cpu_baseline(shape, T, L, budget_s=args.cpu_budget) if world == 1 else None
-    blob = moe.moe_expert_bytes(moe.make_desc(1, shape.E, shape.k, shape.H, shape.I, shape.fmt, shape.act,
-                                              shared=shape.shared))
     ws_bytes = (stats["hits"] + stats["misses"]) * blob // max(1, K)
     cap_hits = stats["hits"] + stats["misses"]
     line = {

@@ -53,3 +53,43 @@ def test_cpu_baseline_samples_large_calls_and_times_small_ones_whole():
     part = bench.cpu_baseline(s, 256, 2, budget_s=0.01)
     assert part["value"] > 0 and "samples" in part["sample"] and "1280" in part["sample"]
     assert bench.cpu_baseline(s, 4, 2, budget_s=0) is None
+
+
+def _fake_meas(T, K, L):
+    R = K * L - 3  # calls whose experts all hit: the expert-kernel counters cover these
+    timing = {"calls": K * L, "resident_calls": R, "route_ms": 0.02 * K * L, "gate_up_ms": 0.02 * R,
+              "down_ms": 0.001 * R, "combine_ms": 0.0, "copy_ms": 0.3 * K,
+              "gate_up_bytes": 10_000_000 * R, "down_bytes": 4_000_000 * R,
+              "combine_bytes": 0, "copy_bytes": 13_000_000 * K}
+    stats = {"hits": 300 * K, "misses": 8 * K, "prefetch_misses": 0, "bytes_h2d": 13_000_000 * K,
+             "kernel_launches": 2 * K * L}
+    return {"ms": 2.0 * K, "e2e_ms": 2.5 * K, "e2e_wall": 2.6 * K, "timing": timing, "stats": stats,
+            "pcie": 52.0, "clk": {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": [], "samples": 5},
+            "t_load": 12.0, "S": 2560, "frac": 0.25, "flags": 0, "L": L}
+
+
+def test_bench_line_from_measurements():
+    """The JSON line the GPU arm prints, built from fake counters on the CPU."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    K, L = 300, 40
+    args = argparse.Namespace(workload="decode", steps=K, warmup=300, cpu_budget=0)
+    d = bench.make_line(args, 1, _fake_meas(1, K, L), 1769984)
+    json.dumps(d)
+    assert d["value"] == round(K * 1 / (2.0 * K * 1e-3), 3) == 500.0
+    assert d["ms_per_step"] == 2.0 and d["steps"] == K and d["warmup"] == 300
+    assert d["e2e"]["value"] == 400.0 and d["e2e"]["h2d_bytes_per_step"] == L * 2048 * 2
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"].startswith("k_dec_fp4")
+    assert r["algorithmic_bytes_per_launch"] == 14_000_000
+    assert abs(r["achieved"] - 14_000_000 / 20e-6 / 1e9) < 0.1 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-4
+    assert d["gpu_launches"] == 2 * K * L and d["cpu_baseline"] is None
+    assert d["cache"]["hit_rate"] == round(300 / 308, 4)
+    assert "%d MB" % (308 * 1769984 // (1 << 20)) in d["config"]["l2"]
+    # prefill: tensor roofline on the gate/up GEMM
+    args = argparse.Namespace(workload="prefill", steps=3, warmup=3, cpu_budget=0)
+    d = bench.make_line(args, 1, _fake_meas(4096, 3, 2), 6291456)
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and "tcgen05" in r["kernel"]
+    assert r["algorithmic_flops_per_launch"] == 4.0 * 512 * 2048 * 4096 * 8
