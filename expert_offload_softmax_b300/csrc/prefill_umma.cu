@@ -48,7 +48,6 @@ constexpr int kThreads = 192;                   // BF16 weights: producer, MMA, 
 constexpr int kXformWarps = 8;                  // FP4 weights: + warps that widen the A tiles to BF16
 constexpr int kThreadsFp4 = kThreads + 32 * kXformWarps;
 constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand tile
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 enum { MODE_GU = 0, MODE_DOWN = 1 };
 
@@ -94,14 +93,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete. Gives up (false) when
-// another role of this CTA has aborted or after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+// another role of this CTA has aborted or after wait_ns (the handle's bound on
+// every device wait, MOE_WAIT_MS).
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long wait_ns) {
     if (mbar_test(b, parity)) return true;
     const uint64_t t0 = gtimer();
     for (;;) {
         if (mbar_test(b, parity)) return true;
         if (*abort_flag) return false;
-        if (gtimer() - t0 > kWaitNs) return false;
+        if (gtimer() - t0 > wait_ns) return false;
     }
 }
 
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 const int z = sl >= 0 ? sl : -sl - 1;
                 const int brow = a.act_row0[u] + nt * BN;
                 for (int kb = 0; kb < n_kb; ++kb) {
-                    if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag, a.wait_ns)) {
                         fail(MOE_DEVERR_TIMEOUT_PRODUCER);
                         ok = false;
                         break;
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                     if (issued_phase[s] >= 0) {
                         const uint64_t t0 = gtimer();
                         while (!mbar_test(&bar_full[s], static_cast<uint32_t>(issued_phase[s])) &&
-                               gtimer() - t0 < kWaitNs) {
+                               gtimer() - t0 < a.wait_ns) {
                         }
                     }
             }
@@ -427,15 +428,15 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 const uint32_t idesc = idesc_bf16(BM, (rows + 15) & ~15);
                 const int acc = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
-                if (!mbar_wait(&bar_tempty[acc], aph ^ 1u, abort_flag)) {
+                if (!mbar_wait(&bar_tempty[acc], aph ^ 1u, abort_flag, a.wait_ns)) {
                     fail(MOE_DEVERR_TIMEOUT_MMA);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d0 = tmem + acc * C::kAccCols;
                 for (int kb = 0; kb < n_kb; ++kb) {
-                    if (!mbar_wait(&bar_full[stage], phase, abort_flag) ||
-                        (kFp4 && !mbar_wait(&bar_afull[stage], phase, abort_flag))) {
+                    if (!mbar_wait(&bar_full[stage], phase, abort_flag, a.wait_ns) ||
+                        (kFp4 && !mbar_wait(&bar_afull[stage], phase, abort_flag, a.wait_ns))) {
                         fail(MOE_DEVERR_TIMEOUT_MMA);
                         ok = false;
                         break;
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             // every MMA issued by this thread has completed once bar_drain flips
             umma_commit(&bar_drain);
             const uint64_t t0 = gtimer();
-            while (!mbar_test(&bar_drain, 0) && gtimer() - t0 < kWaitNs) {
+            while (!mbar_test(&bar_drain, 0) && gtimer() - t0 < a.wait_ns) {
             }
         }
     } else if (warp >= 6) {
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             auto process = [&](long long P, const XRows<MODE>& x) -> bool {
                 const uint32_t ph = static_cast<uint32_t>((P / C::kStages) & 1);
                 int got = 1;
-                if (lane == 0) got = mbar_wait(&bar_empty[sidx], ph ^ 1u, abort_flag) ? 1 : 0;
+                if (lane == 0) got = mbar_wait(&bar_empty[sidx], ph ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     if (lane == 0) fail(MOE_DEVERR_TIMEOUT_PRODUCER);
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             const int r0 = a.act_row0[u] + nt * BN;
             const int acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
-            if (!mbar_wait(&bar_tfull[acc], aph, abort_flag)) {
+            if (!mbar_wait(&bar_tfull[acc], aph, abort_flag, a.wait_ns)) {
                 fail(MOE_DEVERR_TIMEOUT_EPILOGUE);
                 break;
             }

@@ -27,6 +27,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxGridY = 65535;  // CUDA's limit on a grid's y extent
 
 // logits scratch [T][E]
 __device__ __align__(256) float g_route_scratch[MOE_ROUTE_NOALLOC_MAX_LOGITS];
@@ -159,13 +160,15 @@ int setup_device(int dev, float** out) {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return MOE_ERR_CUDA;
         const int big = 200 * 1024;
-        if (cudaFuncSetAttribute(k_na_logits<moe::ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess ||
+            cudaFuncSetAttribute(k_na_logits<moe::ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(k_na_logits<moe::ACT_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
-                cudaSuccess)
+                cudaSuccess) {
+            cudaGetLastError();  // this call's own failure
             return MOE_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = static_cast<float*>(p);
     }
     *out = g_scratch_ptr[dev];
@@ -182,6 +185,7 @@ extern "C" int moe_route_topk_noalloc(const void* hidden, const void* router_w, 
     const size_t esz = act_dtype == MOE_ACT_BF16 ? 2 : 4;
     if (static_cast<size_t>(8) * H * esz > 200 * 1024) return MOE_ERR_INVALID;
     if (static_cast<size_t>(T) * E > static_cast<size_t>(MOE_ROUTE_NOALLOC_MAX_LOGITS)) return MOE_ERR_INVALID;
+    if ((T + 7) / 8 > kMaxGridY) return MOE_ERR_INVALID;  // token blocks are the logits grid's y extent
     if (T == 0) return MOE_OK;
     if (!hidden || !router_w || !topk_idx || !gates) return MOE_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(router_w)) & 15u) return MOE_ERR_INVALID;
@@ -192,11 +196,26 @@ extern "C" int moe_route_topk_noalloc(const void* hidden, const void* router_w, 
     if (rc != MOE_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid((E + 7) / 8, (T + 7) / 8);
-    const size_t smem = static_cast<size_t>(8) * H * esz;
-    if (act_dtype == MOE_ACT_BF16)
-        k_na_logits<moe::ACT_BF16><<<grid, 256, smem, s>>>(hidden, router_w, T, E, H, scratch);
-    else
-        k_na_logits<moe::ACT_FP32><<<grid, 256, smem, s>>>(hidden, router_w, T, E, H, scratch);
-    k_na_topk<<<(T + 7) / 8, 256, 0, s>>>(scratch, T, E, k, topk_idx, gates);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    size_t smem = static_cast<size_t>(8) * H * esz;
+    // each launch's own status: an error another call left pending is neither
+    // reported nor cleared here, and a failed launch of this call clears its own
+    {
+        void* args[] = {const_cast<void**>(&hidden), const_cast<void**>(&router_w), &T, &E, &H, &scratch};
+        const void* fn = act_dtype == MOE_ACT_BF16 ? reinterpret_cast<const void*>(&k_na_logits<moe::ACT_BF16>)
+                                                   : reinterpret_cast<const void*>(&k_na_logits<moe::ACT_FP32>);
+        if (cudaLaunchKernel(fn, grid, dim3(256), args, smem, s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    }
+    {
+        void* args[] = {&scratch, &T, &E, &k, &topk_idx, &gates};
+        smem = 0;
+        if (cudaLaunchKernel(reinterpret_cast<const void*>(&k_na_topk), dim3((T + 7) / 8), dim3(256), args, smem, s) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    }
+    return MOE_OK;
 }

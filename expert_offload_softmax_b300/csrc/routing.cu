@@ -239,7 +239,8 @@ __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, c
 //   divided by their sum. Lane j < k returns selection j.
 // --------------------------------------------------------------------------
 
-// float -> unsigned with the same order (NaN never reaches it)
+// float -> unsigned with the same order (NaN never reaches it; callers turn
+// -0.0 into +0.0 first, since the two compare equal)
 __device__ __forceinline__ uint32_t ord_key(float v) {
     const uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -258,6 +259,7 @@ __device__ __forceinline__ void warp_topk_n(const float* lrow, int E, int k, int
         float x = -INFINITY;
         if (e < E) x = GLOBAL ? __ldcg(lrow + e) : lrow[e];
         if (x != x) x = -INFINITY;
+        x = __fadd_rn(x, 0.0f);  // -0.0 -> +0.0: the two zeros are one logit value (equal, lower index wins)
         v[i] = x;
         key[i] = ord_key(x);
     }

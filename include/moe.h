@@ -240,8 +240,10 @@ int moe_debug_lru_table(moe_handle* h, int32_t* table);
  *  stream: a cudaStream_t (NULL = legacy default stream), on the current device
  * Scratch: a file-scope device array of MOE_ROUTE_NOALLOC_MAX_LOGITS floats
  * (4 MiB, held by every GPU that loads the library until exit); T*E above it,
- * E > 1024, k > min(E, 32), H not a positive multiple of 8 or too large for the
- * shared-memory tile give MOE_ERR_INVALID. Calls no allocator. The first call
+ * T above 8 * 65535 = 524280 (the token blocks of its logits grid), E > 1024,
+ * k > min(E, 32), H not a positive multiple of 8 or too large for the
+ * shared-memory tile give MOE_ERR_INVALID. A failed launch gives MOE_ERR_CUDA;
+ * CUDA errors that other calls left pending are neither reported nor cleared. Calls no allocator. The first call
  * on a device, with that device current, looks the array's address up
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make it
  * before any stream capture. All calls share the array and it keeps the last

@@ -13,16 +13,20 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def test_logit_order_golden():
-    line = [l for l in open(os.path.join(GOLDEN, "logit_order.txt")) if not l.startswith("#")][0]
-    lhs, rhs = line.split("->")
-    parts = lhs.split()
-    H = int(parts[0])
-    w = np.zeros((1, H), np.float32)
-    for p in parts[1:]:
-        i, v = p.split(":")
-        w[0, int(i)] = float(v)
-    x = np.ones((1, H), np.float32)
-    assert oracle.router_logits(x, w)[0, 0] == float(rhs)
+    """Every hand-worked case of the fixture: the chunk -> partial mapping and
+    the order in which the 32 partials are combined."""
+    lines = [l for l in open(os.path.join(GOLDEN, "logit_order.txt")) if l.strip() and not l.startswith("#")]
+    assert len(lines) >= 2
+    for line in lines:
+        lhs, rhs = line.split("->")
+        parts = lhs.split()
+        H = int(parts[0])
+        w = np.zeros((1, H), np.float32)
+        for p in parts[1:]:
+            i, v = p.split(":")
+            w[0, int(i)] = float(v)
+        x = np.ones((1, H), np.float32)
+        assert oracle.router_logits(x, w)[0, 0] == float(rhs), line
 
 
 def test_logits_match_exact_sum_on_integers():
