@@ -62,6 +62,7 @@ def _L():
         lib.orc_expert_ffn.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp]
         lib.orc_layer_tokens.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                          vp, i32, vp]
+        lib.orc_combine.argtypes = [i32, i32, i32, vp, vp, vp]
         _lib = lib
     return _lib
 
@@ -227,6 +228,19 @@ def expert_ffn(x: np.ndarray, Wg, Wu, Wd, mode: int = 0):
     _L().orc_expert_ffn(_p(x), _p(_c(Wg, np.float32)), _p(_c(Wu, np.float32)),
                         _p(_c(Wd, np.float32)), H, I, mode, _p(y), _p(h))
     return y, h
+
+
+def combine(gates_row: np.ndarray, ys) -> np.ndarray:
+    """One token's layer output from its k routed expert outputs ``ys[:k]``
+    (in selection order) and its shared expert outputs ``ys[k:]``."""
+    g = _c(gates_row, np.float32)
+    k = g.size
+    rows = [_c(y, np.float32) for y in ys]
+    H = rows[0].size
+    arr = (ctypes.c_void_p * len(rows))(*[r.ctypes.data for r in rows])
+    out = np.empty(H, np.float32)
+    _L().orc_combine(H, k, len(rows) - k, _p(g), arr, _p(out))
+    return out
 
 
 def layer_tokens(x_f32: np.ndarray, idx: np.ndarray, gates: np.ndarray, weights: dict,

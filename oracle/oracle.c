@@ -347,3 +347,16 @@ void orc_layer_tokens(const float* x, int H, int I, int E, int n_shared, int k, 
     }
     free(y);
 }
+
+/* The combine step of orc_layer_tokens on its own, for callers that computed
+ * the expert outputs separately (one expert at a time over many tokens):
+ * out = sum over j = 0..k-1 (in that order) of gates[j] * y[j], then plus,
+ * unweighted, y[k + s] for each shared expert s. y holds k + n_shared rows of
+ * H floats. Same operations, in the same order, as orc_layer_tokens. */
+void orc_combine(int H, int k, int n_shared, const float* gates, const float* const* y, float* out) {
+    for (int r = 0; r < H; ++r) out[r] = 0.0f;
+    for (int j = 0; j < k; ++j)
+        for (int r = 0; r < H; ++r) out[r] = out[r] + gates[j] * y[j][r];
+    for (int s = 0; s < n_shared; ++s)
+        for (int r = 0; r < H; ++r) out[r] = out[r] + y[k + s][r];
+}

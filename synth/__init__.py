@@ -154,6 +154,13 @@ NVFP4_GSCALE = 1.561e-4
 MXFP4_SCALE_BYTES = (118, 121)
 
 
+# Test-only block-scale tables: every finite E4M3 byte (all but the two NaN
+# codes 0x7F, 0xFF: subnormals, zeros and negative scales included), and E8M0
+# exponent bytes 100..154 (2^-27 .. 2^27).
+E4M3_FINITE_BYTES = tuple(b for b in range(256) if b & 0x7F != 0x7F)
+E8M0_WIDE_BYTES = tuple(range(100, 155))
+
+
 # ---------------------------------------------------------------------------
 # fills
 # ---------------------------------------------------------------------------
@@ -210,6 +217,7 @@ class Shape:
     router_std: float = 0.02
     zipf_s: float = 0.0  # router skew exponent (0 = none)
     act_mode: int = 0    # 0 = SwiGLU, 1 = linear stand-in (closed-form tests)
+    scale_table: tuple = ()  # FP4 block-scale bytes to draw from (uniformly), instead of the default range
 
     def elems_per_expert(self) -> int:
         return 3 * self.H * self.I
@@ -248,12 +256,18 @@ def _tensor(shape: Shape, seed: int, layer: int, expert: int, tag: int, N: int, 
         return {"data": normal_bf16(kd, N * K, shape.w_std).reshape(N, K)}
     codes = code_bytes(kd, N * K // 2).reshape(N, K // 2)
     ks = key(seed, layer, expert, tag * 4 + PART_SCALE)
+    nblk = N * K // (16 if shape.fmt == FMT_NVFP4 else 32)
+    if shape.scale_table:
+        tab = np.asarray(shape.scale_table, dtype=np.uint8)
+        sc = tab[range_bytes(ks, nblk, 0, len(tab) - 1)].reshape(N, -1)
+    elif shape.fmt == FMT_NVFP4:
+        sc = range_bytes(ks, nblk, *NVFP4_SCALE_BYTES).reshape(N, K // 16)
+    else:
+        sc = range_bytes(ks, nblk, *MXFP4_SCALE_BYTES).reshape(N, K // 32)
     if shape.fmt == FMT_NVFP4:
-        sc = range_bytes(ks, N * K // 16, *NVFP4_SCALE_BYTES).reshape(N, K // 16)
         u = uniform(key(seed, layer, expert, tag * 4 + PART_GSCALE), 1)[0]
         g = np.float32(NVFP4_GSCALE * (0.9 + 0.2 * u))
         return {"codes": codes, "scales": sc, "gscale": float(g)}
-    sc = range_bytes(ks, N * K // 32, *MXFP4_SCALE_BYTES).reshape(N, K // 32)
     return {"codes": codes, "scales": sc}
 
 

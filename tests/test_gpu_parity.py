@@ -27,16 +27,20 @@ def _need_gpu():
     build.build()
 
 
-def _run(shape, seed, L, capacity, calls, flags=0, sample=None, max_tokens=0):
-    """calls: list of (layer, T, step). Returns the measured errors."""
-    from moe_harness import GpuStack, OracleStack, compare
+def _run(shape, seed, L, capacity, calls, flags=0, sample=None, max_tokens=0, cover=None):
+    """calls: list of (layer, T, step). sample: check outputs on that many evenly
+    spaced tokens; cover: on at least that many tokens that together select
+    every expert the call routes to. Returns the measured errors."""
+    from moe_harness import GpuStack, OracleStack, compare, oracle_workers
     g = GpuStack(shape, seed, L, capacity, flags, max_tokens=max_tokens)
-    o = OracleStack(shape, seed, L, capacity, prefetch=bool(flags & 1))
+    o = OracleStack(shape, seed, L, capacity, prefetch=bool(flags & 1), workers=oracle_workers() if cover else 0)
     errs = []
     try:
         for (layer, T, step) in calls:
             x = synth.hidden_states(shape, seed, layer, T, step)
             toks = None if sample is None or T <= sample else np.linspace(0, T - 1, sample).astype(int)
+            if cover and T > cover:
+                toks = f"cover:{cover}"
             gr = g.forward(layer, x)
             orr = o.forward(layer, x, toks)
             errs.append(compare(gr, orr))
@@ -189,27 +193,41 @@ def test_workload_decode_nvfp4_layer_subset():
 
 def test_workload_prefill_bf16_layer_subset():
     """prefill-40L-H2048-E256-k8-I512-bf16 at T=4096 on 2 layers with prefetch,
-    routing in full, outputs on 48 sampled tokens."""
+    routing in full, outputs on at least 256 tokens that together select every
+    expert the call routes to."""
     s = synth.PREFILL_BF16
-    _run(s, 0, 2, 256 + 256 + 8, [(0, 4096, 0), (1, 4096, 0)], flags=1, sample=48, max_tokens=4096)
+    _run(s, 0, 2, 256 + 256 + 8, [(0, 4096, 0), (1, 4096, 0)], flags=1, cover=256, max_tokens=4096)
 
 
 def test_workload_large_mxfp4_shared_layer_subset():
     """large-24L-H4096-E256+1-k8-I2048-mxfp4: decode T=1 and prefill T=2048 on
-    2 layers, outputs on sampled tokens."""
+    2 layers; prefill outputs on at least 256 tokens that together select every
+    expert the call routes to (and the shared expert on each of them)."""
     s = synth.LARGE_MXFP4
-    _run(s, 0, 2, 300, [(0, 1, 0), (1, 1, 0), (0, 2048, 1)], sample=6, max_tokens=2048)
+    _run(s, 0, 2, 300, [(0, 1, 0), (1, 1, 0), (0, 2048, 1)], cover=256, max_tokens=2048)
 
 
-def test_workload_stress_nvfp4_layer_subset():
-    """stress-16L-H6144-E160-k8-I2048-nvfp4: decode T=1 with Zipf s=1.1 and
-    step reuse (p=0.7) on 3 layers, pool of 10% of those layers' experts."""
+@pytest.mark.parametrize("frac", [0.05, 0.10, 0.25])
+def test_workload_stress_nvfp4_pool_sweep(frac):
+    """stress-16L-H6144-E160-k8-I2048-nvfp4: 24 decode steps of T=1 with Zipf
+    s=1.1 and step reuse (p=0.7) on 3 layers, pool of 5%, 10% or 25% of those
+    layers' experts (24, 48, 120 slots). Routing and the LRU sequence on every
+    call; outputs on every call of the first 8 steps."""
+    from moe_harness import GpuStack, OracleStack, compare
     s = synth.STRESS_NVFP4
     L = 3
-    cap = max(s.k, int(0.10 * s.E * L))
-    reuse = synth.reuse_flags(0, 12, 0.7)
-    calls, src = [], 0
-    for st in range(12):
-        src = src if reuse[st] else st
-        calls += [(l, 1, src) for l in range(L)]
-    _run(s, 0, L, cap, calls)
+    cap = max(s.k, int(frac * s.E * L + 1e-9))
+    reuse = synth.reuse_flags(0, 24, 0.7)
+    g = GpuStack(s, 0, L, cap)
+    o = OracleStack(s, 0, L, cap, prefetch=False, max_cached_experts=96)
+    try:
+        src = 0
+        for st in range(24):
+            src = src if reuse[st] else st
+            for l in range(L):
+                x = synth.hidden_states(s, 0, l, 1, src)
+                compare(g.forward(l, x), o.forward(l, x, None if st < 8 else []))
+        st_ = g.stats()
+        assert st_["misses"] > 0 and st_["hits"] > 0
+    finally:
+        g.close()

@@ -1,11 +1,15 @@
 """Pins for the oracle's expert FFN and layer combine: closed forms with
 identity-like experts in every weight format, and a dense fp64 numpy (einsum)
 re-computation on the tiny fp32 workload."""
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 FORMATS = [synth.FMT_FP32, synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4]
 
@@ -108,3 +112,19 @@ def test_layer_token_subset_matches_full():
     full = oracle.layer(shape, experts, w, x)
     part = oracle.layer(shape, experts, w, x, toks=[7, 2])
     assert np.array_equal(part["out"], full["out"][[7, 2]])
+
+
+def test_expert_major_evaluation_matches_layer_tokens():
+    """The test harness's expert-at-a-time evaluation (expert outputs in worker
+    processes, then the oracle's combine per token) gives the same bits as
+    the oracle's token-at-a-time layer output, shared expert included."""
+    import sys
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from moe_harness import OracleStack, cover_tokens
+    s = synth.Shape("em", L=1, E=16, k=4, H=256, I=128, fmt=synth.FMT_MXFP4, act=synth.ACT_BF16, shared=1)
+    x = synth.hidden_states(s, 3, 0, 24, 0)
+    a = OracleStack(s, 3, 1, 32, False).forward(0, x, np.arange(24))
+    b = OracleStack(s, 3, 1, 32, False, workers=2).forward(0, x, np.arange(24))
+    assert np.array_equal(a["out"], b["out"])
+    t = cover_tokens(a["topk_idx"], 5)
+    assert set(a["topk_idx"][t].ravel()) == set(a["topk_idx"].ravel()) and len(t) >= 5
