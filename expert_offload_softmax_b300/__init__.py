@@ -29,9 +29,11 @@ MOE_DECODE_MAX_T = 8
 MOE_CACHE_PREFETCH_NEXT_LAYER = 1
 MOE_CACHE_LOG_EVENTS = 2
 MOE_CACHE_SYNC_MISSES = 4
+MOE_CACHE_HOST_MISSES = 8
 
 # every symbol the header declares
-EXPORTS = ["moe_init", "moe_expert_bytes", "moe_repack_expert", "moe_load_expert", "moe_cache_config", "moe_layer_forward", "moe_sync",
+EXPORTS = ["moe_init", "moe_expert_bytes", "moe_repack_expert", "moe_load_expert", "moe_cache_config",
+           "moe_cache_resize", "moe_layer_forward", "moe_sync",
            "moe_stats", "moe_stats_reset", "moe_stats_events", "moe_debug_routing", "moe_debug_lru_table",
            "moe_last_error", "moe_destroy", "moe_timing_enable", "moe_timing", "moe_route_topk_noalloc"]
 MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 20
@@ -98,7 +100,8 @@ def load(path: str | None = None):
     lib.moe_expert_bytes.argtypes = [P(moe_model_desc), P(ctypes.c_size_t)]
     lib.moe_repack_expert.argtypes = [P(moe_model_desc), P(moe_expert_host), ctypes.c_void_p, ctypes.c_size_t]
     lib.moe_load_expert.argtypes = [vp, i32, i32, P(moe_expert_host)]
-    lib.moe_cache_config.argtypes = [vp, i32, u32]
+    lib.moe_cache_config.argtypes = [vp, i32, u32, vp, ctypes.c_size_t]
+    lib.moe_cache_resize.argtypes = [vp, i32, vp, ctypes.c_size_t]
     lib.moe_layer_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp]
     lib.moe_sync.argtypes = [vp]
     lib.moe_stats.argtypes = [vp, P(moe_stats_t)]
@@ -180,8 +183,15 @@ def moe_load_expert(h: int, layer: int, expert: int, w: dict) -> None:
     del kg, ku, kd
 
 
-def moe_cache_config(h: int, capacity_slots: int, flags: int = 0) -> None:
-    _check(h, load().moe_cache_config(h, capacity_slots, flags))
+def moe_cache_config(h: int, capacity_slots: int, flags: int = 0, pool_dev: int = 0, pool_bytes: int = 0) -> None:
+    """Safe point: (re)build an empty cache of capacity_slots slots. pool_dev:
+    optional caller-owned device buffer (address) of pool_bytes bytes."""
+    _check(h, load().moe_cache_config(h, capacity_slots, flags, pool_dev or None, pool_bytes))
+
+
+def moe_cache_resize(h: int, capacity_slots: int, pool_dev: int = 0, pool_bytes: int = 0) -> None:
+    """Safe point: resize the cache, keeping the most recently used experts."""
+    _check(h, load().moe_cache_resize(h, capacity_slots, pool_dev or None, pool_bytes))
 
 
 def moe_layer_forward(h: int, hidden: int, router_w: int, layer_id: int, T: int, out: int,

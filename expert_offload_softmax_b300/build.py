@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_b300.so")
-SOURCES = ["runtime.cu", "routing.cu", "experts.cu", "decode_fp4.cu", "prefill_umma.cu", "route_noalloc.cu"]
+SOURCES = ["runtime.cu", "routing.cu", "experts.cu", "decode_fused.cu", "prefill_umma.cu", "route_noalloc.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

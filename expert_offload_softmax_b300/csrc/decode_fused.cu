@@ -1,0 +1,1217 @@
+// Decode call of the routed MoE layer (T <= 8 tokens, FP4 expert weights) in
+// one cooperative launch: router logits, softmax / top-k / renormalisation,
+// the permutation by expert, the device LRU lookup of the expert cache, the
+// copy of missed experts from the pinned host banks into their pool slots,
+// gate/up + SwiGLU, and down + gate-weighted combine.
+//
+// Follows "FreeToken量子化：MoE推論のセットアップガイド" (freetoken.wiki,
+// architecture page, decode paragraph): an LRU over recently selected experts;
+// a hit runs on the GPU, a miss is copied into the cache over PCIe. Here the
+// copy is made by the kernel itself, reading the pinned host bank through its
+// mapped device view, so a call with misses needs no host round trip (with the
+// cache flag MOE_CACHE_HOST_MISSES the host's copy engines do it instead, and
+// the kernel waits for the release the host posts after them).
+//
+// At T <= 8 the layer is bound by streaming the active experts' packed
+// weights from HBM once; the arithmetic is tiny. Phases:
+//  P1  every CTA stages the token rows in shared memory; warps compute router
+//      logits (one warp per expert, in the fixed summation order) into global
+//      scratch; grid barrier.
+//  P2  every CTA computes the same top-k, permutation and expert plan from the
+//      logits and looks the experts up in the LRU table; CTA 0 alone updates
+//      the LRU (stamps, victims), publishes the slots of the misses and writes
+//      the call record the host reads for its statistics. With misses, all
+//      CTAs copy the missed blobs (host -> pool slot) in parallel; barrier.
+//  P3  warp 0 of each CTA streams 16-row weight tiles with cp.async.bulk into
+//      a ring of shared-memory stages (mbarriers); warps 1-8 consume them with
+//      mma.sync m16n8k16 (swap-AB: 16 weight rows x 8 token columns). Phase 1:
+//      h = gate * silu(W_gate x) * (W_up x); barrier (the producer keeps
+//      streaming phase-2 tiles across it); phase 2: out[t] = sum over experts
+//      of W_down h. Each tile's K range is split over the 8 consumer warps; the
+//      warp that finishes a tile last sums the 8 partials in warp order and
+//      writes the result, so the reduction order is fixed.
+//
+// Exact arithmetic of the operands. NVFP4: code (E2M1) and block scale (E4M3)
+// are both widened to f16 and multiplied there: the product has at most 6
+// significant bits and lies in [2^-10, 2688], so it is exact in f16; the fp32
+// per-tensor scale is applied after the dot product. MXFP4: the E8M0 scale is
+// applied in fp32 to each 32-element partial sum. Activations: each token row
+// is scaled by a power of two so that its largest |x| lies in [2^14, 2^15)
+// before rounding to f16 (exact for every element the f16 normal range holds),
+// and h rows likewise by their token's largest |h|; the power of two is undone
+// in fp32 after the dot product. So neither the bf16 range of the layer's
+// inputs nor that of h is narrowed to f16's.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "mma_common.cuh"
+#include "moe_internal.h"
+#include "route_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kConsumers = 8;
+constexpr int kWarps = kConsumers + 1;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStageGroups = 2 * kChunkGroups;  // K groups (16 rows x 128) per pipeline stage
+constexpr int kMaxStages = 12;
+constexpr int kMaxAssign = kDecodeMaxT * kMaxTopK;
+constexpr int kRedSlotBytes = kConsumers * 32 * 4 * 4;  // one tile's 8 partial accumulators
+constexpr int kSmemLimit = 220 * 1024;                  // dynamic bytes; a few KB static sit beside it
+constexpr int kLruCached = 4096;                        // pools up to this size cache stamps/owners in smem
+
+template <int FMT>
+struct Fp4Cfg {
+    static constexpr int kSbpg = FMT == FMT_NVFP4 ? 8 : 4;
+    static constexpr int kChunkBytes = kTileRows * kChunkGroups * (64 + kSbpg);
+    static constexpr int kStageBytes = 2 * kChunkBytes;
+};
+
+// per-CTA routing state (front of dynamic shared memory)
+struct DecRoute {
+    int32_t tk[kMaxAssign];       // expert of assignment a = t*k + j
+    float g[kMaxAssign];          // its gate
+    int32_t rank[kMaxAssign];     // its row: stable order by expert
+    int32_t uidx[kMaxAssign];     // active index of its expert
+    int32_t first[kMaxAssign];    // 1: the lowest assignment of its expert
+    int32_t members[kMaxAssign];  // ascending distinct experts
+    int32_t mslot[kMaxAssign];    // their pool slots (-1: miss, until the cache update assigns one)
+    int32_t hit[kMaxAssign];      // 1: the member was in the cache
+    int32_t missr[kMaxAssign];    // member index of the r-th miss
+    int32_t rowtok[kMaxAssign + kDecodeMaxT];  // token of h row r
+    float xsc[kDecodeMaxT], xun[kDecodeMaxT];  // activation power-of-two scale and its inverse
+    float hsc[kDecodeMaxT], hun[kDecodeMaxT];
+    unsigned int xmax[kDecodeMaxT], hmax[kDecodeMaxT];
+    int32_t red_cnt[kMaxStages];
+    int32_t nu, n_miss, status, ok;
+    unsigned long long t_copy0;
+};
+
+// dynamic shared memory carve-up, computed on the host
+struct DecGeom {
+    int nst;          // pipeline stages
+    int max_active;   // plan records
+    int act_bytes;    // token rows (phase 1) / h rows (phase 2) in smem; 0: read from global
+    int plan_off, ring_off, red_off, act_off, total;
+    int stage_x;      // 1: P1 stages the raw token rows at ring_off
+    int lru_trow_off, lru_keys_off, lru_cache_off;  // CTA 0's cache-lookup scratch (aliases the ring)
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+// suspends for up to ~20 us waiting for the phase of parity `parity`
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded by wait_ns; false on abort or timeout
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long wait_ns) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        if (mbar_test(b, parity)) return true;
+        if (*abort_flag) return false;
+        if (gtimer() - t0 > wait_ns) return false;
+    }
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar))
+        : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_add_acqrel_gpu(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory"); }
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// One arrival of this CTA at a grid-wide barrier (called by one thread after
+// the CTA has synchronised): arrivals are counted with an acquire-release add
+// that publishes the CTA's writes; the last arrival resets the count and bumps
+// the generation, which the others poll with acquire loads (bounded).
+__device__ bool grid_arrive_wait(const CallArgs& a, int G, int err_code) {
+    unsigned int* cnt = a.grid_bar;
+    unsigned int* gen = a.grid_bar + 1;
+    __threadfence();
+    const unsigned int my_gen = ld_acquire_gpu(gen);
+    const unsigned int prev = atom_add_acqrel_gpu(cnt, 1u);
+    if (prev == static_cast<unsigned int>(G) - 1u) {
+        st_relaxed_gpu(cnt, 0u);
+        red_add_release_gpu(gen, 1u);
+        return true;
+    }
+    const uint64_t t0 = gtimer();
+    while (ld_acquire_gpu(gen) == my_gen) {
+        if (gtimer() - t0 > a.wait_ns) {
+            atomicExch(a.dev_err, err_code);
+            return false;
+        }
+    }
+    return true;
+}
+
+// power of two p with max|v| * p in [2^14, 2^15) (1 for 0 or non-finite), and 1/p
+__device__ __forceinline__ void pow2_scale(unsigned int maxbits, float& sc, float& un) {
+    const int be = static_cast<int>((maxbits >> 23) & 0xFFu);
+    if (maxbits == 0u || be == 0xFF) {
+        sc = 1.0f;
+        un = 1.0f;
+        return;
+    }
+    int s = 141 - be;  // |v| < 2^(be - 126): |v| * 2^s < 2^15
+    s = s > 127 ? 127 : s;
+    sc = __uint_as_float(static_cast<unsigned int>(127 + s) << 23);
+    const int u = -s;  // >= -127
+    un = u >= -126 ? __uint_as_float(static_cast<unsigned int>(127 + u) << 23) : __uint_as_float(0x00400000u);
+}
+
+// f16 of v * sc, two at a time (round to nearest)
+__device__ __forceinline__ uint32_t f16x2_scaled(float lo, float hi, float sc) {
+    __half2 h = __floats2half2_rn(lo * sc, hi * sc);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// eight E4M3 bytes -> four f16x2 (bytes 2i, 2i+1 -> word i); exact
+__device__ __forceinline__ void e4m3x8_to_f16x2(uint2 v, uint32_t (&o)[4]) {
+    asm("{\n.reg .b16 l0, h0, l1, h1;\n"
+        "mov.b32 {l0, h0}, %4;\n"
+        "mov.b32 {l1, h1}, %5;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, l0;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, h0;\n"
+        "cvt.rn.f16x2.e4m3x2 %2, l1;\n"
+        "cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(v.x), "r"(v.y));
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// One 128-element K group of a staged 16-row chunk (ng groups) against one
+// 8-column B run: acc (rows g / g+8, columns 2q / 2q+1) += the group's dot
+// products. NVFP4 (scale folded into the f16 operand): accumulates in the MMA.
+// MXFP4: each 32-element block (two MMA steps) times its E8M0 scale, in fp32.
+template <int FMT>
+__device__ __forceinline__ void mma_group(const unsigned char* chunk, int ng, int w, int g, int q,
+                                          const uint32_t (&b)[16], float (&acc)[4]) {
+    constexpr int kSbpg = Fp4Cfg<FMT>::kSbpg;
+    const uint4 ra = lds128(chunk + fp4_code_off(ng, g, w, q));
+    const uint4 rb = lds128(chunk + fp4_code_off(ng, g + 8, w, q));
+    const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+    if constexpr (FMT == FMT_NVFP4) {
+        uint32_t fa[4], fb[4];
+        e4m3x8_to_f16x2(*reinterpret_cast<const uint2*>(chunk + fp4_scale_off(ng, kSbpg, g, w)), fa);
+        e4m3x8_to_f16x2(*reinterpret_cast<const uint2*>(chunk + fp4_scale_off(ng, kSbpg, g + 8, w)), fb);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            uint32_t oa[4], ob[4];
+            fp4x8_to_f16x2(wa[x], oa);
+            fp4x8_to_f16x2(wb[x], ob);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int s = 2 * x + h;  // MMA step; its 16 elements share one scale per row
+                const uint32_t sel = (s & 1) ? 0x3232u : 0x1010u;
+                const uint32_t sa = __byte_perm(fa[s >> 1], 0u, sel), sb = __byte_perm(fb[s >> 1], 0u, sel);
+                const uint32_t A[4] = {hmul2u(oa[2 * h], sa), hmul2u(ob[2 * h], sb), hmul2u(oa[2 * h + 1], sa),
+                                       hmul2u(ob[2 * h + 1], sb)};
+                mma_f16(acc, A, b[2 * s], b[2 * s + 1], acc);
+            }
+        }
+    } else {
+        const uint32_t va = *reinterpret_cast<const uint32_t*>(chunk + fp4_scale_off(ng, kSbpg, g, w));
+        const uint32_t vb = *reinterpret_cast<const uint32_t*>(chunk + fp4_scale_off(ng, kSbpg, g + 8, w));
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            uint32_t oa[4], ob[4];
+            fp4x8_to_f16x2(wa[x], oa);
+            fp4x8_to_f16x2(wb[x], ob);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int s = 2 * x + h;
+                const uint32_t A[4] = {oa[2 * h], ob[2 * h], oa[2 * h + 1], ob[2 * h + 1]};
+                mma_f16(d, A, b[2 * s], b[2 * s + 1], d);
+            }
+            const float sa = e8m0_to_f32((va >> (8 * x)) & 0xFFu), sb = e8m0_to_f32((vb >> (8 * x)) & 0xFFu);
+            acc[0] = __fmaf_rn(sa, d[0], acc[0]);
+            acc[1] = __fmaf_rn(sa, d[1], acc[1]);
+            acc[2] = __fmaf_rn(sb, d[2], acc[2]);
+            acc[3] = __fmaf_rn(sb, d[3], acc[3]);
+        }
+    }
+}
+
+// B run of one column for K group j: 32 f16 at device positions
+// [128 j + 32 q, +32). From the staged rows (pitch bytes apart), or, when the
+// rows did not fit in shared memory, converted here from global memory: token
+// rows (x, canonical element order) or h rows (bf16, device order).
+__device__ __forceinline__ void load_b_smem(const unsigned char* rows, int pitch, int r, int j, int q,
+                                            uint32_t (&bq)[16]) {
+    if (r < 0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bq[i] = 0u;
+        return;
+    }
+    const unsigned char* p = rows + r * pitch + j * 256 + 64 * q;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 x = lds128(p + 16 * v);
+        bq[4 * v] = x.x; bq[4 * v + 1] = x.y; bq[4 * v + 2] = x.z; bq[4 * v + 3] = x.w;
+    }
+}
+
+template <int ACT>
+__device__ __forceinline__ void load_b_xglobal(const void* hidden, int H, int t, int j, int q, float sc,
+                                               uint32_t (&bq)[16]) {
+    if (t < 0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bq[i] = 0u;
+        return;
+    }
+    // device position 32q + 4s + i of group j holds element 16s + 4q + i
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const size_t e0 = static_cast<size_t>(t) * H + 128 * j + 16 * s + 4 * q;
+        float v[4];
+        if constexpr (ACT == ACT_BF16) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(hidden) + e0));
+            v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+            v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(hidden) + e0));
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        }
+        bq[2 * s] = f16x2_scaled(v[0], v[1], sc);
+        bq[2 * s + 1] = f16x2_scaled(v[2], v[3], sc);
+    }
+}
+
+__device__ __forceinline__ void load_b_hglobal(const uint16_t* hbuf, int I, int r, int j, int q, float sc,
+                                               uint32_t (&bq)[16]) {
+    if (r < 0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bq[i] = 0u;
+        return;
+    }
+    const uint4* p = reinterpret_cast<const uint4*>(hbuf + static_cast<size_t>(r) * I + j * 128 + 32 * q);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 x = __ldcg(p + v);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            bq[4 * v + i] = f16x2_scaled(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u), sc);
+    }
+}
+
+// A pipeline stage: up to 16 K groups of 16 weight rows, made of one or more
+// contiguous pieces of the blobs (one cp.async.bulk each).
+struct Stage {
+    const uint8_t* src[kStageGroups];
+    uint32_t bytes[kStageGroups];
+    int npieces;
+    int tile_end;  // 1: last stage of its output tile
+};
+
+// The stage sequence of one CTA, identical for its producer and consumers.
+//  phase 1: gate/up tiles i = b1, b1 + G1, ... (active expert u = i / (I/8),
+//           unit tile i mod (I/8)); a stage = up to two 8-group chunks.
+//  phase 2: down row tiles rt = b, b + G, ...; for each, every active expert's
+//           16-row tile: up to two chunks of one expert per stage when I >= 1024,
+//           else the whole tiles of several experts (16 groups at most).
+template <int FMT>
+struct StageSeq {
+    const CallArgs* a;
+    const DecExpert* plan;
+    int na, b1, G1, b, G;
+    int UT, G1k, nch1, ns1, n1, my1;  // phase 1
+    int G2k, nch2, nsu, epp, ns2, n2, my2;
+
+    __device__ void init(const CallArgs& ca, const DecExpert* pl, int na_, int blk, int grid) {
+        a = &ca;
+        plan = pl;
+        na = na_;
+        b = blk;
+        G = grid;
+        G1 = grid > 1 ? grid - 1 : 1;
+        b1 = grid > 1 ? blk - 1 : blk;
+        UT = ca.I / 8;
+        G1k = ca.H / kGroupK;
+        nch1 = (G1k + kChunkGroups - 1) / kChunkGroups;
+        ns1 = (nch1 + 1) / 2;
+        n1 = na * UT;
+        my1 = (b1 >= 0 && b1 < n1) ? (n1 - 1 - b1) / G1 + 1 : 0;
+        G2k = ca.I / kGroupK;
+        nch2 = (G2k + kChunkGroups - 1) / kChunkGroups;
+        if (G2k >= kChunkGroups) {
+            nsu = (nch2 + 1) / 2;
+            epp = 1;
+            ns2 = na * nsu;
+        } else {
+            nsu = 1;
+            epp = kStageGroups / G2k;
+            ns2 = (na + epp - 1) / epp;
+        }
+        n2 = ca.H / kTileRows;
+        my2 = b < n2 ? (n2 - 1 - b) / G + 1 : 0;
+    }
+    __device__ int count1() const { return my1 * ns1; }
+    __device__ int count2() const { return my2 * ns2; }
+
+    // phase 1, stage f of this CTA: chunks [c0, c0 + nc) of tile (u, ut)
+    __device__ void where1(int f, int& u, int& ut, int& c0, int& nc) const {
+        const int i = b1 + (f / ns1) * G1;
+        u = i / UT;
+        ut = i % UT;
+        c0 = 2 * (f % ns1);
+        nc = min(2, nch1 - c0);
+    }
+    __device__ void stage1(int f, Stage& st) const {
+        int u, ut, c0, nc;
+        where1(f, u, ut, c0, nc);
+        const uint8_t* tile = plan[u].ptr + a->lay.gu + static_cast<size_t>(ut) * a->lay.gu_tile;
+        uint32_t bytes = 0;
+        for (int c = c0; c < c0 + nc; ++c)
+            bytes += static_cast<uint32_t>(kTileRows) * fp4_chunk_groups(G1k, c) * (64 + Fp4Cfg<FMT>::kSbpg);
+        st.src[0] = tile + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+        st.bytes[0] = bytes;
+        st.npieces = 1;
+        st.tile_end = (f % ns1) == ns1 - 1;
+    }
+    // phase 2, stage f: row tile rt; experts [u0, u0 + nu); chunks [c0, c0 + nc) (one expert) or whole tiles
+    __device__ void where2(int f, int& rt, int& u0, int& nu_, int& c0, int& nc) const {
+        rt = b + (f / ns2) * G;
+        const int k = f % ns2;
+        if (epp == 1) {
+            u0 = k / nsu;
+            nu_ = 1;
+            c0 = 2 * (k % nsu);
+            nc = min(2, nch2 - c0);
+        } else {
+            u0 = k * epp;
+            nu_ = min(epp, na - u0);
+            c0 = 0;
+            nc = 1;
+        }
+    }
+    __device__ void stage2(int f, Stage& st) const {
+        int rt, u0, nu_, c0, nc;
+        where2(f, rt, u0, nu_, c0, nc);
+        const size_t toff = a->lay.d + static_cast<size_t>(rt) * a->lay.d_tile;
+        if (epp == 1) {
+            uint32_t bytes = 0;
+            for (int c = c0; c < c0 + nc; ++c)
+                bytes += static_cast<uint32_t>(kTileRows) * fp4_chunk_groups(G2k, c) * (64 + Fp4Cfg<FMT>::kSbpg);
+            st.src[0] = plan[u0].ptr + toff + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+            st.bytes[0] = bytes;
+            st.npieces = 1;
+        } else {
+            const uint32_t pb = static_cast<uint32_t>(kTileRows) * G2k * (64 + Fp4Cfg<FMT>::kSbpg);
+            for (int p = 0; p < nu_; ++p) {
+                st.src[p] = plan[u0 + p].ptr + toff;
+                st.bytes[p] = pb;
+            }
+            st.npieces = nu_;
+        }
+        st.tile_end = (f % ns2) == ns2 - 1;
+    }
+};
+
+template <int FMT, int ACT>
+__global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo) {
+    using C = Fp4Cfg<FMT>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
+    __shared__ int s_abort;
+
+    DecRoute& R = *reinterpret_cast<DecRoute*>(dsm);
+    DecExpert* plan = reinterpret_cast<DecExpert*>(dsm + geo.plan_off);
+    unsigned char* ring = dsm + geo.ring_off;
+    float* red = reinterpret_cast<float*>(dsm + geo.red_off);
+    unsigned char* act = dsm + geo.act_off;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I, ns = a.n_shared;
+    const int n = T * k;
+    const int nst = geo.nst;
+    const size_t esz = ACT == ACT_BF16 ? 2 : 4;
+    const size_t B = a.lay.bytes;
+    volatile int* abort_flag = &s_abort;
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumers);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < kMaxStages) R.red_cnt[tid] = 0;
+    if (tid < kDecodeMaxT) {
+        R.xmax[tid] = 0u;
+        R.hmax[tid] = 0u;
+    }
+    // programmatic dependent launch: everything the previous call wrote is
+    // visible after this; the next call's CTAs may be scheduled as ours exit
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    // ---------------------------------------------------------------- P1: logits
+    {
+        const unsigned char* xsrc = reinterpret_cast<const unsigned char*>(a.hidden);
+        if (geo.stage_x) {
+            const size_t n16 = static_cast<size_t>(T) * H * esz / 16;
+            for (size_t i = tid; i < n16; i += kThreads)
+                reinterpret_cast<uint4*>(ring)[i] = __ldg(reinterpret_cast<const uint4*>(xsrc) + i);
+            xsrc = ring;
+        }
+        if (b == 0 && tid < kDecodeMaxT) a.hmax[tid] = 0u;  // read after the phase-1 barrier only
+        __syncthreads();
+        // row maxima of the token rows (every CTA, from its own copy)
+        {
+            for (int t = 0; t < T; ++t) {
+                float m = 0.f;
+                for (int i = tid; i < H; i += kThreads) {
+                    const size_t o = static_cast<size_t>(t) * H + i;
+                    const float v = ACT == ACT_BF16
+                                        ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(xsrc)[o]) << 16)
+                                        : reinterpret_cast<const float*>(xsrc)[o];
+                    m = fmaxf(m, fabsf(v));
+                }
+                const unsigned int mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+                if (lane == 0 && mb) atomicMax(&R.xmax[t], mb);
+            }
+        }
+        // router logits: warp w of CTA b takes experts b*9 + w, + 9G, ...
+        for (int e = b * kWarps + warp; e < E; e += G * kWarps) {
+            float acc[kDecodeMaxT];
+#pragma unroll
+            for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
+            const int nchunk = H / 8;
+            for (int cb = lane; cb < nchunk; cb += 32 * 4) {
+                float wv[4][8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cb + 32 * i;
+                    if (c < nchunk) {
+                        const size_t o = static_cast<size_t>(e) * H + 8 * c;
+                        if constexpr (ACT == ACT_BF16) {
+                            const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.router_w) + o));
+                            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                wv[i][2 * jj] = __uint_as_float(wd[jj] << 16);
+                                wv[i][2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
+                            }
+                        } else {
+                            const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.router_w) + o);
+                            const float4 p0 = __ldg(f), p1 = __ldg(f + 1);
+                            wv[i][0] = p0.x; wv[i][1] = p0.y; wv[i][2] = p0.z; wv[i][3] = p0.w;
+                            wv[i][4] = p1.x; wv[i][5] = p1.y; wv[i][6] = p1.z; wv[i][7] = p1.w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cb + 32 * i;
+                    if (c >= nchunk) break;
+#pragma unroll
+                    for (int t = 0; t < kDecodeMaxT; ++t) {
+                        if (t < T) {
+                            const size_t o = static_cast<size_t>(t) * H + 8 * c;
+                            float xv[8];
+                            if constexpr (ACT == ACT_BF16) {
+                                const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(xsrc) + o);
+                                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                                for (int jj = 0; jj < 4; ++jj) {
+                                    xv[2 * jj] = __uint_as_float(wd[jj] << 16);
+                                    xv[2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
+                                }
+                            } else {
+                                const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xsrc) + o);
+                                const float4 p0 = f[0], p1 = f[1];
+                                xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
+                                xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
+                            }
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) acc[t] = __fmaf_rn(xv[jj], wv[i][jj], acc[t]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kDecodeMaxT; ++t) {
+                float v = acc[t];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if (lane == 0 && t < T) a.logits[static_cast<size_t>(t) * E + e] = v;
+            }
+        }
+        __syncthreads();
+        // activation scales; token rows -> f16 device order in smem (CTAs with phase-1 work)
+        if (tid < kDecodeMaxT) pow2_scale(R.xmax[tid], R.xsc[tid], R.xun[tid]);
+        __syncthreads();
+        if (geo.act_bytes && b != 0) {
+            const int xp = H * 2 + 16;
+            const int h4 = H / 4;
+            for (int idx = tid; idx < T * h4; idx += kThreads) {
+                const int t = idx / h4;
+                const int p = 4 * (idx % h4);  // device position
+                const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
+                const size_t src = static_cast<size_t>(t) * H + 128 * j + 16 * s + 4 * q;
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v[i] = ACT == ACT_BF16
+                               ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(xsrc)[src + i]) << 16)
+                               : reinterpret_cast<const float*>(xsrc)[src + i];
+                uint2 o;
+                o.x = f16x2_scaled(v[0], v[1], R.xsc[t]);
+                o.y = f16x2_scaled(v[2], v[3], R.xsc[t]);
+                *reinterpret_cast<uint2*>(act + t * xp + 2 * p) = o;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) R.ok = grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+        __syncthreads();
+    }
+    if (!R.ok) return;  // every CTA gives up the same way; nothing is in flight
+
+    // ---------------------------------------------------------------- P2: routing (every CTA)
+    if (warp < T) {
+        int sel;
+        float gv;
+        warp_topk<true>(a.logits + static_cast<size_t>(warp) * E, E, k, lane, sel, gv);
+        if (lane < k) {
+            R.tk[warp * k + lane] = sel;
+            R.g[warp * k + lane] = gv;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+        const int e = R.tk[i];
+        int rk = 0, first = 1;
+        for (int j2 = 0; j2 < n; ++j2) {
+            const int f = R.tk[j2];
+            rk += (f < e) || (f == e && j2 < i);
+            first &= !(f == e && j2 < i);
+        }
+        R.rank[i] = rk;
+        R.first[i] = first;
+        R.rowtok[rk] = i / k;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+        const int e = R.tk[i];
+        int u = 0;
+        for (int j2 = 0; j2 < n; ++j2) u += R.first[j2] && R.tk[j2] < e;
+        R.uidx[i] = u;
+        if (R.first[i]) R.members[u] = e;
+    }
+    if (tid == 0) {
+        int nu = 0;
+        for (int i = 0; i < n; ++i) nu += R.first[i];
+        R.nu = nu;
+        R.status = nu > a.S ? -4 : 0;  // MOE_ERR_CAPACITY: the call leaves the cache as it was
+    }
+    __syncthreads();
+    const int nu = R.nu;
+    const int na = nu + ns;
+    for (int u = tid; u < na; u += kThreads) {
+        DecExpert& d = plan[u];
+        for (int t = 0; t < kDecodeMaxT; ++t) {
+            d.tok[t] = -1;
+            d.hrow[t] = -1;
+            d.gate[t] = 0.f;
+        }
+        d.cnt = 0;
+        if (u < nu) {
+            const int s = __ldcg(a.table + static_cast<size_t>(a.layer) * E + R.members[u]);
+            R.mslot[u] = s;
+            R.hit[u] = s >= 0 ? 1 : 0;
+            d.ptr = s >= 0 ? a.pool + static_cast<size_t>(s) * B : nullptr;
+        } else {
+            const int sidx = u - nu;
+            d.ptr = a.shared_base + static_cast<size_t>(sidx) * B;
+            d.row0 = n + sidx * T;
+            d.cnt = T;
+            for (int t = 0; t < T; ++t) {
+                d.tok[t] = t;
+                d.hrow[t] = n + sidx * T + t;
+                d.gate[t] = 1.0f;
+            }
+        }
+    }
+    for (int i = tid; i < ns * T; i += kThreads) R.rowtok[n + i] = i % T;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads)
+        if (R.first[i]) plan[R.uidx[i]].row0 = R.rank[i];
+    if (tid == 0) {
+        int r = 0;
+        for (int p = 0; p < nu; ++p)
+            if (!R.hit[p]) R.missr[r++] = p;
+        R.n_miss = r;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+        DecExpert& d = plan[R.uidx[i]];
+        const int t = i / k, nn = R.rank[i] - d.row0;
+        d.tok[nn] = t;
+        d.gate[nn] = R.g[i];
+        d.hrow[t] = R.rank[i];
+        atomicAdd(&d.cnt, 1);
+    }
+    __syncthreads();
+    const int n_miss = R.n_miss;
+    const bool capacity_err = R.status != 0;
+
+    // ---------------------------------------------------------------- P2b: CTA 0 updates the cache
+    CallInfo* info = a.info;
+    auto write_record = [&](int m, unsigned long long copy_ns) {
+        // the call record the host reads (statistics, event log); written last: done
+        for (int p = tid; p < nu; p += kThreads) {
+            info->ev_layer[p] = a.layer;
+            info->ev_expert[p] = R.members[p];
+            info->ev_hit[p] = R.hit[p];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            info->n_uniq = nu;
+            info->n_hit = capacity_err ? 0 : nu - m;
+            info->n_miss = capacity_err ? 0 : m;
+            info->n_pf = info->n_pf_hit = info->n_pf_miss = 0;
+            info->n_events = capacity_err ? 0 : nu;
+            info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
+            info->status = capacity_err ? -4 : 0;
+            info->device_copied = a.device_misses;
+            info->copy_ns = copy_ns;
+            __threadfence_system();
+            info->done = a.seq;
+        }
+    };
+    if (b == 0) {
+        // routing results for moe_debug_routing
+        for (int i = tid; i < n; i += kThreads) {
+            a.topk[i] = R.tk[i];
+            a.gates[i] = R.g[i];
+            a.perm[R.rank[i]] = i;
+            a.inv_perm[i] = R.rank[i];
+        }
+        for (int e = tid; e < E; e += kThreads) a.counts[e] = 0;
+        __syncthreads();
+        for (int u = tid; u < nu; u += kThreads) {
+            a.counts[R.members[u]] = plan[u].cnt;
+            a.act_expert[u] = R.members[u];
+        }
+        if (tid == 0) *a.n_uniq = nu;
+        if (!capacity_err) {
+            // the LRU batch (scratch over the ring: no stage is in use yet)
+            LruShared& sm = *reinterpret_cast<LruShared*>(ring);
+            int32_t* trow = reinterpret_cast<int32_t*>(dsm + geo.lru_trow_off);
+            unsigned long long* keys = reinterpret_cast<unsigned long long*>(dsm + geo.lru_keys_off);
+            const bool cached = geo.lru_cache_off > 0;
+            unsigned long long* st_s = cached ? reinterpret_cast<unsigned long long*>(dsm + geo.lru_cache_off) : nullptr;
+            int32_t* own_s = cached ? reinterpret_cast<int32_t*>(st_s + a.S) : nullptr;
+            for (int e = tid; e < E; e += kThreads) trow[e] = __ldcg(a.table + static_cast<size_t>(a.layer) * E + e);
+            if (cached)
+                for (int s = tid; s < a.S; s += kThreads) {
+                    st_s[s] = __ldcg(a.stamp + s);
+                    own_s[s] = __ldcg(a.owner + s);
+                }
+            if (tid == 0) sm.clock = __ldcg(a.clock);
+            __syncthreads();
+            LruView lv;
+            lv.a = &a;
+            lv.trow0 = trow;
+            lv.trow1 = nullptr;
+            lv.st_s = st_s;
+            lv.own_s = own_s;
+            const int m = lru_batch(a, lv, sm, keys, a.layer, R.members, nu, nullptr, 0, 0);
+            // m == n_miss: the members that missed are those whose table entry was -1
+            for (int r = tid; r < m; r += kThreads) {
+                const int p = sm.miss_p[r];
+                a.pub->slot[r] = sm.member_slot[p];
+                info->miss_layer[r] = a.layer;
+                info->miss_expert[r] = R.members[p];
+                info->miss_slot[r] = sm.member_slot[p];
+            }
+            for (int p = tid; p < nu; p += kThreads) {
+                info->ev_slot[p] = sm.member_slot[p];
+                info->ev_evicted[p] = sm.member_old[p];
+                info->ev_prefetch[p] = 0;
+            }
+            __syncthreads();
+            if (tid == 0 && m > 0) {
+                __threadfence();
+                st_release_gpu64(&a.pub->seq, a.seq);
+            }
+            if (!(m > 0 && a.device_misses)) write_record(m, 0ull);
+        } else {
+            write_record(0, 0ull);
+        }
+        __syncthreads();
+    }
+    if (capacity_err) return;
+
+    // ---------------------------------------------------------------- P2c: misses
+    if (n_miss > 0) {
+        if (tid == 0) {
+            bool ok = true;
+            if (!a.device_misses) ok = wait_ready(a);  // the host's copies have landed
+            if (ok) {
+                const uint64_t t0 = gtimer();
+                while (ld_acquire_gpu64(&a.pub->seq) < a.seq) {
+                    if (gtimer() - t0 > a.wait_ns) {
+                        atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_READY);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            R.ok = ok ? 1 : 0;
+            R.t_copy0 = gtimer();
+        }
+        __syncthreads();
+        if (!R.ok) return;
+        for (int r = tid; r < n_miss; r += kThreads) {
+            const int p = R.missr[r];
+            const int s = __ldcg(&a.pub->slot[r]);
+            R.mslot[p] = s;
+            plan[p].ptr = a.pool + static_cast<size_t>(s) * B;
+        }
+        __syncthreads();
+        if (a.device_misses) {
+            // copy the missed blobs: CTA b takes a contiguous share of the 16-byte vectors
+            const size_t per_blob = B / 16;
+            const size_t total = per_blob * n_miss;
+            const size_t share = (total + G - 1) / G;
+            const size_t v0 = share * b, v1 = min(total, v0 + share);
+            const uint8_t* bank = a.banks[a.layer];
+            constexpr int kU = 4;
+            for (size_t v = v0 + tid; v < v1; v += static_cast<size_t>(kThreads) * kU) {
+                uint4 x[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const size_t vv = v + static_cast<size_t>(u) * kThreads;
+                    if (vv < v1) {
+                        const size_t r = vv / per_blob, off = vv % per_blob;
+                        const int e = R.members[R.missr[r]];
+                        x[u] = __ldcs(reinterpret_cast<const uint4*>(bank + static_cast<size_t>(e) * B) + off);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const size_t vv = v + static_cast<size_t>(u) * kThreads;
+                    if (vv < v1) {
+                        const size_t r = vv / per_blob, off = vv % per_blob;
+                        reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.pool) + static_cast<size_t>(R.mslot[R.missr[r]]) * B)[off] = x[u];
+                    }
+                }
+            }
+            // the bulk copies (async proxy) of every CTA read these bytes next
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncthreads();
+            if (tid == 0) R.ok = grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_PRODUCER) ? 1 : 0;
+            __syncthreads();
+            if (!R.ok) return;
+            if (b == 0) {
+                const unsigned long long dt = gtimer() - R.t_copy0;
+                write_record(n_miss, dt);
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---------------------------------------------------------------- P3: experts
+    StageSeq<FMT> seq;
+    seq.init(a, plan, na, b, G);
+    const int nf1 = seq.count1(), nf2 = seq.count2();
+    const int xp = H * 2 + 16, hp = I * 2 + 16;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued[kMaxStages];
+        for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+        bool ok = true;
+        Stage st;
+        for (int f = 0; f < nf1 + nf2 && ok; ++f) {
+            if (f < nf1) seq.stage1(f, st);
+            else seq.stage2(f - nf1, st);
+            int got = 1;
+            if (lane == 0) {
+                got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns) && !*abort_flag;
+                if (got) {
+                    uint32_t tot = 0;
+                    for (int p = 0; p < st.npieces; ++p) tot += st.bytes[p];
+                    mbar_expect_tx(&full[stage], tot);
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            if (lane < st.npieces) {
+                uint32_t off = 0;
+                for (int p = 0; p < lane; ++p) off += st.bytes[p];
+                bulk_g2s(ring + stage * C::kStageBytes + off, st.src[lane], st.bytes[lane], &full[stage]);
+            }
+            issued[stage] = static_cast<int>(phase);
+            if (++stage == nst) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok && lane == 0 && !*abort_flag) {
+            atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_PRODUCER);
+            *abort_flag = 1;
+        }
+        // every copy this warp issued must land before the CTA may exit
+        if (lane == 0)
+            for (int s = 0; s < nst; ++s)
+                if (issued[s] >= 0) {
+                    const uint64_t t0 = gtimer();
+                    while (!mbar_test(&full[s], static_cast<uint32_t>(issued[s])) && gtimer() - t0 < a.wait_ns) {
+                    }
+                }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- consumers
+        const int w = warp - 1, ct = tid - 32;
+        const int g = lane >> 2, q = lane & 3;
+        // NVFP4 per-tensor scales live in the blobs
+        for (int u = ct; u < na; u += 32 * kConsumers) {
+            if constexpr (FMT == FMT_NVFP4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(plan[u].ptr + a.lay.gsc));  // may be this call's copy
+                plan[u].gs[0] = v.x; plan[u].gs[1] = v.y; plan[u].gs[2] = v.z;
+            } else {
+                plan[u].gs[0] = plan[u].gs[1] = plan[u].gs[2] = 1.0f;
+            }
+        }
+        consumer_sync();
+        const uint16_t* hb = reinterpret_cast<const uint16_t*>(a.hbuf);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool dead = false;
+        auto wait_full = [&]() -> const unsigned char* {
+            if (!dead && !mbar_wait(&full[stage], phase, abort_flag, a.wait_ns)) {
+                dead = true;
+                atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            return ring + stage * C::kStageBytes;
+        };
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == nst) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        // this warp's partial of a finished tile into the stage's slot; true for the
+        // warp that arrives last (it then holds the tile's sum in v, in warp order)
+        auto tile_reduce = [&](const float (&acc)[4], float (&v)[4]) -> bool {
+            float* slot = red + stage * (kConsumers * 32 * 4);
+            *reinterpret_cast<float4*>(slot + (w * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            __threadfence_block();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = atomicAdd(&R.red_cnt[stage], 1) == kConsumers - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last) return false;
+            __threadfence_block();
+            v[0] = v[1] = v[2] = v[3] = 0.f;
+#pragma unroll
+            for (int y = 0; y < kConsumers; ++y) {
+                const float4 p = *reinterpret_cast<const float4*>(slot + (y * 32 + lane) * 4);
+                v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+            }
+            if (lane == 0) R.red_cnt[stage] = 0;
+            return true;
+        };
+        // ---------------- phase 1: gate/up + SwiGLU
+        {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int f = 0; f < nf1; ++f) {
+                int u, ut, c0, nc;
+                seq.where1(f, u, ut, c0, nc);
+                const DecExpert& m = plan[u];
+                const int tok = m.tok[g];
+                const unsigned char* st = wait_full();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c = c0 + half;
+                    if (half < nc) {
+                        const int ng = fp4_chunk_groups(seq.G1k, c);
+                        if (w < ng && !dead) {
+                            const int j = c * kChunkGroups + w;
+                            uint32_t bq[16];
+                            if (geo.act_bytes) load_b_smem(act, xp, tok, j, q, bq);
+                            else load_b_xglobal<ACT>(a.hidden, H, tok, j, q, tok >= 0 ? R.xsc[tok] : 1.f, bq);
+                            mma_group<FMT>(st + half * C::kChunkBytes, ng, w, g, q, bq, acc);
+                        }
+                    }
+                }
+                if ((f % seq.ns1) == seq.ns1 - 1) {
+                    float v[4];
+                    if (tile_reduce(acc, v)) {
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int nn = 2 * q + h2;
+                            float hv = 0.f;
+                            if (nn < m.cnt) {
+                                const int t = m.tok[nn];
+                                const int r = m.row0 + nn;
+                                const float gate = v[h2] * m.gs[0] * R.xun[t], up = v[2 + h2] * m.gs[1] * R.xun[t];
+                                const float av = a.mode == 1 ? gate : silu(gate);
+                                hv = av * up * m.gate[nn];
+                                reinterpret_cast<__nv_bfloat16*>(a.hbuf)[static_cast<size_t>(r) * I + dpos(ut * 8 + g)] =
+                                    __float2bfloat16_rn(hv);
+                                atomicMax(&R.hmax[t], __float_as_uint(fabsf(hv)));
+                            }
+                        }
+                    }
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                }
+                release();
+            }
+        }
+        // ---------------- barrier: every h row of the call is written
+        consumer_sync();
+        if (ct < T && R.hmax[ct]) atomicMax(&a.hmax[ct], R.hmax[ct]);
+        consumer_sync();
+        if (ct == 0) R.ok = (!*abort_flag && grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_EPILOGUE)) ? 1 : 0;
+        consumer_sync();
+        if (!R.ok) *abort_flag = 1;
+        if (ct < T) pow2_scale(__ldcg(&a.hmax[ct]), R.hsc[ct], R.hun[ct]);
+        consumer_sync();
+        // ---------------- phase 2: down projection + combine
+        if (nf2 > 0) {
+            const int hrows = n + ns * T;
+            if (geo.act_bytes) {
+                // every h row of the call into shared memory as f16, scaled per token
+                const int per_row = I / 8;
+                for (int i = ct; i < hrows * per_row; i += 32 * kConsumers) {
+                    const int r = i / per_row, c8 = i % per_row;
+                    const uint4 x = __ldcg(reinterpret_cast<const uint4*>(hb + static_cast<size_t>(r) * I) + c8);
+                    const float sc = R.hsc[R.rowtok[r]];
+                    const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+                    uint4 o;
+                    o.x = f16x2_scaled(__uint_as_float(wv[0] << 16), __uint_as_float(wv[0] & 0xFFFF0000u), sc);
+                    o.y = f16x2_scaled(__uint_as_float(wv[1] << 16), __uint_as_float(wv[1] & 0xFFFF0000u), sc);
+                    o.z = f16x2_scaled(__uint_as_float(wv[2] << 16), __uint_as_float(wv[2] & 0xFFFF0000u), sc);
+                    o.w = f16x2_scaled(__uint_as_float(wv[3] << 16), __uint_as_float(wv[3] & 0xFFFF0000u), sc);
+                    *reinterpret_cast<uint4*>(act + r * hp + 16 * c8) = o;
+                }
+                consumer_sync();
+            }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int f = 0; f < nf2; ++f) {
+                int rt, u0, nu_, c0, nc;
+                seq.where2(f, rt, u0, nu_, c0, nc);
+                const unsigned char* st = wait_full();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int gs = w + kConsumers * half;  // group slot of this stage
+                    int u, c, ww, ng, off;
+                    if (seq.epp == 1) {
+                        u = u0;
+                        c = c0 + half;
+                        ww = w;
+                        ng = c < c0 + nc ? fp4_chunk_groups(seq.G2k, c) : 0;
+                        off = half * C::kChunkBytes;
+                    } else {
+                        const int p = gs / seq.G2k;
+                        u = u0 + p;
+                        c = 0;
+                        ww = gs % seq.G2k;
+                        ng = p < nu_ ? seq.G2k : 0;
+                        off = p * kTileRows * seq.G2k * (64 + C::kSbpg);
+                    }
+                    if (ww < ng && !dead) {
+                        const int hr = plan[u].hrow[g];
+                        const int j = c * kChunkGroups + ww;
+                        uint32_t bq[16];
+                        if (geo.act_bytes) load_b_smem(act, hp, hr, j, q, bq);
+                        else load_b_hglobal(hb, I, hr, j, q, R.hsc[g < T ? g : 0], bq);
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_group<FMT>(st + off, ng, ww, g, q, bq, d);
+                        const float gsd = plan[u].gs[2];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) acc[x] = __fmaf_rn(gsd, d[x], acc[x]);
+                    }
+                }
+                if (seq.count2() && ((f % seq.ns2) == seq.ns2 - 1)) {
+                    float v[4];
+                    if (tile_reduce(acc, v)) {
+                        const int r0 = rt * kTileRows;
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int t = 2 * q + h2;
+                            if (t < T) {
+#pragma unroll
+                                for (int rr = 0; rr < 2; ++rr) {
+                                    const size_t o = static_cast<size_t>(t) * H + r0 + g + 8 * rr;
+                                    const float x = v[2 * rr + h2] * R.hun[t];
+                                    if constexpr (ACT == ACT_BF16)
+                                        reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(x);
+                                    else
+                                        reinterpret_cast<float*>(a.out)[o] = x;
+                                }
+                            }
+                        }
+                    }
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                }
+                release();
+            }
+        }
+    }
+    __syncthreads();
+}
+
+template <int FMT>
+size_t lru_need(const CallArgs& a, int* trow_off, int* keys_off, int* cache_off, int base) {
+    size_t o = base + (sizeof(LruShared) + 127) / 128 * 128;
+    *trow_off = static_cast<int>(o);
+    o += (static_cast<size_t>(a.E) * 4 + 127) / 128 * 128;
+    *keys_off = static_cast<int>(o);
+    size_t P = 1;
+    while (P < static_cast<size_t>(a.S)) P <<= 1;
+    o += P * 8;
+    if (a.S <= kLruCached) {
+        *cache_off = static_cast<int>(o);
+        o += static_cast<size_t>(a.S) * 12;
+    } else {
+        *cache_off = 0;
+    }
+    return o;
+}
+
+template <int FMT>
+bool geometry(const CallArgs& a, DecGeom& g) {
+    const int T = a.T, H = a.H, I = a.I, k = a.k, ns = a.n_shared;
+    const size_t esz = a.act == ACT_BF16 ? 2 : 4;
+    g.max_active = std::min(a.E, T * k) + ns;
+    size_t o = (sizeof(DecRoute) + 127) / 128 * 128;
+    g.plan_off = static_cast<int>(o);
+    o += static_cast<size_t>(g.max_active) * sizeof(DecExpert);
+    o = (o + 127) / 128 * 128;
+    g.ring_off = static_cast<int>(o);
+    const size_t fixed = o;
+    const size_t per_stage = Fp4Cfg<FMT>::kStageBytes + kRedSlotBytes;
+    const size_t act_need = std::max(static_cast<size_t>(T) * (H * 2 + 16),
+                                     static_cast<size_t>(T) * (k + ns) * (I * 2 + 16));
+    const size_t x_stage = static_cast<size_t>(T) * H * esz;
+    int to, ko, co;
+    const size_t lru_end = lru_need<FMT>(a, &to, &ko, &co, static_cast<int>(fixed));
+    for (int with_act = 1; with_act >= 0; --with_act) {
+        const size_t actb = with_act ? (act_need + 127) / 128 * 128 : 0;
+        if (fixed + actb + 2 * per_stage > static_cast<size_t>(kSmemLimit)) continue;
+        int nst = static_cast<int>((kSmemLimit - fixed - actb) / per_stage);
+        nst = std::min(nst, kMaxStages);
+        const size_t ring_end = fixed + static_cast<size_t>(nst) * per_stage + actb;
+        if (lru_end > static_cast<size_t>(kSmemLimit)) return false;
+        g.nst = nst;
+        g.act_bytes = static_cast<int>(actb);
+        g.red_off = static_cast<int>(fixed + static_cast<size_t>(nst) * Fp4Cfg<FMT>::kStageBytes);
+        g.act_off = static_cast<int>(fixed + static_cast<size_t>(nst) * per_stage);
+        g.total = static_cast<int>(std::max(ring_end, lru_end));
+        g.stage_x = fixed + x_stage <= static_cast<size_t>(g.total) ? 1 : 0;
+        g.lru_trow_off = to;
+        g.lru_keys_off = ko;
+        g.lru_cache_off = co;
+        return g.total <= kSmemLimit;
+    }
+    return false;
+}
+
+template <int FMT, int ACT>
+cudaError_t launch_one(const CallArgs& a, int grid, cudaStream_t s, bool pdl) {
+    DecGeom geo{};
+    if (grid < 2) return cudaErrorInvalidValue;  // CTA 0 runs the cache update beside the others' work
+    if (!geometry<FMT>(a, geo)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(geo.total);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k_decode<FMT, ACT>, a, geo);
+}
+
+}  // namespace
+
+cudaError_t decode_set_attributes() {
+    cudaError_t e;
+    const int lim = kSmemLimit;
+    if ((e = cudaFuncSetAttribute(k_decode<FMT_NVFP4, ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
+    if ((e = cudaFuncSetAttribute(k_decode<FMT_NVFP4, ACT_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
+    if ((e = cudaFuncSetAttribute(k_decode<FMT_MXFP4, ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
+    if ((e = cudaFuncSetAttribute(k_decode<FMT_MXFP4, ACT_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const CallArgs& a, int num_sms, cudaStream_t s, bool pdl) {
+    const bool bf = a.act == ACT_BF16;
+    if (a.fmt == FMT_NVFP4)
+        return bf ? launch_one<FMT_NVFP4, ACT_BF16>(a, num_sms, s, pdl) : launch_one<FMT_NVFP4, ACT_FP32>(a, num_sms, s, pdl);
+    return bf ? launch_one<FMT_MXFP4, ACT_BF16>(a, num_sms, s, pdl) : launch_one<FMT_MXFP4, ACT_FP32>(a, num_sms, s, pdl);
+}
+
+}  // namespace moe

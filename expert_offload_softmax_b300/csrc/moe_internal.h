@@ -81,6 +81,9 @@ struct CallInfo {
     int32_t n_pf, n_pf_hit, n_pf_miss;  // prefetch batch (n_pf = 0: none)
     int32_t n_events;
     int32_t dev_err;         // sticky device error word at the time of this call (0 = none)
+    int32_t device_copied;   // 1: the call's misses were copied by its own kernel (decode)
+    int32_t pad_;
+    unsigned long long copy_ns;  // device-copied misses: first copy issued -> all landed (%globaltimer)
     // misses to copy: demand misses first, then prefetch misses
     int32_t miss_layer[2 * kMaxExperts];
     int32_t miss_expert[2 * kMaxExperts];
@@ -109,6 +112,15 @@ struct DecExpert {
 };
 static_assert(sizeof(DecExpert) == 128, "decode plan record");
 constexpr int kDecPlanHeader = 128;
+
+// Published by the CTA of the fused decode kernel that runs the cache lookup,
+// for the kernel's other CTAs: the pool slots chosen for the call's misses (in
+// the ascending order of the missed experts), valid once seq equals the call's
+// sequence number.
+struct DecPub {
+    unsigned long long seq;
+    int32_t slot[kMaxExperts];
+};
 
 struct CallArgs {
     // shape
@@ -170,6 +182,12 @@ struct CallArgs {
     unsigned long long seq;
     int self_release;
     unsigned long long wait_ns;  // bound of every device-side wait
+    // fused decode (FP4 weights, T <= 8)
+    const uint8_t* const* banks;  // [L] device views of the mapped pinned host banks
+    float* xmax;           // [8] max |x| of each token row (this call)
+    unsigned int* hmax;    // [8] max |h| (float bits) of each token's intermediate rows
+    DecPub* pub;           // miss slots for the kernel's CTAs
+    int device_misses;     // 1: the decode kernel copies its misses itself; 0: the host does
 };
 
 // Bounded wait of the expert kernels for their call's weights (one thread);
@@ -237,10 +255,13 @@ cudaError_t launch_route(const CallArgs& a, cudaStream_t s);
 // tensor-core path when `maps` holds valid descriptors.
 cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu, cudaEvent_t ev_down,
                            const UmmaMaps* maps, int num_sms, int* launches);
-// decode (T <= 8) with FP4 weights: gate/up + down in one cooperative kernel
-bool decode_fp4_supported(int fmt, int T);
-cudaError_t decode_fp4_set_attributes();
-cudaError_t launch_decode_fp4(const CallArgs& a, int num_sms, cudaStream_t s);
+// decode (T <= 8) with FP4 weights: the whole call (router, top-k,
+// permutation, cache lookup, miss copies, gate/up, down, combine) in one
+// cooperative kernel
+inline bool decode_fused(int fmt, int T) { return (fmt == FMT_NVFP4 || fmt == FMT_MXFP4) && T <= kDecodeMaxT; }
+cudaError_t decode_set_attributes();
+// smem_ok: false when the shape's cache-lookup scratch does not fit
+cudaError_t launch_decode(const CallArgs& a, int num_sms, cudaStream_t s, bool pdl);
 // loads every expert kernel (called once by moe_init)
 cudaError_t experts_preload();
 // true when a prefill call of this shape takes the tensor-core path

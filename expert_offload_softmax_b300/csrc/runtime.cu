@@ -62,6 +62,9 @@ struct TimedCall {
     cudaEvent_t r0 = nullptr, r1 = nullptr, f0 = nullptr, f1 = nullptr, f2 = nullptr, f3 = nullptr;
     cudaEvent_t c0 = nullptr, c1 = nullptr;
     bool has_copy = false, has_combine = false, had_miss = false;
+    bool fused = false;         // one decode kernel (r0 -> r1) covers the whole call
+    bool dev_copy = false;      // its misses were copied by the kernel: copy_ns from the call record
+    uint64_t copy_ns = 0;
     uint64_t gu_bytes = 0, down_bytes = 0, combine_bytes = 0, copy_bytes = 0;
 };
 
@@ -70,6 +73,7 @@ struct PendingCall {
     uint64_t seq = 0;
     int layer = 0, T = 0;
     bool self_release = true;
+    bool fused = false;
     TimedCall* tc = nullptr;
 };
 
@@ -80,10 +84,13 @@ struct moe_handle {
     // host banks: per layer, E blobs (pinned); loaded flags
     std::vector<uint8_t*> bank;
     std::vector<uint8_t> loaded;
+    std::vector<const uint8_t*> bank_dev;  // device views of the mapped banks
+    bool banks_dirty = false;             // bank_dev changed since the device table was written
     // shared experts: device resident [L][n_shared] blobs
     uint8_t* shared_dev = nullptr;
     // pool and LRU state
     uint8_t* pool = nullptr;
+    bool pool_owned = false;  // false: the caller's buffer (moe_cache_config / moe_cache_resize)
     int S = 0;
     unsigned flags = 0;
     int32_t* table = nullptr;
@@ -114,6 +121,7 @@ struct moe_handle {
     // every release, so a release always follows all of its call's copies
     cudaStream_t stream = nullptr, copy = nullptr, copy2 = nullptr;
     cudaEvent_t ev_join = nullptr;
+    cudaEvent_t ev_pf = nullptr;  // a decode call's stream waits on it for earlier prefetch copies
     // enqueue side (caller's thread)
     uint64_t submitted = 0;
     bool prefetch_may_be_pending = false;
@@ -318,7 +326,9 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
 }
 
 void free_pool(moe_handle* h) {
-    cudaFree(h->pool); h->pool = nullptr;
+    if (h->pool_owned) cudaFree(h->pool);
+    h->pool = nullptr;
+    h->pool_owned = false;
     cudaFree(h->table); h->table = nullptr;
     cudaFree(h->owner); h->owner = nullptr;
     cudaFree(h->stamp); h->stamp = nullptr;
@@ -330,7 +340,8 @@ TimedCall* acquire_timed(moe_handle* h) {
     if (!h->spare.empty()) {
         TimedCall* t = h->spare.back();
         h->spare.pop_back();
-        t->has_copy = t->has_combine = t->had_miss = false;
+        t->has_copy = t->has_combine = t->had_miss = t->fused = t->dev_copy = false;
+        t->copy_ns = 0;
         t->gu_bytes = t->down_bytes = t->combine_bytes = t->copy_bytes = 0;
         return t;
     }
@@ -357,7 +368,7 @@ void harvest(moe_handle* h, bool wait) {
     while (!h->pending.empty()) {
         TimedCall* t = h->pending.front();
         if (t->seq > done) break;
-        cudaEvent_t last = t->has_combine ? t->f3 : t->f2;
+        cudaEvent_t last = t->fused ? t->r1 : (t->has_combine ? t->f3 : t->f2);
         if (wait) {
             cudaEventSynchronize(last);
             if (t->has_copy) cudaEventSynchronize(t->c1);
@@ -366,6 +377,21 @@ void harvest(moe_handle* h, bool wait) {
             break;
         }
         h->tm.calls++;
+        if (t->fused) {
+            // the decode kernel does routing, cache lookup and the experts
+            if (!t->had_miss) {
+                h->tm.resident_calls++;
+                h->tm.gate_up_ms += elapsed(t->r0, t->r1);
+                h->tm.gate_up_bytes += t->gu_bytes;
+                h->tm.down_bytes += t->down_bytes;
+            }
+            if (t->dev_copy) h->tm.copy_ms += static_cast<double>(t->copy_ns) * 1e-6;
+            else if (t->has_copy) h->tm.copy_ms += elapsed(t->c0, t->c1);
+            h->tm.copy_bytes += t->copy_bytes;
+            h->pending.pop_front();
+            h->spare.push_back(t);
+            continue;
+        }
         h->tm.route_ms += elapsed(t->r0, t->r1);
         if (!t->had_miss) {
             // expert kernels of calls without demand misses: pure kernel time
@@ -444,7 +470,8 @@ void service_call(moe_handle* h, const PendingCall& pc) {
     std::atomic_thread_fence(std::memory_order_acquire);
     const int status = inf->status;
     const int nm = inf->n_miss, npm = inf->n_pf_miss, nu = inf->n_uniq;
-    const bool kernel_released = pc.self_release && nm == 0;
+    const bool dev_copied = inf->device_copied != 0;  // the decode kernel copied its own misses
+    const bool kernel_released = dev_copied || (pc.self_release && nm == 0);
     if (status == MOE_ERR_CAPACITY)
         record_error(h, MOE_ERR_CAPACITY, "the layer's experts do not fit in the expert pool");
     else if (status != 0)
@@ -455,7 +482,7 @@ void service_call(moe_handle* h, const PendingCall& pc) {
     const size_t B = h->lay.bytes;
     TimedCall* tc = pc.tc;
     cudaError_t ce = cudaSuccess;
-    if (tc && nm + npm > 0) {
+    if (tc && nm + npm > 0 && !dev_copied) {
         cudaEventRecord(tc->c0, h->copy);
         tc->has_copy = true;
     }
@@ -472,7 +499,7 @@ void service_call(moe_handle* h, const PendingCall& pc) {
         }
         return r;
     };
-    ce = copy_range(0, nm);
+    if (!dev_copied) ce = copy_range(0, nm);
     if (ce == cudaSuccess && !kernel_released) {
         if (h->fault_drop_release && nm > 0) h->fault_drop_release = false;
         else ce = post_ready(h, pc.seq);
@@ -510,6 +537,13 @@ void service_call(moe_handle* h, const PendingCall& pc) {
         tc->down_bytes = na * wd + rows * I * he + (tc->has_combine ? rows * H * 2 : T * H * ea);
         tc->combine_bytes = tc->has_combine ? rows * H * 2 + T * H * ea : 0;
         tc->copy_bytes = static_cast<uint64_t>(nm + npm) * B;
+        if (pc.fused) {
+            // the decode kernel also reads the router matrix [E][H] (and writes h as bf16)
+            tc->had_miss = nm > 0;
+            tc->gu_bytes += static_cast<uint64_t>(h->d.num_experts) * H * ea;
+            tc->dev_copy = dev_copied;
+            tc->copy_ns = inf->copy_ns;
+        }
     }
     std::lock_guard<std::mutex> lk(h->mu);
     h->st.calls++;
@@ -634,7 +668,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (e != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::routing_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::umma_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
-    if (moe::decode_fp4_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (moe::decode_set_attributes() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (moe::experts_preload() != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, desc->device) != cudaSuccess)
         return bail(MOE_ERR_CUDA);
@@ -649,6 +683,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     const int L = h->d.num_layers, E = h->d.num_experts, ns = h->d.num_shared, k = h->d.top_k;
     const size_t H = h->d.hidden, I = h->d.inter, Tm = h->max_tokens;
     h->bank.assign(L, nullptr);
+    h->bank_dev.assign(L, nullptr);
     h->loaded.assign(static_cast<size_t>(L) * E, 0);
     if (ns > 0) {
         if (cudaMalloc(&h->shared_dev, static_cast<size_t>(L) * ns * h->lay.bytes) != cudaSuccess) return bail(MOE_ERR_OOM);
@@ -687,6 +722,10 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
         {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
         {8, reinterpret_cast<void**>(&a.grid_bar)},
+        {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.xmax)},
+        {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
+        {sizeof(moe::DecPub), reinterpret_cast<void**>(&a.pub)},
+        {static_cast<size_t>(L) * 8, reinterpret_cast<void**>(const_cast<uint8_t***>(&a.banks))},
         {moe::kDecPlanHeader + static_cast<size_t>(E + ns) * sizeof(moe::DecExpert), reinterpret_cast<void**>(&a.dplan)},
         {8, reinterpret_cast<void**>(&a.ready)},
         {4, reinterpret_cast<void**>(&a.n_uniq)},
@@ -728,6 +767,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     if (cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaStreamCreateWithFlags(&h->copy2, cudaStreamNonBlocking) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
+    if (cudaEventCreateWithFlags(&h->ev_pf, cudaEventDisableTiming) != cudaSuccess) return bail(MOE_ERR_CUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) return bail(MOE_ERR_CUDA);
     a.E = E; a.k = k; a.H = static_cast<int>(H); a.I = static_cast<int>(I); a.n_shared = ns; a.L = L;
     a.nb_max = static_cast<int>(nb_max);
@@ -763,12 +803,22 @@ int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host*
     {
         std::lock_guard<std::mutex> lk(h->load_mu);
         if (!h->bank[layer]) {
+            // mapped: the decode kernel reads missed experts straight from the bank
             void* p = nullptr;
-            if (cudaHostAlloc(&p, static_cast<size_t>(E) * B, cudaHostAllocDefault) != cudaSuccess) {
+            void* dp = nullptr;
+            if (cudaHostAlloc(&p, static_cast<size_t>(E) * B, cudaHostAllocMapped | cudaHostAllocPortable) !=
+                cudaSuccess) {
                 cudaGetLastError();
                 return fail(h, MOE_ERR_OOM, "pinned host bank allocation failed");
             }
+            if (cudaHostGetDevicePointer(&dp, p, 0) != cudaSuccess) {
+                cudaGetLastError();
+                cudaFreeHost(p);
+                return fail(h, MOE_ERR_CUDA, "no device view of the pinned host bank");
+            }
             h->bank[layer] = static_cast<uint8_t*>(p);
+            h->bank_dev[layer] = static_cast<const uint8_t*>(dp);
+            h->banks_dirty = true;
         }
         bank = h->bank[layer];
     }
@@ -778,11 +828,64 @@ int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host*
     return MOE_OK;
 }
 
-int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
+}  // extern "C"
+
+namespace {
+
+// a pool of S slots: the caller's buffer (checked) or a new allocation
+int take_pool(moe_handle* h, size_t S, void* pool_dev, size_t pool_bytes, uint8_t** out, bool* owned) {
+    const size_t need = S * h->lay.bytes;
+    if (pool_dev) {
+        if (reinterpret_cast<uintptr_t>(pool_dev) & 255u) return fail(h, MOE_ERR_INVALID, "pool buffer must be 256-byte aligned");
+        if (pool_bytes < need) return fail(h, MOE_ERR_INVALID, "pool buffer smaller than capacity_slots expert blobs");
+        *out = static_cast<uint8_t*>(pool_dev);
+        *owned = false;
+        return MOE_OK;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, MOE_ERR_OOM, "device pool allocation failed");
+    }
+    *out = static_cast<uint8_t*>(p);
+    *owned = true;
+    return MOE_OK;
+}
+
+// TMA descriptors of the prefill GEMMs over the pool's weight regions
+int build_pool_maps(moe_handle* h) {
+    h->maps.have_pool = false;
+    if (h->maps.have_io && h->d.weight_fmt != moe::FMT_BF16) {
+        h->maps.have_pool = true;  // FP4 prefill builds its weight tiles in shared memory: no pool maps
+    } else if (h->maps.have_io) {
+        const uint64_t H = h->d.hidden, I = h->d.inter, S = h->S;
+        if (!moe::umma_map_3d(&h->maps.pool_gu, h->pool + h->lay.gu, S, h->lay.bytes, 2 * I, H, 64) ||
+            !moe::umma_map_3d(&h->maps.pool_d, h->pool + h->lay.d, S, h->lay.bytes, H, I, 128))
+            return fail(h, MOE_ERR_CUDA, "TMA descriptor encoding failed");
+        if (h->d.num_shared == 0) {
+            h->maps.shared_gu = h->maps.pool_gu;  // never selected: no shared experts
+            h->maps.shared_d = h->maps.pool_d;
+        }
+        h->maps.have_pool = true;
+    }
+    return MOE_OK;
+}
+
+void bind_pool(moe_handle* h) {
+    CallArgs& a = h->base;
+    a.table = h->table; a.owner = h->owner; a.stamp = h->stamp; a.clock = h->clock;
+    a.pool = h->pool; a.S = h->S;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* pool_dev, size_t pool_bytes) {
     if (!h) return MOE_ERR_INVALID;
     if (capacity_slots < h->d.top_k) return fail(h, MOE_ERR_CAPACITY, "capacity below top_k");
     if (capacity_slots > moe::kMaxSlots) return fail(h, MOE_ERR_INVALID, "capacity above 16384 slots");
-    if (flags & ~(MOE_CACHE_PREFETCH_NEXT_LAYER | MOE_CACHE_LOG_EVENTS | MOE_CACHE_SYNC_MISSES))
+    if (flags & ~(MOE_CACHE_PREFETCH_NEXT_LAYER | MOE_CACHE_LOG_EVENTS | MOE_CACHE_SYNC_MISSES | MOE_CACHE_HOST_MISSES))
         return fail(h, MOE_ERR_INVALID, "unknown cache flag");
     CK(h, cudaSetDevice(h->d.device));
     drain(h);
@@ -790,11 +893,8 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     free_pool(h);
     const int L = h->d.num_layers, E = h->d.num_experts;
     const size_t S = capacity_slots;
-    if (cudaMalloc(&h->pool, S * h->lay.bytes) != cudaSuccess) {
-        cudaGetLastError();
-        free_pool(h);
-        return fail(h, MOE_ERR_OOM, "device pool allocation failed");
-    }
+    int r = take_pool(h, S, pool_dev, pool_bytes, &h->pool, &h->pool_owned);
+    if (r != MOE_OK) return r;
     if (cudaMalloc(&h->table, static_cast<size_t>(L) * E * 4) != cudaSuccess ||
         cudaMalloc(&h->owner, S * 4) != cudaSuccess || cudaMalloc(&h->stamp, S * 8) != cudaSuccess ||
         cudaMalloc(&h->clock, 8) != cudaSuccess) {
@@ -813,21 +913,10 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
     const unsigned long long rv = h->submitted;
     CK(h, cudaMemcpy(h->ready, &rv, 8, cudaMemcpyHostToDevice));
     CK(h, cudaDeviceSynchronize());
-    h->maps.have_pool = false;
-    if (h->maps.have_io && h->d.weight_fmt != moe::FMT_BF16) {
-        h->maps.have_pool = true;  // FP4 prefill builds its weight tiles in shared memory: no pool maps
-    } else if (h->maps.have_io) {
-        const uint64_t H = h->d.hidden, I = h->d.inter;
-        if (!moe::umma_map_3d(&h->maps.pool_gu, h->pool + h->lay.gu, S, h->lay.bytes, 2 * I, H, 64) ||
-            !moe::umma_map_3d(&h->maps.pool_d, h->pool + h->lay.d, S, h->lay.bytes, H, I, 128)) {
-            free_pool(h);
-            return fail(h, MOE_ERR_CUDA, "TMA descriptor encoding failed");
-        }
-        if (h->d.num_shared == 0) {
-            h->maps.shared_gu = h->maps.pool_gu;  // never selected: no shared experts
-            h->maps.shared_d = h->maps.pool_d;
-        }
-        h->maps.have_pool = true;
+    h->S = capacity_slots;
+    if ((r = build_pool_maps(h)) != MOE_OK) {
+        free_pool(h);
+        return r;
     }
     {
         std::lock_guard<std::mutex> lk(h->mu);
@@ -836,14 +925,109 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags) {
         h->sticky_timeout = false;
         h->events.clear();
     }
-    h->S = capacity_slots;
     h->flags = flags;
     h->prefetch_may_be_pending = false;
+    bind_pool(h);
     CallArgs& a = h->base;
-    a.table = h->table; a.owner = h->owner; a.stamp = h->stamp; a.clock = h->clock;
-    a.pool = h->pool; a.S = h->S;
+    a.device_misses = (flags & MOE_CACHE_HOST_MISSES) ? 0 : 1;
     a.prefetch = (flags & MOE_CACHE_PREFETCH_NEXT_LAYER) ? 1 : 0;
     a.log_events = (flags & MOE_CACHE_LOG_EVENTS) ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_cache_resize(moe_handle* h, int capacity_slots, void* pool_dev, size_t pool_bytes) {
+    if (!h) return MOE_ERR_INVALID;
+    if (!h->pool) return fail(h, MOE_ERR_STATE, "moe_cache_config has not been called");
+    if (capacity_slots < h->d.top_k) return fail(h, MOE_ERR_CAPACITY, "capacity below top_k");
+    if (capacity_slots > moe::kMaxSlots) return fail(h, MOE_ERR_INVALID, "capacity above 16384 slots");
+    CK(h, cudaSetDevice(h->d.device));
+    drain(h);
+    CK(h, cudaDeviceSynchronize());
+    const int L = h->d.num_layers, E = h->d.num_experts;
+    const int S0 = h->S, S1 = capacity_slots;
+    const size_t B = h->lay.bytes;
+    // the cache state, on the host
+    std::vector<int32_t> table(static_cast<size_t>(L) * E), owner(S0);
+    std::vector<unsigned long long> stamp(S0);
+    CK(h, cudaMemcpy(table.data(), h->table, table.size() * 4, cudaMemcpyDeviceToHost));
+    CK(h, cudaMemcpy(owner.data(), h->owner, owner.size() * 4, cudaMemcpyDeviceToHost));
+    CK(h, cudaMemcpy(stamp.data(), h->stamp, stamp.size() * 8, cudaMemcpyDeviceToHost));
+    // keep the S1 most recently used experts; those in slots below S1 stay put,
+    // the others fill the free slots below S1 in ascending order of their old slot
+    std::vector<int> resident;
+    for (int s = 0; s < S0; ++s)
+        if (owner[s] >= 0) resident.push_back(s);
+    std::sort(resident.begin(), resident.end(), [&](int x, int y) {
+        return stamp[x] != stamp[y] ? stamp[x] > stamp[y] : x < y;
+    });
+    std::vector<uint8_t> kept(S0, 0);
+    for (size_t i = 0; i < resident.size() && i < static_cast<size_t>(S1); ++i) kept[resident[i]] = 1;
+    std::vector<int> dest(S0, -1);
+    std::vector<uint8_t> taken(S1, 0);
+    for (int s = 0; s < S0 && s < S1; ++s)
+        if (kept[s]) {
+            dest[s] = s;
+            taken[s] = 1;
+        }
+    int hole = 0;
+    for (int s = S1; s < S0; ++s) {
+        if (!kept[s]) continue;
+        while (taken[hole]) ++hole;
+        dest[s] = hole;
+        taken[hole] = 1;
+    }
+    std::vector<int32_t> owner1(S1, -1);
+    std::vector<unsigned long long> stamp1(S1, 0ull);
+    for (int s = 0; s < S0; ++s) {
+        if (owner[s] < 0) continue;
+        if (dest[s] >= 0) {
+            owner1[dest[s]] = owner[s];
+            stamp1[dest[s]] = stamp[s];
+            table[owner[s]] = dest[s];
+        } else {
+            table[owner[s]] = -1;
+        }
+    }
+    // the new pool, and the kept experts' blobs in their new slots
+    uint8_t* pool1 = nullptr;
+    bool owned1 = false;
+    const bool in_place = pool_dev != nullptr && pool_dev == h->pool;
+    if (in_place) {
+        if (pool_bytes < static_cast<size_t>(S1) * B) return fail(h, MOE_ERR_INVALID, "pool buffer smaller than capacity_slots expert blobs");
+        pool1 = h->pool;
+        owned1 = h->pool_owned;
+    } else {
+        const int r = take_pool(h, S1, pool_dev, pool_bytes, &pool1, &owned1);
+        if (r != MOE_OK) return r;
+    }
+    for (int s = 0; s < S0; ++s)
+        if (dest[s] >= 0 && (!in_place || dest[s] != s))
+            CK(h, cudaMemcpy(pool1 + static_cast<size_t>(dest[s]) * B, h->pool + static_cast<size_t>(s) * B, B,
+                             cudaMemcpyDeviceToDevice));
+    int32_t* owner_d = nullptr;
+    unsigned long long* stamp_d = nullptr;
+    if (cudaMalloc(&owner_d, static_cast<size_t>(S1) * 4) != cudaSuccess ||
+        cudaMalloc(&stamp_d, static_cast<size_t>(S1) * 8) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(owner_d);
+        if (owned1 && !in_place) cudaFree(pool1);
+        return fail(h, MOE_ERR_OOM, "LRU table allocation failed");
+    }
+    CK(h, cudaMemcpy(owner_d, owner1.data(), owner1.size() * 4, cudaMemcpyHostToDevice));
+    CK(h, cudaMemcpy(stamp_d, stamp1.data(), stamp1.size() * 8, cudaMemcpyHostToDevice));
+    CK(h, cudaMemcpy(h->table, table.data(), table.size() * 4, cudaMemcpyHostToDevice));
+    CK(h, cudaDeviceSynchronize());
+    if (!in_place && h->pool_owned) cudaFree(h->pool);
+    cudaFree(h->owner);
+    cudaFree(h->stamp);
+    h->pool = pool1;
+    h->pool_owned = owned1;
+    h->owner = owner_d;
+    h->stamp = stamp_d;
+    h->S = S1;
+    const int r = build_pool_maps(h);
+    if (r != MOE_OK) return r;
+    bind_pool(h);
     return MOE_OK;
 }
 
@@ -895,8 +1079,51 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         tc = acquire_timed(h);
         if (!tc) return fail(h, MOE_ERR_OOM, "timing events");
         tc->seq = seq;
-        CK(h, cudaEventRecord(tc->r0, s));
     }
+    if (moe::decode_fused(h->d.weight_fmt, T)) {
+        // decode with FP4 weights: one kernel does the whole call, including the
+        // copies of its misses (unless MOE_CACHE_HOST_MISSES); it never waits for
+        // the host except in that mode
+        if (h->banks_dirty) {
+            CK(h, cudaMemcpy(const_cast<uint8_t**>(a.banks), h->bank_dev.data(), sizeof(void*) * L,
+                             cudaMemcpyHostToDevice));
+            h->banks_dirty = false;
+        }
+        if (h->prefetch_may_be_pending) {
+            // a prefill call's prefetch copies of this layer may still be landing
+            drain(h);
+            CK(h, cudaEventRecord(h->ev_pf, h->copy));
+            CK(h, cudaStreamWaitEvent(s, h->ev_pf, 0));
+        }
+        a.self_release = 1;
+        if (tc) CK(h, cudaEventRecord(tc->r0, s));
+        const cudaError_t le = moe::launch_decode(a, h->num_sms, s, true);
+        if (le != cudaSuccess) return cuda_fail(h, le, "decode kernel launch");
+        if (tc) {
+            CK(h, cudaEventRecord(tc->r1, s));
+            tc->fused = true;
+        }
+        h->submitted = seq;
+        h->prefetch_may_be_pending = false;
+        h->last_T = T;
+        h->last_stream = s;
+        {
+            std::lock_guard<std::mutex> lk(h->mu);
+            PendingCall pc;
+            pc.seq = seq;
+            pc.layer = layer_id;
+            pc.T = T;
+            pc.self_release = true;
+            pc.fused = true;
+            pc.tc = tc;
+            h->queue.push_back(pc);
+            if (tc) h->pending.push_back(tc);
+            h->st.kernel_launches += 1;
+        }
+        h->cv.notify_one();
+        return MOE_OK;
+    }
+    if (tc) CK(h, cudaEventRecord(tc->r0, s));
     CK(h, moe::launch_route(a, s));
     if (tc) {
         CK(h, cudaEventRecord(tc->r1, s));
@@ -1064,6 +1291,7 @@ void moe_destroy(moe_handle* h) {
     if (h->copy) cudaStreamDestroy(h->copy);
     if (h->copy2) cudaStreamDestroy(h->copy2);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->ev_pf) cudaEventDestroy(h->ev_pf);
     delete h;
 }
 

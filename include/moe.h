@@ -18,18 +18,21 @@
  *
  * Every routed expert of every layer lives in a library-owned pinned host
  * bank; the GPU holds one pool of S expert slots shared by all layers. Each
- * call looks its experts up in a device-side LRU table; misses are copied into
- * the pool with cudaMemcpyAsync on a side stream. Prefill calls (T > 8) with
- * MOE_CACHE_PREFETCH_NEXT_LAYER also stream all experts of layer+1 into the
- * pool while this layer computes, when the pool has room for both.
+ * call looks its experts up in a device-side LRU table. Misses of prefill calls
+ * (T > 8) are copied into the pool with cudaMemcpyAsync on side streams, and
+ * with MOE_CACHE_PREFETCH_NEXT_LAYER all experts of layer+1 also stream into
+ * the pool while this layer computes, when the pool has room for both. Decode
+ * calls (T <= 8) with FP4 weights run as one kernel that copies its own misses
+ * from the mapped banks (or, with MOE_CACHE_HOST_MISSES, waits for the host's
+ * cudaMemcpyAsync copies).
  *
  * Calls are asynchronous: moe_layer_forward enqueues the call's kernels and
  * returns. A service thread owned by the handle reads each call's cache result
- * from mapped host memory, issues the miss copies and then releases the call's
- * expert kernels, which wait for that release on the device (bounded). A call
- * whose experts all hit releases itself on the device. Errors that the device
- * side of a call finds (capacity, bounded-wait timeouts) are reported by the
- * next moe_layer_forward or moe_sync.
+ * from mapped host memory; for host-copied misses it issues the copies and
+ * then releases the call's expert kernels, which wait for that release on the
+ * device (bounded). A call whose experts all hit releases itself on the
+ * device. Errors that the device side of a call finds (capacity, bounded-wait
+ * timeouts) are reported by the next moe_layer_forward or moe_sync.
  *
  * Conventions
  *  - Every call returns MOE_OK (0) or a negative moe_status. Nothing throws and
@@ -78,10 +81,16 @@ typedef enum moe_act_mode { MOE_MODE_SWIGLU = 0, MOE_MODE_LINEAR_TEST = 1 } moe_
 #define MOE_DECODE_MAX_T 8                /* T <= 8: decode path; T > 8: prefill path */
 #define MOE_CACHE_PREFETCH_NEXT_LAYER 1u  /* prefill: stream layer+1 behind layer */
 #define MOE_CACHE_LOG_EVENTS 2u           /* keep a per-expert hit/miss event log */
-#define MOE_CACHE_SYNC_MISSES 4u          /* service each call's misses before its expert
-                                             kernels are launched (the calling thread waits
-                                             for the routing kernel and the copies); for
-                                             debugging and for tools that serialise launches */
+#define MOE_CACHE_SYNC_MISSES 4u          /* host-copied misses: service each call's misses
+                                             before its expert kernels are launched (the
+                                             calling thread waits for the routing kernel and
+                                             the copies); for debugging and for tools that
+                                             serialise launches */
+#define MOE_CACHE_HOST_MISSES 8u          /* decode calls with FP4 weights: the host copies
+                                             their misses with cudaMemcpyAsync on a side stream
+                                             and the decode kernel waits (bounded) for its
+                                             release; by default that kernel copies its misses
+                                             itself, reading the mapped pinned banks */
 
 typedef struct moe_model_desc {
     int32_t num_layers;   /* L >= 1 */
@@ -149,83 +158,134 @@ typedef struct moe_event {
 
 typedef struct moe_handle moe_handle;
 
-/* Creates a handle: validates the shape, picks the device, creates the copy
- * stream and events, and allocates the per-call device scratch (sized for
- * max_tokens). Host banks are allocated lazily per layer by moe_load_expert.
- * Returns MOE_ERR_INVALID for an unsupported shape, MOE_ERR_OOM/CUDA on
- * allocation failure (nothing is leaked). */
+/* Creates a handle for one MoE layer stack (the layer whose experts the pages
+ * keep in host RAM with the GPU as their cache: freetoken.wiki architecture
+ * page, two-tier expert memory paragraph). Validates the shape, picks the
+ * device, creates the copy streams and events, and allocates the per-call
+ * device scratch (sized for max_tokens). Host banks are allocated lazily per
+ * layer by moe_load_expert. Returns MOE_ERR_INVALID for an unsupported shape,
+ * MOE_ERR_OOM/CUDA on allocation failure (nothing is leaked). */
 int moe_init(const moe_model_desc* desc, moe_handle** out);
 
-/* Bytes of one expert in the library's device layout (the unit the cache
- * stores and copies). */
+/* Bytes of one expert in the library's device layout: the unit the cache
+ * stores and copies (one expert is the unit of the pages' expert cache,
+ * freetoken.wiki architecture page, two-tier expert memory paragraph). */
 int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
 
 /* Writes one expert, given in the canonical host layout, into `blob` (host
  * memory of blob_bytes >= moe_expert_bytes) in the library's device layout:
  * the bytes moe_load_expert keeps in its pinned bank and a cache slot holds.
  * Host-only (no device is touched); for tools that prepare or inspect blobs.
- * MOE_ERR_INVALID for a bad shape, NULL pointers or a short buffer. */
+ * MOE_ERR_INVALID for a bad shape, NULL pointers or a short buffer. The
+ * formats are those the bhrtaym-blog post lists (section on supported models
+ * and quantisation formats: MXFP4, NVFP4, BF16). */
 int moe_repack_expert(const moe_model_desc* desc, const moe_expert_host* w, void* blob, size_t blob_bytes);
 
 /* Copies one expert from the canonical host layout into the library's pinned
  * host bank (routed experts, expert < E) or into device-resident memory
  * (shared experts, E <= expert < E + num_shared), repacking it into the device
- * layout. The caller's buffers may be freed on return. Synchronous. Unlike the
- * other calls, which expect one host thread at a time per handle, this one may
- * run concurrently from several host threads (e.g. one per layer), as long as
- * no forward call is in progress; each (layer, expert) is loaded by one thread. */
+ * layout ("every routed expert lives in host RAM": freetoken.wiki architecture
+ * page, two-tier expert memory paragraph). Banks are pinned and mapped into the
+ * device's address space. The caller's buffers may be freed on return.
+ * Synchronous. Unlike the other calls, which expect one host thread at a time
+ * per handle, this one may run concurrently from several host threads (e.g.
+ * one per layer), as long as no forward call is in progress; each (layer,
+ * expert) is loaded by one thread. */
 int moe_load_expert(moe_handle* h, int layer, int expert, const moe_expert_host* w);
 
-/* A safe point: waits until every enqueued call has finished, then (re)builds
- * the expert pool with capacity_slots slots shared by all layers, empties the
- * LRU table and the event log, and clears errors of earlier calls (including a
- * bounded-wait timeout). flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS,
- * MOE_CACHE_SYNC_MISSES; other bits give MOE_ERR_INVALID. Every
- * routed expert must have been loaded before the first forward call.
- * capacity_slots < top_k gives MOE_ERR_CAPACITY. */
-int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags);
+/* A safe point that (re)builds the cache (freetoken.wiki architecture page:
+ * the scheduler resizes and rebuilds the GPU expert cache at its safe points).
+ * Waits until every enqueued call has finished, then makes a pool of
+ * capacity_slots slots shared by all layers, empties the LRU table and the
+ * event log, and clears errors of earlier calls (including a bounded-wait
+ * timeout).
+ *  flags: MOE_CACHE_PREFETCH_NEXT_LAYER, MOE_CACHE_LOG_EVENTS,
+ *         MOE_CACHE_SYNC_MISSES, MOE_CACHE_HOST_MISSES; other bits give
+ *         MOE_ERR_INVALID.
+ *  pool_dev, pool_bytes: optional caller-owned device buffer for the pool
+ *         (e.g. from the caller's framework allocator): 256-byte aligned, at
+ *         least capacity_slots * moe_expert_bytes bytes, kept alive by the
+ *         caller until the next moe_cache_config / moe_cache_resize with
+ *         another buffer or moe_destroy; the library never frees it. NULL:
+ *         the library allocates (and frees) the pool.
+ * Every routed expert must have been loaded before the first forward call.
+ * capacity_slots < top_k gives MOE_ERR_CAPACITY; a short or misaligned
+ * pool_dev gives MOE_ERR_INVALID. */
+int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* pool_dev, size_t pool_bytes);
 
-/* One call of MoE layer `layer_id` on T tokens (0 <= T <= max_tokens):
- * hidden [T, H], router_w [E, H], out [T, H], all device memory in the handle's
- * act_dtype, row-major. Enqueued on `stream` (a cudaStream_t; NULL = the
- * handle's own stream) and returns without waiting for the device; the host
- * blocks only when 16 calls are already waiting for the service thread (with
- * MOE_CACHE_SYNC_MISSES it also blocks until the call's misses have landed). out is
- * complete once `stream` has passed the call. A call whose layer's experts
- * exceed the pool leaves the cache unchanged and out unwritten; the next
- * moe_layer_forward or moe_sync returns MOE_ERR_CAPACITY for it. Errors found
- * for earlier calls are returned before anything is enqueued. */
+/* A safe point that resizes the cache and keeps what it holds (freetoken.wiki
+ * architecture page: the cache is resized at the scheduler's safe points; the
+ * bhrtaym-blog post's CLI table: `ft ctl cache --moe N` changes it without
+ * stopping the server). Waits until every enqueued call has finished. The
+ * min(capacity_slots, resident) most recently used experts stay cached with
+ * their recency; a kept expert whose slot is below capacity_slots keeps its
+ * slot, the other kept experts move, in ascending order of their old slot, to
+ * the lowest slots left free; every other expert leaves the cache. Flags,
+ * statistics, the event log and pending errors are unchanged.
+ *  pool_dev, pool_bytes: as for moe_cache_config. The current pool buffer may
+ *         be passed again (resizing in place: bytes of moved experts are copied
+ *         within it); NULL: the library allocates a new pool (and frees the
+ *         old one if it owned it).
+ * MOE_ERR_STATE before moe_cache_config; capacity_slots < top_k gives
+ * MOE_ERR_CAPACITY. */
+int moe_cache_resize(moe_handle* h, int capacity_slots, void* pool_dev, size_t pool_bytes);
+
+/* One call of MoE layer `layer_id` on T tokens (0 <= T <= max_tokens): the
+ * routed MoE layer of the pages' offload backend (bhrtaym-blog post, section
+ * on the four MoE backends, `offload`; freetoken.wiki architecture page:
+ * decode runs hits on the GPU and copies misses into the cache over PCIe,
+ * prefill streams the next layer's experts behind the current layer).
+ *  hidden [T, H], router_w [E, H], out [T, H]: device memory in the handle's
+ *         act_dtype, row-major, 16-byte aligned, owned by the caller (alive
+ *         until `stream` has passed the call).
+ *  stream: a cudaStream_t (NULL = the handle's own stream).
+ * Returns without waiting for the device; the host blocks only when 16 calls
+ * are already waiting for the service thread (with MOE_CACHE_SYNC_MISSES it
+ * also blocks until the call's host-copied misses have landed). out is
+ * complete once `stream` has passed the call. Decode (T <= 8) with FP4 weights
+ * is one kernel that also copies the call's misses from the mapped banks
+ * (unless MOE_CACHE_HOST_MISSES). A call whose experts exceed the pool leaves
+ * the cache unchanged and out unwritten; the next moe_layer_forward or
+ * moe_sync returns MOE_ERR_CAPACITY for it. Errors found for earlier calls are
+ * returned before anything is enqueued. */
 int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, int layer_id,
                       int T, void* out, void* stream);
 
 /* Waits until every call enqueued so far has been serviced and has finished on
- * the device (its stream and the copy stream), then returns the first error
+ * the device (its stream and the copy streams), then returns the first error
  * found for any of them (MOE_ERR_CAPACITY once; MOE_ERR_TIMEOUT until the next
  * moe_cache_config), or MOE_OK. */
 int moe_sync(moe_handle* h);
 
-/* Cumulative counters since moe_init (or the last moe_stats_reset). */
+/* Cumulative cache counters since moe_init (or the last moe_stats_reset):
+ * hits, misses, prefetches, evictions, bytes copied (the quantities the
+ * pages' cache reasons about: freetoken.wiki architecture page, decode LRU
+ * paragraph). Waits for the service thread. */
 int moe_stats(moe_handle* h, moe_stats_t* s);
 int moe_stats_reset(moe_handle* h);
 
 /* enable != 0: start timing the following forward calls (accumulators reset);
- * enable == 0: stop. */
+ * enable == 0: stop. Measurement support (no counterpart on the pages). */
 int moe_timing_enable(moe_handle* h, int enable);
 
 /* Waits for all timed work to finish and returns the accumulated totals. */
 int moe_timing(moe_handle* h, moe_timing_t* t);
 
 /* Drains up to cap logged events (MOE_CACHE_LOG_EVENTS) into buf, in the order
- * the cache served them; *n receives the number written. */
+ * the cache served them; *n receives the number written. One event per expert
+ * access of the decode LRU and of the prefill prefetch batch (freetoken.wiki
+ * architecture page, decode LRU and prefill double-buffering paragraphs). */
 int moe_stats_events(moe_handle* h, moe_event* buf, int cap, int* n);
 
 /* Host copies of the routing of the last forward call (any pointer may be
  * NULL): topk_idx [T*k], gates [T*k], perm [T*k], counts [E], uniq [E]
- * (ascending experts with at least one token; *n_uniq entries). Synchronous. */
+ * (ascending experts with at least one token; *n_uniq entries). Synchronous.
+ * Test support (no counterpart on the pages). */
 int moe_debug_routing(moe_handle* h, int32_t* topk_idx, float* gates, int32_t* perm,
                       int32_t* counts, int32_t* uniq, int32_t* n_uniq);
 
-/* Host copy of the LRU table [L*E] (slot or -1) after the last call. */
+/* Host copy of the LRU table [L*E] (slot or -1) after the last call. Test
+ * support (no counterpart on the pages). */
 int moe_debug_lru_table(moe_handle* h, int32_t* table);
 
 /* Router top-k that allocates nothing (the pages describe no counterpart: it
@@ -243,8 +303,8 @@ int moe_debug_lru_table(moe_handle* h, int32_t* table);
  * T above 8 * 65535 = 524280 (the token blocks of its logits grid), E > 1024,
  * k > min(E, 32), H not a positive multiple of 8 or too large for the
  * shared-memory tile give MOE_ERR_INVALID. A failed launch gives MOE_ERR_CUDA;
- * CUDA errors that other calls left pending are neither reported nor cleared. Calls no allocator. The first call
- * on a device, with that device current, looks the array's address up
+ * CUDA errors that other calls left pending are neither reported nor cleared.
+ * Calls no allocator. The first call on a device, with that device current, looks the array's address up
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make it
  * before any stream capture. All calls share the array and it keeps the last
  * call's contents; calls whose work overlaps on the GPU race on it. */
@@ -252,8 +312,11 @@ int moe_debug_lru_table(moe_handle* h, int32_t* table);
 int moe_route_topk_noalloc(const void* hidden, const void* router_w, int T, int E, int H, int k, int act_dtype,
                            int32_t* topk_idx, float* gates, void* stream);
 
+/* Human-readable reason of the handle's last failed call ("NULL handle" for NULL). */
 const char* moe_last_error(const moe_handle* h);
 
+/* Waits for the device, stops the service thread and frees everything the
+ * library allocated (a caller-owned pool buffer is left alone). */
 void moe_destroy(moe_handle* h);
 
 #ifdef __cplusplus

@@ -63,6 +63,8 @@ def _L():
         lib.orc_layer_tokens.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                          vp, i32, vp]
         lib.orc_combine.argtypes = [i32, i32, i32, vp, vp, vp]
+        lib.orc_lru_resize.restype = i32
+        lib.orc_lru_resize.argtypes = [i32, i32, i32, vp, vp, vp, i32, vp, vp, vp]
         _lib = lib
     return _lib
 
@@ -204,6 +206,19 @@ class LRU:
             raise LRU.CapacityError(f"layer {layer}: {n} experts do not fit in {self.S} slots")
         return {"expert": ev[0], "hit": ev[1], "slot": ev[2], "evicted": ev[3],
                 "layer": np.full(n, layer, np.int32)}
+
+    def resize(self, S_new: int) -> np.ndarray:
+        """Resize the pool at a safe point (see ``orc_lru_resize``): the most
+        recently used experts that fit stay cached. Returns moved[old slot] =
+        new slot (or -1)."""
+        new_owner = np.empty(S_new, np.int32)
+        new_stamp = np.empty(S_new, np.uint64)
+        S_old = self.S
+        moved = np.empty(max(1, S_old), np.int32)
+        _L().orc_lru_resize(self.L, self.E, S_old, _p(self.table), _p(self.owner), _p(self.stamp), S_new,
+                            _p(new_owner), _p(new_stamp), _p(moved))
+        self.owner, self.stamp, self.S = new_owner, new_stamp, S_new
+        return moved[:S_old]
 
     def access(self, layer: int, uniq: np.ndarray, T: int, prefetch: bool):
         evs = [self.batch(layer, uniq)]

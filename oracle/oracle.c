@@ -360,3 +360,81 @@ void orc_combine(int H, int k, int n_shared, const float* gates, const float* co
     for (int s = 0; s < n_shared; ++s)
         for (int r = 0; r < H; ++r) out[r] = out[r] + y[k + s][r];
 }
+
+/* ------------------------------------------------------------------------- */
+/* Resizing the pool at a safe point                                         */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    uint64_t stamp;
+    int32_t slot;
+} orc_slot_age;
+
+static int orc_by_recency(const void* a, const void* b) {
+    const orc_slot_age* x = (const orc_slot_age*)a;
+    const orc_slot_age* y = (const orc_slot_age*)b;
+    if (x->stamp != y->stamp) return x->stamp > y->stamp ? -1 : 1; /* most recent first */
+    return x->slot < y->slot ? -1 : (x->slot > y->slot);
+}
+
+/* Resize the pool from S_old to S_new slots at a safe point, keeping the most
+ * recently used experts (the cache is "resized and rebuilt at the scheduler's
+ * safe points" on the freetoken.wiki architecture page; the pages do not say
+ * which experts survive, so the reading here keeps the LRU order):
+ *  - the min(S_new, resident) cached experts with the largest stamps stay;
+ *  - a kept expert whose slot is below S_new keeps that slot; the other kept
+ *    experts move, in ascending order of their old slot, to the lowest slots
+ *    below S_new that hold no kept expert;
+ *  - every other expert leaves the cache (its table entry becomes -1);
+ *  - stamps move with their experts, free slots get stamp 0 and owner -1, and
+ *    the clock is unchanged.
+ * new_owner / new_stamp receive the S_new-slot state, table is updated in
+ * place, and moved[s] (s < S_old) receives the new slot of old slot s's
+ * expert, or -1 if it was dropped or empty. Returns the number kept. */
+int orc_lru_resize(int L, int E, int S_old, int32_t* table, const int32_t* owner, const uint64_t* stamp,
+                   int S_new, int32_t* new_owner, uint64_t* new_stamp, int32_t* moved) {
+    (void)L;
+    (void)E;
+    orc_slot_age* res = (orc_slot_age*)malloc(sizeof(orc_slot_age) * (size_t)(S_old > 0 ? S_old : 1));
+    int n = 0;
+    for (int s = 0; s < S_old; ++s) {
+        moved[s] = -1;
+        if (owner[s] >= 0) {
+            res[n].stamp = stamp[s];
+            res[n].slot = s;
+            n++;
+        }
+    }
+    qsort(res, (size_t)n, sizeof(orc_slot_age), orc_by_recency);
+    int keep = n < S_new ? n : S_new;
+    unsigned char* kept = (unsigned char*)calloc((size_t)(S_old > 0 ? S_old : 1), 1);
+    for (int i = 0; i < keep; ++i) kept[res[i].slot] = 1;
+    for (int s = 0; s < S_new; ++s) {
+        new_owner[s] = -1;
+        new_stamp[s] = 0;
+    }
+    /* kept experts already below S_new stay where they are */
+    for (int s = 0; s < S_old && s < S_new; ++s)
+        if (kept[s]) moved[s] = s;
+    /* the others fill the free slots below S_new, in ascending old-slot order */
+    int hole = 0;
+    for (int s = S_new; s < S_old; ++s) {
+        if (!kept[s]) continue;
+        while (hole < S_new && hole < S_old && kept[hole]) hole++;
+        moved[s] = hole;
+        hole++;
+    }
+    for (int s = 0; s < S_old; ++s) {
+        if (owner[s] < 0) continue;
+        if (moved[s] >= 0) {
+            new_owner[moved[s]] = owner[s];
+            new_stamp[moved[s]] = stamp[s];
+            table[owner[s]] = moved[s];
+        } else {
+            table[owner[s]] = -1;
+        }
+    }
+    free(res);
+    free(kept);
+    return keep;
+}

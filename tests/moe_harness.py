@@ -45,9 +45,15 @@ class GpuStack:
                        for l in range(L)]
         self.stream = torch.cuda.Stream(device=self.dev)
 
-    def reconfigure(self, capacity: int, flags: int = 0):
-        """A safe point: empty the cache and rebuild the pool with ``capacity`` slots."""
-        moe.moe_cache_config(self.h, capacity, flags | moe.MOE_CACHE_LOG_EVENTS)
+    def reconfigure(self, capacity: int, flags: int = 0, pool=None):
+        """A safe point: empty the cache and rebuild the pool with ``capacity``
+        slots (``pool``: optional caller-owned torch uint8 device tensor)."""
+        moe.moe_cache_config(self.h, capacity, flags | moe.MOE_CACHE_LOG_EVENTS,
+                             pool.data_ptr() if pool is not None else 0, pool.numel() if pool is not None else 0)
+
+    def resize(self, capacity: int, pool=None):
+        moe.moe_cache_resize(self.h, capacity, pool.data_ptr() if pool is not None else 0,
+                             pool.numel() if pool is not None else 0)
 
     def to_dev(self, a: np.ndarray):
         t = self.torch
@@ -106,6 +112,9 @@ class OracleStack:
                        for l in range(L)]
         self.cache = {}
         self.max_cached = max_cached_experts
+
+    def resize(self, capacity: int):
+        self.lru.resize(capacity)
 
     def weights(self, layer, e):
         key = (layer, e)

@@ -35,6 +35,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"].startswith("decode-40L")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["nproc"] >= 1 and "cpu_model" in cb
+    # the steps it reports are the oracle layer calls it timed, in this run
+    assert d["timed_s"] > 0 and d["ms_per_step"] * d["steps"] <= d["timed_s"] * 1e3 * 1.05 + 1
+    assert d["config"]["pool_slots"] == 2560 and d["config"]["cache_flags"] == 0
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
 
@@ -81,7 +85,7 @@ def test_bench_line_from_measurements():
     assert d["ms_per_step"] == 2.0 and d["steps"] == K and d["warmup"] == 300
     assert d["e2e"]["value"] == 400.0 and d["e2e"]["h2d_bytes_per_step"] == L * 2048 * 2
     r = d["roofline"]
-    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"].startswith("k_dec_fp4")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"].startswith("k_decode")
     assert r["algorithmic_bytes_per_launch"] == 14_000_000
     assert abs(r["achieved"] - 14_000_000 / 20e-6 / 1e9) < 0.1 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-4
     assert d["gpu_launches"] == 2 * K * L and d["cpu_baseline"] is None

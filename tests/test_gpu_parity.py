@@ -109,6 +109,17 @@ def test_zipf_skewed_decode_many_steps():
     _run(s, 16, 4, 64, calls)
 
 
+def test_host_copied_decode_misses_match_oracle():
+    """MOE_CACHE_HOST_MISSES: the host copies each decode call's misses with
+    cudaMemcpyAsync and the decode kernel waits for its release; routing, the
+    cache sequence and the outputs are those of the oracle (as for the default,
+    where the kernel copies them itself)."""
+    s = synth.Shape("zipf", L=4, E=64, k=8, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16, zipf_s=1.0)
+    _run(s, 16, 4, 64, [(l, 1 + (st % 8), st) for st in range(6) for l in range(4)], flags=8)
+    s = synth.Shape("small", L=2, E=16, k=4, H=384, I=256, fmt=synth.FMT_MXFP4, act=synth.ACT_BF16, shared=1)
+    _run(s, 13, 2, 20, [(l % 2, 1 + l % 8, l) for l in range(10)], flags=8)
+
+
 def test_sync_misses_mode_matches_oracle():
     """MOE_CACHE_SYNC_MISSES moves the miss copies before the expert launches;
     the cache sequence and the outputs are those of the asynchronous path."""

@@ -132,3 +132,67 @@ def test_lru_with_prefetch_equals_textbook():
         assert len(ev["expert"]) == len(ref)
         for i, r in enumerate(ref):
             assert (ev["hit"][i], ev["slot"][i], ev["evicted"][i]) == r
+
+
+def _textbook_resize(t, S_new):
+    """The textbook LRU after a resize: the S_new most recently used keys stay,
+    in their recency order; a kept key whose slot is below S_new keeps it, the
+    others take the lowest slots below S_new left free, in ascending old-slot
+    order."""
+    items = list(t.order.items())           # least recent first
+    kept = items[max(0, len(items) - S_new):]
+    stay = {k: s for k, s in kept if s < S_new}
+    movers = sorted((s, k) for k, s in kept if s >= S_new)
+    holes = [s for s in range(S_new) if s not in set(stay.values())]
+    new_slot = dict(stay)
+    for (old, k), hole in zip(movers, holes):
+        new_slot[k] = hole
+    nt = TextbookLRU(S_new)
+    nt.order = OrderedDict((k, new_slot[k]) for k, _ in kept)
+    nt.free = [s for s in range(S_new) if s not in set(new_slot.values())]
+    return nt
+
+
+@pytest.mark.parametrize("S_old,S_new", [(6, 9), (9, 4), (5, 5), (8, 2), (4, 12), (7, 1)])
+def test_resize_keeps_most_recent_and_continues_as_textbook(S_old, S_new):
+    rng = np.random.default_rng(S_old * 31 + S_new)
+    L, E = 3, 6
+    trace = []
+    for _ in range(14):
+        layer = int(rng.integers(L))
+        m = sorted(rng.choice(E, size=int(rng.integers(1, min(E, S_old) + 1)), replace=False).tolist())
+        trace.append((layer, m))
+    o, t = _run_both(L, E, S_old, trace)
+    before = {int(o.owner[s]): s for s in range(S_old) if o.owner[s] >= 0}
+    moved = o.resize(S_new)
+    t = _textbook_resize(t, S_new)
+    # the cached set and its slots are the textbook's
+    got = {int(o.owner[s]): s for s in range(S_new) if o.owner[s] >= 0}
+    assert got == dict(t.order)
+    for key, s in got.items():
+        assert o.table[key] == s
+    for key in set(before) - set(got):
+        assert o.table[key] == -1
+    # moved[] maps each old slot to its expert's new slot
+    for key, s_old in before.items():
+        assert moved[s_old] == got.get(key, -1)
+    # free slots read as never filled
+    assert all(o.stamp[s] == 0 for s in range(S_new) if o.owner[s] < 0)
+    # and the cache then behaves as the textbook LRU of the new capacity
+    for _ in range(10):
+        layer = int(rng.integers(L))
+        m = sorted(rng.choice(E, size=int(rng.integers(1, min(E, S_new) + 1)), replace=False).tolist())
+        ev = o.batch(layer, np.array(m, np.int32))
+        ref = t.batch([layer * E + e for e in m])
+        for p in range(len(m)):
+            assert (ev["hit"][p], ev["slot"][p], ev["evicted"][p]) == ref[p]
+
+
+def test_resize_growing_moves_nothing():
+    o = oracle.LRU(2, 8, 5)
+    for layer, m in ((0, [1, 2, 3]), (1, [0, 4]), (0, [2, 5])):
+        o.batch(layer, np.array(m, np.int32))
+    owner = o.owner.copy()
+    moved = o.resize(11)
+    assert all(moved[s] == (s if owner[s] >= 0 else -1) for s in range(5))
+    assert np.array_equal(o.owner[:5], owner) and (o.owner[5:] == -1).all()
