@@ -56,10 +56,12 @@ namespace {
 constexpr int kConsumers = 8;
 constexpr int kWarps = kConsumers + 1;
 constexpr int kThreads = 32 * kWarps;
+static_assert(kDecodeMaxT * kMaxTopK < 32 * kWarps, "one assignment per thread in the routing counts");
 constexpr int kStageGroups = 2 * kChunkGroups;  // K groups (16 rows x 128) per pipeline stage
 constexpr int kMaxStages = 12;
 constexpr int kMaxAssign = kDecodeMaxT * kMaxTopK;
 constexpr int kRedSlotBytes = kConsumers * 32 * 4 * 4;  // one tile's 8 partial accumulators
+constexpr int kRedSlots = 4;                            // tiles whose reduction can be in flight
 constexpr int kSmemLimit = 220 * 1024;                  // dynamic bytes; a few KB static sit beside it
 constexpr int kLruCached = 4096;                        // pools up to this size cache stamps/owners in smem
 
@@ -82,10 +84,12 @@ struct DecRoute {
     int32_t hit[kMaxAssign];      // 1: the member was in the cache
     int32_t missr[kMaxAssign];    // member index of the r-th miss
     int32_t rowtok[kMaxAssign + kDecodeMaxT];  // token of h row r
+    int32_t trow[kMaxExperts];    // this layer's LRU table row as it was before the call
     float xsc[kDecodeMaxT], xun[kDecodeMaxT];  // activation power-of-two scale and its inverse
     float hsc[kDecodeMaxT], hun[kDecodeMaxT];
     unsigned int xmax[kDecodeMaxT], hmax[kDecodeMaxT];
-    int32_t red_cnt[kMaxStages];
+    int32_t red_cnt[kRedSlots];   // arrivals at each reduction slot
+    int32_t red_gen[kRedSlots];   // uses of each slot finished
     int32_t nu, n_miss, status, ok;
     unsigned long long t_copy0;
 };
@@ -96,7 +100,7 @@ struct DecGeom {
     int max_active;   // plan records
     int act_bytes;    // token rows (phase 1) / h rows (phase 2) in smem; 0: read from global
     int plan_off, ring_off, red_off, act_off, total;
-    int stage_x;      // 1: P1 stages the raw token rows at ring_off
+    int stage_x;      // 1: P1 stages the raw token rows and this CTA's router rows at ring_off
     int lru_trow_off, lru_keys_off, lru_cache_off;  // CTA 0's cache-lookup scratch (aliases the ring)
 };
 
@@ -140,11 +144,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(su32(bar))
         : "memory");
 }
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -153,43 +152,49 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned lo
 __device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned int atom_add_acqrel_gpu(unsigned int* p, unsigned int v) {
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ void st_relaxed_gpu(unsigned int* p, unsigned int v) {
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_add_release_gpu(unsigned int* p, unsigned int v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory"); }
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
-// One arrival of this CTA at a grid-wide barrier (called by one thread after
-// the CTA has synchronised): arrivals are counted with an acquire-release add
-// that publishes the CTA's writes; the last arrival resets the count and bumps
-// the generation, which the others poll with acquire loads (bounded).
-__device__ bool grid_arrive_wait(const CallArgs& a, int G, int err_code) {
-    unsigned int* cnt = a.grid_bar;
-    unsigned int* gen = a.grid_bar + 1;
+// Grid-wide barriers without a shared counter: CTA b announces that it has
+// reached barrier `epoch` by storing epoch into its own flag (a release store
+// that publishes the CTA's writes), and a CTA passes the barrier once the
+// flags of all participating CTAs [first, last) hold at least epoch (one warp
+// polls them, coalesced, with acquire loads; bounded). Epochs grow with the
+// call's sequence number, so no flag is ever reset.
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void grid_arrive(const CallArgs& a, int b, unsigned long long epoch) {
     __threadfence();
-    const unsigned int my_gen = ld_acquire_gpu(gen);
-    const unsigned int prev = atom_add_acqrel_gpu(cnt, 1u);
-    if (prev == static_cast<unsigned int>(G) - 1u) {
-        st_relaxed_gpu(cnt, 0u);
-        red_add_release_gpu(gen, 1u);
-        return true;
-    }
+    st_release_gpu_u64(a.grid_flags + b, epoch);
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// called by a whole warp; true once every flag in [first, last) >= epoch. The
+// polls are relaxed loads, all in flight together; the acquire fence after the
+// last poll orders what the CTA reads next after every participant's release.
+__device__ bool grid_wait(const CallArgs& a, int first, int last, unsigned long long epoch, int err_code) {
+    const int lane = threadIdx.x & 31;
     const uint64_t t0 = gtimer();
-    while (ld_acquire_gpu(gen) == my_gen) {
+    for (;;) {
+        bool mine = true;
+#pragma unroll 8
+        for (int i = first + lane; i < last; i += 32) mine &= ld_relaxed_gpu64(a.grid_flags + i) >= epoch;
+        if (__all_sync(0xffffffffu, mine)) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
         if (gtimer() - t0 > a.wait_ns) {
-            atomicExch(a.dev_err, err_code);
+            if (lane == 0) atomicExch(a.dev_err, err_code);
             return false;
         }
     }
-    return true;
 }
 
 // power of two p with max|v| * p in [2^14, 2^15) (1 for 0 or non-finite), and 1/p
@@ -232,12 +237,15 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
 }
 
 // One 128-element K group of a staged 16-row chunk (ng groups) against one
-// 8-column B run: acc (rows g / g+8, columns 2q / 2q+1) += the group's dot
-// products. NVFP4 (scale folded into the f16 operand): accumulates in the MMA.
-// MXFP4: each 32-element block (two MMA steps) times its E8M0 scale, in fp32.
+// 8-column B run: acc0 + acc1 (rows g / g+8, columns 2q / 2q+1) += the group's
+// dot products. NVFP4 (scale folded into the f16 operand): accumulates in the
+// MMA, even steps into acc0 and odd steps into acc1 (two independent chains,
+// so consecutive MMAs of a warp do not wait for each other). MXFP4: each
+// 32-element block (two MMA steps from zero) times its E8M0 scale, in fp32,
+// into acc0.
 template <int FMT>
 __device__ __forceinline__ void mma_group(const unsigned char* chunk, int ng, int w, int g, int q,
-                                          const uint32_t (&b)[16], float (&acc)[4]) {
+                                          const uint32_t (&b)[16], float (&acc0)[4], float (&acc1)[4]) {
     constexpr int kSbpg = Fp4Cfg<FMT>::kSbpg;
     const uint4 ra = lds128(chunk + fp4_code_off(ng, g, w, q));
     const uint4 rb = lds128(chunk + fp4_code_off(ng, g + 8, w, q));
@@ -258,7 +266,8 @@ __device__ __forceinline__ void mma_group(const unsigned char* chunk, int ng, in
                 const uint32_t sa = __byte_perm(fa[s >> 1], 0u, sel), sb = __byte_perm(fb[s >> 1], 0u, sel);
                 const uint32_t A[4] = {hmul2u(oa[2 * h], sa), hmul2u(ob[2 * h], sb), hmul2u(oa[2 * h + 1], sa),
                                        hmul2u(ob[2 * h + 1], sb)};
-                mma_f16(acc, A, b[2 * s], b[2 * s + 1], acc);
+                if (h == 0) mma_f16(acc0, A, b[2 * s], b[2 * s + 1], acc0);
+                else mma_f16(acc1, A, b[2 * s], b[2 * s + 1], acc1);
             }
         }
     } else {
@@ -277,10 +286,10 @@ __device__ __forceinline__ void mma_group(const unsigned char* chunk, int ng, in
                 mma_f16(d, A, b[2 * s], b[2 * s + 1], d);
             }
             const float sa = e8m0_to_f32((va >> (8 * x)) & 0xFFu), sb = e8m0_to_f32((vb >> (8 * x)) & 0xFFu);
-            acc[0] = __fmaf_rn(sa, d[0], acc[0]);
-            acc[1] = __fmaf_rn(sa, d[1], acc[1]);
-            acc[2] = __fmaf_rn(sb, d[2], acc[2]);
-            acc[3] = __fmaf_rn(sb, d[3], acc[3]);
+            acc0[0] = __fmaf_rn(sa, d[0], acc0[0]);
+            acc0[1] = __fmaf_rn(sa, d[1], acc0[1]);
+            acc0[2] = __fmaf_rn(sb, d[2], acc0[2]);
+            acc0[3] = __fmaf_rn(sb, d[3], acc0[3]);
         }
     }
 }
@@ -358,9 +367,11 @@ struct Stage {
 };
 
 // The stage sequence of one CTA, identical for its producer and consumers.
+// CTA 0 runs the cache update and takes no tiles; CTA b >= 1 is worker b1 = b-1
+// of G1 = G-1.
 //  phase 1: gate/up tiles i = b1, b1 + G1, ... (active expert u = i / (I/8),
 //           unit tile i mod (I/8)); a stage = up to two 8-group chunks.
-//  phase 2: down row tiles rt = b, b + G, ...; for each, every active expert's
+//  phase 2: down row tiles rt = b1, b1 + G1, ...; for each, every active expert's
 //           16-row tile: up to two chunks of one expert per stage when I >= 1024,
 //           else the whole tiles of several experts (16 groups at most).
 template <int FMT>
@@ -397,7 +408,7 @@ struct StageSeq {
             ns2 = (na + epp - 1) / epp;
         }
         n2 = ca.H / kTileRows;
-        my2 = b < n2 ? (n2 - 1 - b) / G + 1 : 0;
+        my2 = (b1 >= 0 && b1 < n2) ? (n2 - 1 - b1) / G1 + 1 : 0;
     }
     __device__ int count1() const { return my1 * ns1; }
     __device__ int count2() const { return my2 * ns2; }
@@ -424,7 +435,7 @@ struct StageSeq {
     }
     // phase 2, stage f: row tile rt; experts [u0, u0 + nu); chunks [c0, c0 + nc) (one expert) or whole tiles
     __device__ void where2(int f, int& rt, int& u0, int& nu_, int& c0, int& nc) const {
-        rt = b + (f / ns2) * G;
+        rt = b1 + (f / ns2) * G1;
         const int k = f % ns2;
         if (epp == 1) {
             u0 = k / nsu;
@@ -465,7 +476,7 @@ template <int FMT, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo) {
     using C = Fp4Cfg<FMT>;
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], p1bar;
     __shared__ int s_abort;
 
     DecRoute& R = *reinterpret_cast<DecRoute*>(dsm);
@@ -481,16 +492,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
     const size_t B = a.lay.bytes;
     volatile int* abort_flag = &s_abort;
+    // the call's grid barriers: logits written / misses copied / h written
+    const unsigned long long epoch0 = a.seq * 4ull, epoch1 = epoch0 + 1, epoch2 = epoch0 + 2;
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumers);
         }
+        mbar_init(&p1bar, 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < kMaxStages) R.red_cnt[tid] = 0;
+    if (tid < kRedSlots) {
+        R.red_cnt[tid] = 0;
+        R.red_gen[tid] = 0;
+    }
     if (tid < kDecodeMaxT) {
         R.xmax[tid] = 0u;
         R.hmax[tid] = 0u;
@@ -500,88 +517,113 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
+    // optional phase timeline (MOE_TRACE): per CTA, %globaltimer at fixed points
+    auto mark = [&](int point) {
+        if (a.trace) a.trace[static_cast<size_t>(b) * kTracePoints + point] = gtimer();
+    };
+    if (tid == 0) mark(0);
 
     // ---------------------------------------------------------------- P1: logits
+    // This CTA's experts are e = b, b + G, ...; with the token rows they are
+    // staged in shared memory by bulk copies (one round trip), then warp j
+    // computes the logits of expert b + j*G for every token.
+    const unsigned char* xsrc = reinterpret_cast<const unsigned char*>(a.hidden);
     {
-        const unsigned char* xsrc = reinterpret_cast<const unsigned char*>(a.hidden);
-        if (geo.stage_x) {
-            const size_t n16 = static_cast<size_t>(T) * H * esz / 16;
-            for (size_t i = tid; i < n16; i += kThreads)
-                reinterpret_cast<uint4*>(ring)[i] = __ldg(reinterpret_cast<const uint4*>(xsrc) + i);
+        const uint32_t xbytes = static_cast<uint32_t>(T) * H * static_cast<uint32_t>(esz);
+        const uint32_t rbytes = static_cast<uint32_t>(H) * static_cast<uint32_t>(esz);
+        const int nexp = b < E ? (E - 1 - b) / G + 1 : 0;
+        const bool staged = geo.stage_x != 0;  // token rows and this CTA's router rows fit (host-checked)
+        if (staged && tid == 0) {
+            mbar_expect_tx(&p1bar, xbytes + static_cast<uint32_t>(nexp) * rbytes);
+            bulk_g2s(ring, a.hidden, xbytes, &p1bar);
+            for (int j = 0; j < nexp; ++j)
+                bulk_g2s(ring + xbytes + static_cast<size_t>(j) * rbytes,
+                         reinterpret_cast<const unsigned char*>(a.router_w) + static_cast<size_t>(b + j * G) * rbytes,
+                         rbytes, &p1bar);
+        }
+        // this layer's table row before anything of this call changes it: CTA 0
+        // rewrites entries of missed experts after the barrier below
+        for (int e = tid; e < E; e += kThreads) R.trow[e] = __ldcg(a.table + static_cast<size_t>(a.layer) * E + e);
+        if (staged) {
+            if (!mbar_wait(&p1bar, 0, abort_flag, a.wait_ns)) atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_PRODUCER);
             xsrc = ring;
         }
-        if (b == 0 && tid < kDecodeMaxT) a.hmax[tid] = 0u;  // read after the phase-1 barrier only
         __syncthreads();
-        // row maxima of the token rows (every CTA, from its own copy)
-        {
-            for (int t = 0; t < T; ++t) {
-                float m = 0.f;
-                for (int i = tid; i < H; i += kThreads) {
-                    const size_t o = static_cast<size_t>(t) * H + i;
-                    const float v = ACT == ACT_BF16
-                                        ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(xsrc)[o]) << 16)
-                                        : reinterpret_cast<const float*>(xsrc)[o];
-                    m = fmaxf(m, fabsf(v));
+        // row maxima of the token rows (every CTA, from its own copy): warp t, token t
+        if (warp < T) {
+            const int t = warp;
+            float m = 0.f;
+            for (int i = 8 * lane; i < H; i += 8 * 32) {
+                float v[8];
+                const size_t o = static_cast<size_t>(t) * H + i;
+                if constexpr (ACT == ACT_BF16) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(xsrc) + o);
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        v[2 * jj] = __uint_as_float(wd[jj] << 16);
+                        v[2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
+                    }
+                } else {
+                    const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xsrc) + o);
+                    const float4 p0 = f[0], p1 = f[1];
+                    v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+                    v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
                 }
-                const unsigned int mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-                if (lane == 0 && mb) atomicMax(&R.xmax[t], mb);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) m = fmaxf(m, fabsf(v[jj]));
             }
+            const unsigned int mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+            if (lane == 0) R.xmax[t] = mb;
         }
-        // router logits: warp w of CTA b takes experts b*9 + w, + 9G, ...
-        for (int e = b * kWarps + warp; e < E; e += G * kWarps) {
+        // router logits in the fixed order: lane l accumulates chunks l, l+32, ...
+        // of 8 elements with fused multiply-adds, then the xor butterfly
+        const int nchunk = H / 8;
+        for (int j = warp; j < nexp; j += kWarps) {
+            const int e = b + j * G;
+            const unsigned char* wrow = staged ? ring + xbytes + static_cast<size_t>(j) * rbytes
+                                               : reinterpret_cast<const unsigned char*>(a.router_w) + static_cast<size_t>(e) * rbytes;
             float acc[kDecodeMaxT];
 #pragma unroll
             for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
-            const int nchunk = H / 8;
-            for (int cb = lane; cb < nchunk; cb += 32 * 4) {
-                float wv[4][8];
+            for (int c = lane; c < nchunk; c += 32) {
+                float wv[8];
+                if constexpr (ACT == ACT_BF16) {
+                    const uint4 u = staged ? *reinterpret_cast<const uint4*>(wrow + 16 * c)
+                                           : __ldg(reinterpret_cast<const uint4*>(wrow + 16 * c));
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = cb + 32 * i;
-                    if (c < nchunk) {
-                        const size_t o = static_cast<size_t>(e) * H + 8 * c;
+                    for (int jj = 0; jj < 4; ++jj) {
+                        wv[2 * jj] = __uint_as_float(wd[jj] << 16);
+                        wv[2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
+                    }
+                } else {
+                    const float4* f = reinterpret_cast<const float4*>(wrow + 32 * c);
+                    const float4 p0 = staged ? f[0] : __ldg(f), p1 = staged ? f[1] : __ldg(f + 1);
+                    wv[0] = p0.x; wv[1] = p0.y; wv[2] = p0.z; wv[3] = p0.w;
+                    wv[4] = p1.x; wv[5] = p1.y; wv[6] = p1.z; wv[7] = p1.w;
+                }
+#pragma unroll
+                for (int t = 0; t < kDecodeMaxT; ++t) {
+                    if (t < T) {
+                        const size_t o = static_cast<size_t>(t) * H + 8 * c;
+                        float xv[8];
                         if constexpr (ACT == ACT_BF16) {
-                            const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.router_w) + o));
+                            const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(xsrc) + o);
                             const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int jj = 0; jj < 4; ++jj) {
-                                wv[i][2 * jj] = __uint_as_float(wd[jj] << 16);
-                                wv[i][2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
+                                xv[2 * jj] = __uint_as_float(wd[jj] << 16);
+                                xv[2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
                             }
                         } else {
-                            const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.router_w) + o);
-                            const float4 p0 = __ldg(f), p1 = __ldg(f + 1);
-                            wv[i][0] = p0.x; wv[i][1] = p0.y; wv[i][2] = p0.z; wv[i][3] = p0.w;
-                            wv[i][4] = p1.x; wv[i][5] = p1.y; wv[i][6] = p1.z; wv[i][7] = p1.w;
+                            const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xsrc) + o);
+                            const float4 p0 = f[0], p1 = f[1];
+                            xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
+                            xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
                         }
-                    }
-                }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = cb + 32 * i;
-                    if (c >= nchunk) break;
-#pragma unroll
-                    for (int t = 0; t < kDecodeMaxT; ++t) {
-                        if (t < T) {
-                            const size_t o = static_cast<size_t>(t) * H + 8 * c;
-                            float xv[8];
-                            if constexpr (ACT == ACT_BF16) {
-                                const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(xsrc) + o);
-                                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                                for (int jj = 0; jj < 4; ++jj) {
-                                    xv[2 * jj] = __uint_as_float(wd[jj] << 16);
-                                    xv[2 * jj + 1] = __uint_as_float(wd[jj] & 0xFFFF0000u);
-                                }
-                            } else {
-                                const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(xsrc) + o);
-                                const float4 p0 = f[0], p1 = f[1];
-                                xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
-                                xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
-                            }
-#pragma unroll
-                            for (int jj = 0; jj < 8; ++jj) acc[t] = __fmaf_rn(xv[jj], wv[i][jj], acc[t]);
-                        }
+                        for (int jj = 0; jj < 8; ++jj) acc[t] = __fmaf_rn(xv[jj], wv[jj], acc[t]);
                     }
                 }
             }
@@ -618,7 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             }
         }
         __syncthreads();
-        if (tid == 0) R.ok = grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+        if (tid == 0) {
+            mark(1);
+            grid_arrive(a, b, epoch0);
+        }
+        if (warp == 0) {
+            const bool ok = grid_wait(a, 0, G, epoch0, MOE_DEVERR_TIMEOUT_EPILOGUE);
+            if (lane == 0) {
+                R.ok = ok ? 1 : 0;
+                mark(2);
+            }
+        }
         __syncthreads();
     }
     if (!R.ok) return;  // every CTA gives up the same way; nothing is in flight
@@ -634,9 +686,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         }
     }
     __syncthreads();
+    // stable order by expert: row of assignment i = #{j : e_j < e_i or (e_j == e_i and j < i)}
+    int my_first = 0;
     for (int i = tid; i < n; i += kThreads) {
         const int e = R.tk[i];
         int rk = 0, first = 1;
+#pragma unroll 16
         for (int j2 = 0; j2 < n; ++j2) {
             const int f = R.tk[j2];
             rk += (f < e) || (f == e && j2 < i);
@@ -645,23 +700,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         R.rank[i] = rk;
         R.first[i] = first;
         R.rowtok[rk] = i / k;
+        my_first += first;
     }
-    __syncthreads();
+    const int nu = __syncthreads_count(my_first);  // n <= 256 < threads: one assignment per thread
     for (int i = tid; i < n; i += kThreads) {
         const int e = R.tk[i];
         int u = 0;
+#pragma unroll 16
         for (int j2 = 0; j2 < n; ++j2) u += R.first[j2] && R.tk[j2] < e;
         R.uidx[i] = u;
         if (R.first[i]) R.members[u] = e;
     }
     if (tid == 0) {
-        int nu = 0;
-        for (int i = 0; i < n; ++i) nu += R.first[i];
         R.nu = nu;
         R.status = nu > a.S ? -4 : 0;  // MOE_ERR_CAPACITY: the call leaves the cache as it was
     }
     __syncthreads();
-    const int nu = R.nu;
     const int na = nu + ns;
     for (int u = tid; u < na; u += kThreads) {
         DecExpert& d = plan[u];
@@ -672,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         }
         d.cnt = 0;
         if (u < nu) {
-            const int s = __ldcg(a.table + static_cast<size_t>(a.layer) * E + R.members[u]);
+            const int s = R.trow[R.members[u]];
             R.mslot[u] = s;
             R.hit[u] = s >= 0 ? 1 : 0;
             d.ptr = s >= 0 ? a.pool + static_cast<size_t>(s) * B : nullptr;
@@ -692,13 +746,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     __syncthreads();
     for (int i = tid; i < n; i += kThreads)
         if (R.first[i]) plan[R.uidx[i]].row0 = R.rank[i];
-    if (tid == 0) {
-        int r = 0;
-        for (int p = 0; p < nu; ++p)
-            if (!R.hit[p]) R.missr[r++] = p;
-        R.n_miss = r;
-    }
-    __syncthreads();
+    // the r-th missed member, in member order
+    for (int p = tid; p < nu; p += kThreads)
+        if (!R.hit[p]) {
+            int r = 0;
+#pragma unroll 16
+            for (int p2 = 0; p2 < p; ++p2) r += !R.hit[p2];
+            R.missr[r] = p;
+        }
+    const int n_miss_all = __syncthreads_count(tid < nu && !R.hit[tid]);
+    if (tid == 0) R.n_miss = n_miss_all;
     for (int i = tid; i < n; i += kThreads) {
         DecExpert& d = plan[R.uidx[i]];
         const int t = i / k, nn = R.rank[i] - d.row0;
@@ -710,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     __syncthreads();
     const int n_miss = R.n_miss;
     const bool capacity_err = R.status != 0;
+    if (tid == 0) mark(3);
 
     // ---------------------------------------------------------------- P2b: CTA 0 updates the cache
     CallInfo* info = a.info;
@@ -796,6 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             write_record(0, 0ull);
         }
         __syncthreads();
+        if (tid == 0) mark(4);
     }
     if (capacity_err) return;
 
@@ -857,7 +916,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             // the bulk copies (async proxy) of every CTA read these bytes next
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncthreads();
-            if (tid == 0) R.ok = grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_PRODUCER) ? 1 : 0;
+            if (tid == 0) grid_arrive(a, b, epoch1);
+            if (warp == 0) {
+                const bool ok = grid_wait(a, 0, G, epoch1, MOE_DEVERR_TIMEOUT_PRODUCER);
+                if (lane == 0) R.ok = ok ? 1 : 0;
+            }
             __syncthreads();
             if (!R.ok) return;
             if (b == 0) {
@@ -868,6 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         __syncthreads();
     }
 
+    if (tid == 0) mark(5);
     // ---------------------------------------------------------------- P3: experts
     StageSeq<FMT> seq;
     seq.init(a, plan, na, b, G);
@@ -957,30 +1021,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                 phase ^= 1u;
             }
         };
-        // this warp's partial of a finished tile into the stage's slot; true for the
-        // warp that arrives last (it then holds the tile's sum in v, in warp order)
+        // this warp's partial of finished tile number ti (counted over both
+        // phases) into reduction slot ti mod kRedSlots, once that slot's previous
+        // tile has been summed (bounded wait); true for the warp that arrives
+        // last, which then holds the tile's sum in v, in warp order. The caller
+        // has already released the tile's stages, so the weight stream goes on.
+        int ti = 0;
         auto tile_reduce = [&](const float (&acc)[4], float (&v)[4]) -> bool {
-            float* slot = red + stage * (kConsumers * 32 * 4);
-            *reinterpret_cast<float4*>(slot + (w * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            const int slot = ti % kRedSlots, use = ti / kRedSlots;
+            ++ti;
+            float* sl = red + slot * (kConsumers * 32 * 4);
+            volatile int32_t* gen = &R.red_gen[slot];
+            if (*gen != use) {
+                const uint64_t t0 = gtimer();
+                while (*gen != use) {
+                    if (gtimer() - t0 > a.wait_ns) {
+                        dead = true;
+                        atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_EPILOGUE);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+            *reinterpret_cast<float4*>(sl + (w * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             __threadfence_block();
             __syncwarp();
             int last = 0;
-            if (lane == 0) last = atomicAdd(&R.red_cnt[stage], 1) == kConsumers - 1;
+            if (lane == 0) last = atomicAdd(&R.red_cnt[slot], 1) == kConsumers - 1;
             last = __shfl_sync(0xffffffffu, last, 0);
             if (!last) return false;
             __threadfence_block();
             v[0] = v[1] = v[2] = v[3] = 0.f;
 #pragma unroll
             for (int y = 0; y < kConsumers; ++y) {
-                const float4 p = *reinterpret_cast<const float4*>(slot + (y * 32 + lane) * 4);
+                const float4 p = *reinterpret_cast<const float4*>(sl + (y * 32 + lane) * 4);
                 v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
             }
-            if (lane == 0) R.red_cnt[stage] = 0;
+            __syncwarp();
+            if (lane == 0) {
+                R.red_cnt[slot] = 0;
+                __threadfence_block();
+                *gen = use + 1;  // the slot is free for tile ti + kRedSlots
+            }
             return true;
         };
         // ---------------- phase 1: gate/up + SwiGLU
         {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[4][4] = {};  // four independent chains: (chunk half, even/odd step)
             for (int f = 0; f < nf1; ++f) {
                 int u, ut, c0, nc;
                 seq.where1(f, u, ut, c0, nc);
@@ -997,13 +1084,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                             uint32_t bq[16];
                             if (geo.act_bytes) load_b_smem(act, xp, tok, j, q, bq);
                             else load_b_xglobal<ACT>(a.hidden, H, tok, j, q, tok >= 0 ? R.xsc[tok] : 1.f, bq);
-                            mma_group<FMT>(st + half * C::kChunkBytes, ng, w, g, q, bq, acc);
+                            mma_group<FMT>(st + half * C::kChunkBytes, ng, w, g, q, bq, acc[2 * half], acc[2 * half + 1]);
                         }
                     }
                 }
+                release();
                 if ((f % seq.ns1) == seq.ns1 - 1) {
-                    float v[4];
-                    if (tile_reduce(acc, v)) {
+                    float v[4], part[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) part[x] = ((acc[0][x] + acc[1][x]) + acc[2][x]) + acc[3][x];
+                    if (tile_reduce(part, v)) {
 #pragma unroll
                         for (int h2 = 0; h2 < 2; ++h2) {
                             const int nn = 2 * q + h2;
@@ -1020,20 +1110,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                             }
                         }
                     }
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) acc[y][0] = acc[y][1] = acc[y][2] = acc[y][3] = 0.f;
                 }
-                release();
             }
         }
-        // ---------------- barrier: every h row of the call is written
+        // ---------------- barrier: every h row of the call is written (workers only)
         consumer_sync();
-        if (ct < T && R.hmax[ct]) atomicMax(&a.hmax[ct], R.hmax[ct]);
-        consumer_sync();
-        if (ct == 0) R.ok = (!*abort_flag && grid_arrive_wait(a, G, MOE_DEVERR_TIMEOUT_EPILOGUE)) ? 1 : 0;
-        consumer_sync();
-        if (!R.ok) *abort_flag = 1;
-        if (ct < T) pow2_scale(__ldcg(&a.hmax[ct]), R.hsc[ct], R.hun[ct]);
-        consumer_sync();
+        if (ct == 0) mark(6);
+        if (b != 0) {
+            // this CTA's largest |h| per token, then the barrier, then the maxima of all workers
+            if (ct < kDecodeMaxT) a.hmax[static_cast<size_t>(b) * kDecodeMaxT + ct] = R.hmax[ct];
+            consumer_sync();
+            if (ct == 0) grid_arrive(a, b, epoch2);
+            if (w == 0) {
+                const bool ok = !*abort_flag && grid_wait(a, 1, G, epoch2, MOE_DEVERR_TIMEOUT_EPILOGUE);
+                if (lane == 0) R.ok = ok ? 1 : 0;
+            }
+            consumer_sync();
+            if (!R.ok) *abort_flag = 1;
+            if (w < T) {
+                unsigned int mx = 0u;
+                for (int c2 = 1 + lane; c2 < G; c2 += 32)
+                    mx = max(mx, __ldcg(a.hmax + static_cast<size_t>(c2) * kDecodeMaxT + w));
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                if (lane == 0) pow2_scale(mx, R.hsc[w], R.hun[w]);
+            }
+            if (ct == 0) mark(7);
+            consumer_sync();
+        }
         // ---------------- phase 2: down projection + combine
         if (nf2 > 0) {
             const int hrows = n + ns * T;
@@ -1083,14 +1188,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                         uint32_t bq[16];
                         if (geo.act_bytes) load_b_smem(act, hp, hr, j, q, bq);
                         else load_b_hglobal(hb, I, hr, j, q, R.hsc[g < T ? g : 0], bq);
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_group<FMT>(st + off, ng, ww, g, q, bq, d);
+                        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_group<FMT>(st + off, ng, ww, g, q, bq, d0, d1);
                         const float gsd = plan[u].gs[2];
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) acc[x] = __fmaf_rn(gsd, d[x], acc[x]);
+                        for (int x = 0; x < 4; ++x) acc[x] = __fmaf_rn(gsd, d0[x] + d1[x], acc[x]);
                     }
                 }
-                if (seq.count2() && ((f % seq.ns2) == seq.ns2 - 1)) {
+                release();
+                if ((f % seq.ns2) == seq.ns2 - 1) {
                     float v[4];
                     if (tile_reduce(acc, v)) {
                         const int r0 = rt * kTileRows;
@@ -1112,11 +1218,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                     }
                     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
                 }
-                release();
             }
         }
+        consumer_sync();
+        if (ct == 0) mark(8);
     }
     __syncthreads();
+    if (tid == 0) mark(9);
 }
 
 template <int FMT>
@@ -1138,7 +1246,7 @@ size_t lru_need(const CallArgs& a, int* trow_off, int* keys_off, int* cache_off,
 }
 
 template <int FMT>
-bool geometry(const CallArgs& a, DecGeom& g) {
+bool geometry(const CallArgs& a, int grid, DecGeom& g) {
     const int T = a.T, H = a.H, I = a.I, k = a.k, ns = a.n_shared;
     const size_t esz = a.act == ACT_BF16 ? 2 : 4;
     g.max_active = std::min(a.E, T * k) + ns;
@@ -1148,25 +1256,28 @@ bool geometry(const CallArgs& a, DecGeom& g) {
     o = (o + 127) / 128 * 128;
     g.ring_off = static_cast<int>(o);
     const size_t fixed = o;
-    const size_t per_stage = Fp4Cfg<FMT>::kStageBytes + kRedSlotBytes;
+    const size_t stage = Fp4Cfg<FMT>::kStageBytes;
+    const size_t red = static_cast<size_t>(kRedSlots) * kRedSlotBytes;
     const size_t act_need = std::max(static_cast<size_t>(T) * (H * 2 + 16),
                                      static_cast<size_t>(T) * (k + ns) * (I * 2 + 16));
-    const size_t x_stage = static_cast<size_t>(T) * H * esz;
+    // P1 stages the token rows and this CTA's router rows at ring_off
+    const size_t rows_per_cta = (static_cast<size_t>(a.E) + grid - 1) / grid;
+    const size_t p1_stage = static_cast<size_t>(T) * H * esz + rows_per_cta * H * esz;
     int to, ko, co;
     const size_t lru_end = lru_need<FMT>(a, &to, &ko, &co, static_cast<int>(fixed));
+    if (lru_end > static_cast<size_t>(kSmemLimit)) return false;
     for (int with_act = 1; with_act >= 0; --with_act) {
         const size_t actb = with_act ? (act_need + 127) / 128 * 128 : 0;
-        if (fixed + actb + 2 * per_stage > static_cast<size_t>(kSmemLimit)) continue;
-        int nst = static_cast<int>((kSmemLimit - fixed - actb) / per_stage);
+        if (fixed + red + actb + 2 * stage > static_cast<size_t>(kSmemLimit)) continue;
+        int nst = static_cast<int>((kSmemLimit - fixed - red - actb) / stage);
         nst = std::min(nst, kMaxStages);
-        const size_t ring_end = fixed + static_cast<size_t>(nst) * per_stage + actb;
-        if (lru_end > static_cast<size_t>(kSmemLimit)) return false;
         g.nst = nst;
         g.act_bytes = static_cast<int>(actb);
-        g.red_off = static_cast<int>(fixed + static_cast<size_t>(nst) * Fp4Cfg<FMT>::kStageBytes);
-        g.act_off = static_cast<int>(fixed + static_cast<size_t>(nst) * per_stage);
+        g.red_off = static_cast<int>(fixed + static_cast<size_t>(nst) * stage);
+        g.act_off = static_cast<int>(g.red_off + red);
+        const size_t ring_end = g.act_off + actb;
         g.total = static_cast<int>(std::max(ring_end, lru_end));
-        g.stage_x = fixed + x_stage <= static_cast<size_t>(g.total) ? 1 : 0;
+        g.stage_x = fixed + p1_stage <= static_cast<size_t>(g.total) && p1_stage < (1u << 20) ? 1 : 0;
         g.lru_trow_off = to;
         g.lru_keys_off = ko;
         g.lru_cache_off = co;
@@ -1179,7 +1290,7 @@ template <int FMT, int ACT>
 cudaError_t launch_one(const CallArgs& a, int grid, cudaStream_t s, bool pdl) {
     DecGeom geo{};
     if (grid < 2) return cudaErrorInvalidValue;  // CTA 0 runs the cache update beside the others' work
-    if (!geometry<FMT>(a, geo)) return cudaErrorInvalidValue;
+    if (!geometry<FMT>(a, grid, geo)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

@@ -113,6 +113,12 @@ struct DecExpert {
 static_assert(sizeof(DecExpert) == 128, "decode plan record");
 constexpr int kDecPlanHeader = 128;
 
+// phase marks the decode kernel records per CTA when a trace buffer is given
+// (MOE_TRACE): start, logits written, barrier 1 passed, plan done, cache
+// updated (CTA 0), misses copied, phase 1 done, barrier 2 passed, phase 2
+// done, end
+constexpr int kTracePoints = 10;
+
 // Published by the CTA of the fused decode kernel that runs the cache lookup,
 // for the kernel's other CTAs: the pool slots chosen for the call's misses (in
 // the ascending order of the missed experts), valid once seq equals the call's
@@ -160,7 +166,7 @@ struct CallArgs {
     int32_t* baseT;        // [E][nb] rows of expert e before CTA b's (exclusive scan over b)
     int16_t* lrank;        // [T*k] rank of assignment a among its CTA's assignments to the same expert
     int nb_max;            // column stride of cntT / baseT
-    unsigned int* grid_bar;  // [2] grid barrier of the decode expert kernel: arrivals, generation
+    unsigned long long* grid_flags;  // [CTAs] barrier epoch each decode CTA has reached
     unsigned char* dplan;  // decode plan: header + (E + n_shared) records
     int32_t* n_uniq;       // [1]
     int32_t* n_active;     // [1]
@@ -185,9 +191,10 @@ struct CallArgs {
     // fused decode (FP4 weights, T <= 8)
     const uint8_t* const* banks;  // [L] device views of the mapped pinned host banks
     float* xmax;           // [8] max |x| of each token row (this call)
-    unsigned int* hmax;    // [8] max |h| (float bits) of each token's intermediate rows
+    unsigned int* hmax;    // [CTAs][8] each decode CTA's max |h| (float bits) per token
     DecPub* pub;           // miss slots for the kernel's CTAs
     int device_misses;     // 1: the decode kernel copies its misses itself; 0: the host does
+    unsigned long long* trace;  // optional [CTAs][kTracePoints] %globaltimer marks of the decode kernel
 };
 
 // Bounded wait of the expert kernels for their call's weights (one thread);

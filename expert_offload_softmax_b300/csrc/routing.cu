@@ -550,6 +550,8 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
             info->n_hit = info->n_miss = info->n_pf = info->n_pf_hit = info->n_pf_miss = 0;
             info->n_events = 0;
             info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
+            info->device_copied = 0;
+            info->copy_ns = 0;
             info->status = -4;  // MOE_ERR_CAPACITY
             *a.n_active = 0;
             if (decode) *reinterpret_cast<int32_t*>(a.dplan) = 0;
@@ -645,6 +647,8 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         info->n_pf_miss = m_pf;
         info->n_events = nu + n_pf;
         info->dev_err = *reinterpret_cast<volatile int32_t*>(a.dev_err);
+        info->device_copied = 0;  // this call's misses are the host's to copy
+        info->copy_ns = 0;
         info->status = 0;
         if (a.self_release && m == 0) *a.ready = a.seq;
         __threadfence_system();

@@ -115,6 +115,8 @@ struct moe_handle {
     // kernels run into their bounded wait
     bool fault_drop_release = false;
     bool log = false;  // MOE_LOG: one stderr line per serviced call
+    unsigned long long* trace = nullptr;  // MOE_TRACE: the decode kernel's per-CTA phase marks
+    bool last_fused = false;
     // streams / events
     // miss copies alternate between two copy streams (the copy engines overlap
     // one copy's setup with another's transfer); `copy` joins `copy2` before
@@ -659,6 +661,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     h->lay = layout_for(h->d);
     if (const char* f = std::getenv("MOE_FAULT")) h->fault_drop_release = std::strcmp(f, "drop_release") == 0;
     h->log = std::getenv("MOE_LOG") != nullptr;
+    const bool want_trace = std::getenv("MOE_TRACE") != nullptr;
     if (const char* w = std::getenv("MOE_WAIT_MS")) {
         const long ms = std::strtol(w, nullptr, 10);
         if (ms > 0) h->wait_ns = static_cast<unsigned long long>(ms) * 1000000ull;
@@ -721,9 +724,9 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E) * nb_max * 2, reinterpret_cast<void**>(&a.cntT)},
         {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
         {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
-        {8, reinterpret_cast<void**>(&a.grid_bar)},
+        {static_cast<size_t>(h->num_sms) * 8, reinterpret_cast<void**>(&a.grid_flags)},
         {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.xmax)},
-        {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
+        {static_cast<size_t>(h->num_sms) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
         {sizeof(moe::DecPub), reinterpret_cast<void**>(&a.pub)},
         {static_cast<size_t>(L) * 8, reinterpret_cast<void**>(const_cast<uint8_t***>(&a.banks))},
         {moe::kDecPlanHeader + static_cast<size_t>(E + ns) * sizeof(moe::DecExpert), reinterpret_cast<void**>(&a.dplan)},
@@ -743,6 +746,12 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         off += align_up(p.bytes, 256);
     }
     h->ready = a.ready;
+    if (want_trace) {
+        if (cudaMalloc(&h->trace, static_cast<size_t>(h->num_sms) * moe::kTracePoints * 8) != cudaSuccess)
+            return bail(MOE_ERR_OOM);
+        cudaMemset(h->trace, 0, static_cast<size_t>(h->num_sms) * moe::kTracePoints * 8);
+        a.trace = h->trace;
+    }
     if (umma) {
         // TMA descriptors over the gathered activations, h, and the resident shared experts
         bool ok = moe::umma_map_2d(&h->maps.x, a.xperm, rows, H, 128) && moe::umma_map_2d(&h->maps.h, a.hbuf, rows, I, 128);
@@ -908,7 +917,7 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* po
     CK(h, cudaMemset(h->clock, 0, 8));
     CK(h, cudaMemset(h->base.dev_err, 0, 4));
     CK(h, cudaMemset(h->base.route_done, 0, 4));
-    CK(h, cudaMemset(h->base.grid_bar, 0, 8));
+
     // the ready word continues from the last serviced call
     const unsigned long long rv = h->submitted;
     CK(h, cudaMemcpy(h->ready, &rv, 8, cudaMemcpyHostToDevice));
@@ -1062,6 +1071,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     }
     CallInfo* rec = h->info_h + (seq % kRing);
     reinterpret_cast<volatile unsigned long long*>(&rec->done)[0] = 0;
+    reinterpret_cast<volatile int32_t*>(&rec->device_copied)[0] = 0;
     CallArgs a = h->base;
     a.T = T;
     a.layer = layer_id;
@@ -1105,6 +1115,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         }
         h->submitted = seq;
         h->prefetch_may_be_pending = false;
+        h->last_fused = true;
         h->last_T = T;
         h->last_stream = s;
         {
@@ -1135,6 +1146,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     // record is consumed in order
     h->submitted = seq;
     h->prefetch_may_be_pending = want_pf;
+    h->last_fused = false;
     h->last_T = T;
     h->last_stream = s;
     {
@@ -1192,6 +1204,30 @@ int moe_sync(moe_handle* h) {
     if (dev_err != 0)
         record_error(h, MOE_ERR_TIMEOUT, "a kernel gave up a bounded wait (device error " + std::to_string(dev_err) +
                                              "); call moe_cache_config to reset");
+    if (h->trace && h->last_fused) {
+        // the last decode call's phase marks: min / median / max over CTAs, in us after the first start
+        const int G = h->num_sms, P = moe::kTracePoints;
+        std::vector<unsigned long long> t(static_cast<size_t>(G) * P);
+        CK(h, cudaMemcpy(t.data(), h->trace, t.size() * 8, cudaMemcpyDeviceToHost));
+        unsigned long long t0 = ~0ull;
+        for (int b = 0; b < G; ++b)
+            if (t[static_cast<size_t>(b) * P]) t0 = std::min(t0, t[static_cast<size_t>(b) * P]);
+        std::string line = "[moe] trace T=" + std::to_string(h->last_T);
+        for (int p = 0; p < P; ++p) {
+            std::vector<double> v;
+            for (int b = 0; b < G; ++b) {
+                const unsigned long long x = t[static_cast<size_t>(b) * P + p];
+                if (x >= t0) v.push_back((x - t0) * 1e-3);
+            }
+            if (v.empty()) continue;
+            std::sort(v.begin(), v.end());
+            char buf[96];
+            std::snprintf(buf, sizeof(buf), " p%d=%.2f/%.2f/%.2f", p, v.front(), v[v.size() / 2], v.back());
+            line += buf;
+        }
+        std::fprintf(stderr, "%s\n", line.c_str());
+        CK(h, cudaMemset(h->trace, 0, t.size() * 8));
+    }
     return take_error(h);
 }
 
@@ -1285,6 +1321,7 @@ void moe_destroy(moe_handle* h) {
         if (b) cudaFreeHost(b);
     cudaFree(h->shared_dev);
     cudaFree(h->scratch);
+    cudaFree(h->trace);
     if (h->info_h) cudaFreeHost(h->info_h);
     if (h->ready_vals) cudaFreeHost(h->ready_vals);
     if (h->stream) cudaStreamDestroy(h->stream);
