@@ -155,46 +155,35 @@ __device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory"); }
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
-// Grid-wide barriers without a shared counter: CTA b announces that it has
-// reached barrier `epoch` by storing epoch into its own flag (a release store
-// that publishes the CTA's writes), and a CTA passes the barrier once the
-// flags of all participating CTAs [first, last) hold at least epoch (one warp
-// polls them, coalesced, with acquire loads; bounded). Epochs grow with the
-// call's sequence number, so no flag is ever reset.
-__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void grid_arrive(const CallArgs& a, int b, unsigned long long epoch) {
-    __threadfence();
-    st_release_gpu_u64(a.grid_flags + b, epoch);
-}
-
 __device__ __forceinline__ unsigned long long ld_relaxed_gpu64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ void red_release_add64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
-// called by a whole warp; true once every flag in [first, last) >= epoch. The
-// polls are relaxed loads, all in flight together; the acquire fence after the
-// last poll orders what the CTA reads next after every participant's release.
-__device__ bool grid_wait(const CallArgs& a, int first, int last, unsigned long long epoch, int err_code) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t t0 = gtimer();
-    for (;;) {
-        bool mine = true;
-#pragma unroll 8
-        for (int i = first + lane; i < last; i += 32) mine &= ld_relaxed_gpu64(a.grid_flags + i) >= epoch;
-        if (__all_sync(0xffffffffu, mine)) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            return true;
-        }
-        if (gtimer() - t0 > a.wait_ns) {
-            if (lane == 0) atomicExch(a.dev_err, err_code);
-            return false;
+// Grid-wide barriers on monotone arrival counters (never reset between calls):
+// barrier k of a call has P participants, and every decode call adds exactly P
+// to counter k (a call that skips the barrier adds the missing arrivals in one
+// step), so the call's target is (calls before it + 1) * P, which the host
+// passes. Arriving is a release add (it publishes the CTA's writes); waiting
+// is one thread polling with relaxed loads, then an acquire fence.
+__device__ __forceinline__ void bar_arrive(unsigned long long* cnt, unsigned long long n) { red_release_add64(cnt, n); }
+
+__device__ bool bar_wait(const CallArgs& a, const unsigned long long* cnt, unsigned long long target, int err_code) {
+    if (ld_relaxed_gpu64(cnt) < target) {
+        const uint64_t t0 = gtimer();
+        while (ld_relaxed_gpu64(cnt) < target) {
+            if (gtimer() - t0 > a.wait_ns) {
+                atomicExch(a.dev_err, err_code);
+                return false;
+            }
         }
     }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return true;
 }
 
 // power of two p with max|v| * p in [2^14, 2^15) (1 for 0 or non-finite), and 1/p
@@ -492,8 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
     const size_t B = a.lay.bytes;
     volatile int* abort_flag = &s_abort;
-    // the call's grid barriers: logits written / misses copied / h written
-    const unsigned long long epoch0 = a.seq * 4ull, epoch1 = epoch0 + 1, epoch2 = epoch0 + 2;
+    // the call's grid barriers: logits written (all CTAs), misses copied (all
+    // CTAs), h written (workers 1..G-1)
+    const unsigned long long tgt0 = (a.dcall + 1) * static_cast<unsigned long long>(G);
+    const unsigned long long tgt2 = (a.dcall + 1) * static_cast<unsigned long long>(G - 1);
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -549,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             xsrc = ring;
         }
         __syncthreads();
+        if (tid == 0) mark(10);
         // row maxima of the token rows (every CTA, from its own copy): warp t, token t
         if (warp < T) {
             const int t = warp;
@@ -637,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         }
         __syncthreads();
         // activation scales; token rows -> f16 device order in smem (CTAs with phase-1 work)
+        if (tid == 0) mark(11);
         if (tid < kDecodeMaxT) pow2_scale(R.xmax[tid], R.xsc[tid], R.xun[tid]);
         __syncthreads();
         if (geo.act_bytes && b != 0) {
@@ -662,14 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         __syncthreads();
         if (tid == 0) {
             mark(1);
-            grid_arrive(a, b, epoch0);
-        }
-        if (warp == 0) {
-            const bool ok = grid_wait(a, 0, G, epoch0, MOE_DEVERR_TIMEOUT_EPILOGUE);
-            if (lane == 0) {
-                R.ok = ok ? 1 : 0;
-                mark(2);
-            }
+            bar_arrive(a.bar_cnt, 1);
+            R.ok = bar_wait(a, a.bar_cnt, tgt0, MOE_DEVERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+            mark(2);
         }
         __syncthreads();
     }
@@ -686,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         }
     }
     __syncthreads();
+    if (tid == 0) mark(12);
     // stable order by expert: row of assignment i = #{j : e_j < e_i or (e_j == e_i and j < i)}
     int my_first = 0;
     for (int i = tid; i < n; i += kThreads) {
@@ -793,6 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             info->done = a.seq;
         }
     };
+    if (b == 0 && tid == 0) {
+        // barriers this call will not hold still count their participants
+        const bool holds_copy_barrier = !capacity_err && n_miss > 0 && a.device_misses;
+        if (!holds_copy_barrier) bar_arrive(a.bar_cnt + 1, static_cast<unsigned long long>(G));
+        if (capacity_err) bar_arrive(a.bar_cnt + 2, static_cast<unsigned long long>(G - 1));
+    }
     if (b == 0) {
         // routing results for moe_debug_routing
         for (int i = tid; i < n; i += kThreads) {
@@ -916,10 +911,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             // the bulk copies (async proxy) of every CTA read these bytes next
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncthreads();
-            if (tid == 0) grid_arrive(a, b, epoch1);
-            if (warp == 0) {
-                const bool ok = grid_wait(a, 0, G, epoch1, MOE_DEVERR_TIMEOUT_PRODUCER);
-                if (lane == 0) R.ok = ok ? 1 : 0;
+            if (tid == 0) {
+                bar_arrive(a.bar_cnt + 1, 1);
+                R.ok = bar_wait(a, a.bar_cnt + 1, tgt0, MOE_DEVERR_TIMEOUT_PRODUCER) ? 1 : 0;
             }
             __syncthreads();
             if (!R.ok) return;
@@ -1074,6 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                 const DecExpert& m = plan[u];
                 const int tok = m.tok[g];
                 const unsigned char* st = wait_full();
+                if (ct == 0 && (f == 0 || f == nf1 - 1)) mark(f == 0 ? 13 : 14);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int c = c0 + half;
@@ -1122,10 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             // this CTA's largest |h| per token, then the barrier, then the maxima of all workers
             if (ct < kDecodeMaxT) a.hmax[static_cast<size_t>(b) * kDecodeMaxT + ct] = R.hmax[ct];
             consumer_sync();
-            if (ct == 0) grid_arrive(a, b, epoch2);
-            if (w == 0) {
-                const bool ok = !*abort_flag && grid_wait(a, 1, G, epoch2, MOE_DEVERR_TIMEOUT_EPILOGUE);
-                if (lane == 0) R.ok = ok ? 1 : 0;
+            if (ct == 0) {
+                bar_arrive(a.bar_cnt + 2, 1);
+                R.ok = (bar_wait(a, a.bar_cnt + 2, tgt2, MOE_DEVERR_TIMEOUT_EPILOGUE) && !*abort_flag) ? 1 : 0;
             }
             consumer_sync();
             if (!R.ok) *abort_flag = 1;
@@ -1164,6 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                 int rt, u0, nu_, c0, nc;
                 seq.where2(f, rt, u0, nu_, c0, nc);
                 const unsigned char* st = wait_full();
+                if (ct == 0 && f == nf2 - 1) mark(15);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int gs = w + kConsumers * half;  // group slot of this stage

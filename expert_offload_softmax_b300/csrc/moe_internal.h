@@ -114,10 +114,12 @@ static_assert(sizeof(DecExpert) == 128, "decode plan record");
 constexpr int kDecPlanHeader = 128;
 
 // phase marks the decode kernel records per CTA when a trace buffer is given
-// (MOE_TRACE): start, logits written, barrier 1 passed, plan done, cache
-// updated (CTA 0), misses copied, phase 1 done, barrier 2 passed, phase 2
-// done, end
-constexpr int kTracePoints = 10;
+// (MOE_TRACE): 0 start, 1 logits written, 2 barrier 1 passed, 3 plan done,
+// 4 cache updated (CTA 0), 5 misses copied, 6 phase 1 done, 7 barrier 2
+// passed, 8 phase 2 done, 9 end; 10 token and router rows staged, 11 logits
+// computed, 12 top-k done, 13 first phase-1 stage landed, 14 last phase-1
+// stage landed, 15 last phase-2 stage landed
+constexpr int kTracePoints = 16;
 
 // Published by the CTA of the fused decode kernel that runs the cache lookup,
 // for the kernel's other CTAs: the pool slots chosen for the call's misses (in
@@ -166,7 +168,8 @@ struct CallArgs {
     int32_t* baseT;        // [E][nb] rows of expert e before CTA b's (exclusive scan over b)
     int16_t* lrank;        // [T*k] rank of assignment a among its CTA's assignments to the same expert
     int nb_max;            // column stride of cntT / baseT
-    unsigned long long* grid_flags;  // [CTAs] barrier epoch each decode CTA has reached
+    unsigned long long* bar_cnt;     // [3] arrival counters of the decode kernel's grid barriers
+    unsigned long long dcall;        // decode kernel launches before this one since the counters were reset
     unsigned char* dplan;  // decode plan: header + (E + n_shared) records
     int32_t* n_uniq;       // [1]
     int32_t* n_active;     // [1]

@@ -117,6 +117,7 @@ struct moe_handle {
     bool log = false;  // MOE_LOG: one stderr line per serviced call
     unsigned long long* trace = nullptr;  // MOE_TRACE: the decode kernel's per-CTA phase marks
     bool last_fused = false;
+    unsigned long long dcalls = 0;  // decode kernel launches since the barrier counters were reset
     // streams / events
     // miss copies alternate between two copy streams (the copy engines overlap
     // one copy's setup with another's transfer); `copy` joins `copy2` before
@@ -724,7 +725,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E) * nb_max * 2, reinterpret_cast<void**>(&a.cntT)},
         {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
         {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
-        {static_cast<size_t>(h->num_sms) * 8, reinterpret_cast<void**>(&a.grid_flags)},
+        {3 * 8, reinterpret_cast<void**>(&a.bar_cnt)},
         {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.xmax)},
         {static_cast<size_t>(h->num_sms) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
         {sizeof(moe::DecPub), reinterpret_cast<void**>(&a.pub)},
@@ -917,6 +918,8 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* po
     CK(h, cudaMemset(h->clock, 0, 8));
     CK(h, cudaMemset(h->base.dev_err, 0, 4));
     CK(h, cudaMemset(h->base.route_done, 0, 4));
+    CK(h, cudaMemset(h->base.bar_cnt, 0, 3 * 8));
+    h->dcalls = 0;
 
     // the ready word continues from the last serviced call
     const unsigned long long rv = h->submitted;
@@ -1106,9 +1109,11 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
             CK(h, cudaStreamWaitEvent(s, h->ev_pf, 0));
         }
         a.self_release = 1;
+        a.dcall = h->dcalls;
         if (tc) CK(h, cudaEventRecord(tc->r0, s));
         const cudaError_t le = moe::launch_decode(a, h->num_sms, s, true);
         if (le != cudaSuccess) return cuda_fail(h, le, "decode kernel launch");
+        h->dcalls++;
         if (tc) {
             CK(h, cudaEventRecord(tc->r1, s));
             tc->fused = true;
