@@ -269,8 +269,10 @@ def run_passes(moe, torch, h, shape, L, T, S, flags, hid, router, dev, W, K, dis
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    hw0 = time.perf_counter()
     for st in range(W, W + K):
         step(st, x_dev)
+    host_ms = (time.perf_counter() - hw0) * 1e3 / K  # enqueue time per step (host-bound if close to ms_per_step)
     ev1.record(stream)
     stream.synchronize()
     moe.moe_sync(h)
@@ -316,7 +318,7 @@ def run_passes(moe, torch, h, shape, L, T, S, flags, hid, router, dev, W, K, dis
     moe.moe_timing_enable(h, False)
     del x_dev, hid_pin, out_pin, xin
     return {"ms": ms, "e2e_ms": e2e_ms, "e2e_wall": e2e_wall, "timing": timing, "stats": stats,
-            "e2e_misses": e2e_stats["misses"], "clk": clk}
+            "e2e_misses": e2e_stats["misses"], "clk": clk, "host_ms": host_ms}
 
 
 def prefill_object(moe, torch, dev, args):
@@ -504,6 +506,7 @@ def make_line(args, world, meas, blob_bytes):
         "roofline": roof,
         "kernels_us_per_call": _kernel_us(timing),
         "h2d_copy_ms_per_step": round(timing["copy_ms"] / K, 4),
+        "host_enqueue_ms_per_step": round(meas.get("host_ms", 0.0), 4),
         "cache": {"hit_rate": round(stats["hits"] / cap_hits, 4) if cap_hits else None,
                   "misses_per_step": round(stats["misses"] / K, 3),
                   "h2d_bytes_per_step": int(stats["bytes_h2d"] // K),

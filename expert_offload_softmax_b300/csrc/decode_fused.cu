@@ -92,6 +92,7 @@ struct DecRoute {
     int32_t red_gen[kRedSlots];   // uses of each slot finished
     int32_t nu, n_miss, status, ok;
     unsigned long long t_copy0;
+    unsigned long long tks[kDecodeMaxT][32];  // top-k scratch of token t's warp
 };
 
 // dynamic shared memory carve-up, computed on the host
@@ -144,6 +145,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(su32(bar))
         : "memory");
 }
+// The same copy with an L2 eviction priority: expert weights stream through L2
+// once per call (evict first), so that they do not push out what every call
+// reuses (router rows, LRU state, the kernel's own code), which is kept with
+// evict last.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -151,6 +173,9 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned lo
 }
 __device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory"); }
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -160,8 +185,45 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu64(const unsigned lo
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// Row `src` of the tagged decode logits into dst (E floats), waiting (bounded)
+// for every entry to carry this call's sequence number: each entry is one
+// 64-bit store, so the value is read together with the tag that validates it
+// and no separate barrier is needed. False on timeout (this lane).
+__device__ __forceinline__ bool poll_logits(const unsigned long long* src, int E, uint32_t seq, float* dst, int lane,
+                                            unsigned long long wait_ns);
+
 __device__ __forceinline__ void red_release_add64(unsigned long long* p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ bool poll_logits(const unsigned long long* src, int E, uint32_t seq, float* dst, int lane,
+                                            unsigned long long wait_ns) {
+    const uint64_t t0 = gtimer();
+    for (int base = 0; base < E; base += 256) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = base + lane + 32 * i;
+            v[i] = e < E ? ld_relaxed_gpu64(src + e) : static_cast<unsigned long long>(seq) << 32;
+        }
+        for (;;) {
+            bool done = true;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (static_cast<uint32_t>(v[i] >> 32) != seq) {
+                    done = false;
+                    v[i] = ld_relaxed_gpu64(src + base + lane + 32 * i);
+                }
+            if (done) break;
+            if (gtimer() - t0 > wait_ns) return false;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = base + lane + 32 * i;
+            if (e < E) dst[e] = __uint_as_float(static_cast<uint32_t>(v[i]));
+        }
+    }
+    return true;
 }
 
 // Grid-wide barriers on monotone arrival counters (never reset between calls):
@@ -172,7 +234,7 @@ __device__ __forceinline__ void red_release_add64(unsigned long long* p, unsigne
 // is one thread polling with relaxed loads, then an acquire fence.
 __device__ __forceinline__ void bar_arrive(unsigned long long* cnt, unsigned long long n) { red_release_add64(cnt, n); }
 
-__device__ bool bar_wait(const CallArgs& a, const unsigned long long* cnt, unsigned long long target, int err_code) {
+__device__ __forceinline__ bool bar_wait(const CallArgs& a, const unsigned long long* cnt, unsigned long long target, int err_code) {
     if (ld_relaxed_gpu64(cnt) < target) {
         const uint64_t t0 = gtimer();
         while (ld_relaxed_gpu64(cnt) < target) {
@@ -348,13 +410,6 @@ __device__ __forceinline__ void load_b_hglobal(const uint16_t* hbuf, int I, int 
 
 // A pipeline stage: up to 16 K groups of 16 weight rows, made of one or more
 // contiguous pieces of the blobs (one cp.async.bulk each).
-struct Stage {
-    const uint8_t* src[kStageGroups];
-    uint32_t bytes[kStageGroups];
-    int npieces;
-    int tile_end;  // 1: last stage of its output tile
-};
-
 // The stage sequence of one CTA, identical for its producer and consumers.
 // CTA 0 runs the cache update and takes no tiles; CTA b >= 1 is worker b1 = b-1
 // of G1 = G-1.
@@ -365,18 +420,29 @@ struct Stage {
 //           else the whole tiles of several experts (16 groups at most).
 template <int FMT>
 struct StageSeq {
-    const CallArgs* a;
+    // blob offsets of the gate/up and down tiles and their strides, copied from
+    // the kernel's arguments: a load through a pointer to a kernel argument is
+    // a memory round trip, a register is not
+    size_t gu, gu_tile, d, d_tile;
     const DecExpert* plan;
-    int na, b1, G1, b, G;
-    int UT, G1k, nch1, ns1, n1, my1;  // phase 1
-    int G2k, nch2, nsu, epp, ns2, n2, my2;
+    int na, b1, G1;
+    int UT, G1k, nch1, ns1, n1, my1, G1q, G1r;  // phase 1
+    int G2k, nch2, nsu, epp, ns2, n2, my2;      // phase 2
+    // Cursor: the stage this copy of the sequence stands at. The producer and
+    // each consumer walk the stages in order, so the position advances by
+    // additions; integer division (a long dependent chain on the GPU) only
+    // runs once, here.
+    int f, nf1;
+    int u, ut, cs;        // phase 1: active expert, its unit tile, chunk step
+    int rt, k2, u0, csu;  // phase 2: row tile, stage within it, first expert, chunk step
 
     __device__ void init(const CallArgs& ca, const DecExpert* pl, int na_, int blk, int grid) {
-        a = &ca;
+        gu = ca.lay.gu;
+        gu_tile = ca.lay.gu_tile;
+        d = ca.lay.d;
+        d_tile = ca.lay.d_tile;
         plan = pl;
         na = na_;
-        b = blk;
-        G = grid;
         G1 = grid > 1 ? grid - 1 : 1;
         b1 = grid > 1 ? blk - 1 : blk;
         UT = ca.I / 8;
@@ -385,6 +451,11 @@ struct StageSeq {
         ns1 = (nch1 + 1) / 2;
         n1 = na * UT;
         my1 = (b1 >= 0 && b1 < n1) ? (n1 - 1 - b1) / G1 + 1 : 0;
+        G1q = G1 / UT;
+        G1r = G1 - G1q * UT;
+        u = b1 >= 0 ? b1 / UT : 0;
+        ut = b1 >= 0 ? b1 - u * UT : 0;
+        cs = 0;
         G2k = ca.I / kGroupK;
         nch2 = (G2k + kChunkGroups - 1) / kChunkGroups;
         if (G2k >= kChunkGroups) {
@@ -398,71 +469,103 @@ struct StageSeq {
         }
         n2 = ca.H / kTileRows;
         my2 = (b1 >= 0 && b1 < n2) ? (n2 - 1 - b1) / G1 + 1 : 0;
+        rt = b1;
+        k2 = u0 = csu = 0;
+        f = 0;
+        nf1 = my1 * ns1;
     }
     __device__ int count1() const { return my1 * ns1; }
     __device__ int count2() const { return my2 * ns2; }
 
-    // phase 1, stage f of this CTA: chunks [c0, c0 + nc) of tile (u, ut)
-    __device__ void where1(int f, int& u, int& ut, int& c0, int& nc) const {
-        const int i = b1 + (f / ns1) * G1;
-        u = i / UT;
-        ut = i % UT;
-        c0 = 2 * (f % ns1);
-        nc = min(2, nch1 - c0);
-    }
-    __device__ void stage1(int f, Stage& st) const {
-        int u, ut, c0, nc;
-        where1(f, u, ut, c0, nc);
-        const uint8_t* tile = plan[u].ptr + a->lay.gu + static_cast<size_t>(ut) * a->lay.gu_tile;
-        uint32_t bytes = 0;
-        for (int c = c0; c < c0 + nc; ++c)
-            bytes += static_cast<uint32_t>(kTileRows) * fp4_chunk_groups(G1k, c) * (64 + Fp4Cfg<FMT>::kSbpg);
-        st.src[0] = tile + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
-        st.bytes[0] = bytes;
-        st.npieces = 1;
-        st.tile_end = (f % ns1) == ns1 - 1;
-    }
-    // phase 2, stage f: row tile rt; experts [u0, u0 + nu); chunks [c0, c0 + nc) (one expert) or whole tiles
-    __device__ void where2(int f, int& rt, int& u0, int& nu_, int& c0, int& nc) const {
-        rt = b1 + (f / ns2) * G1;
-        const int k = f % ns2;
+    // phase 1, the current stage: chunks [c0, c0 + nc) of tile (u, ut); the
+    // tile's last stage when cs == ns1 - 1
+    __device__ int c0_1() const { return 2 * cs; }
+    __device__ int nc_1() const { return min(2, nch1 - 2 * cs); }
+    __device__ bool end1() const { return cs == ns1 - 1; }
+    // phase 2, the current stage: row tile rt; experts [u0, u0 + nu); chunks
+    // [c0, c0 + nc) of one expert, or the whole tiles of several
+    __device__ void where2(int& rt_, int& u0_, int& nu_, int& c0, int& nc) const {
+        rt_ = rt;
+        u0_ = u0;
         if (epp == 1) {
-            u0 = k / nsu;
             nu_ = 1;
-            c0 = 2 * (k % nsu);
+            c0 = 2 * csu;
             nc = min(2, nch2 - c0);
         } else {
-            u0 = k * epp;
             nu_ = min(epp, na - u0);
             c0 = 0;
             nc = 1;
         }
     }
-    __device__ void stage2(int f, Stage& st) const {
-        int rt, u0, nu_, c0, nc;
-        where2(f, rt, u0, nu_, c0, nc);
-        const size_t toff = a->lay.d + static_cast<size_t>(rt) * a->lay.d_tile;
-        if (epp == 1) {
-            uint32_t bytes = 0;
-            for (int c = c0; c < c0 + nc; ++c)
-                bytes += static_cast<uint32_t>(kTileRows) * fp4_chunk_groups(G2k, c) * (64 + Fp4Cfg<FMT>::kSbpg);
-            st.src[0] = plan[u0].ptr + toff + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
-            st.bytes[0] = bytes;
-            st.npieces = 1;
-        } else {
-            const uint32_t pb = static_cast<uint32_t>(kTileRows) * G2k * (64 + Fp4Cfg<FMT>::kSbpg);
-            for (int p = 0; p < nu_; ++p) {
-                st.src[p] = plan[u0 + p].ptr + toff;
-                st.bytes[p] = pb;
+    __device__ bool end2() const { return k2 == ns2 - 1; }
+    __device__ void advance() {
+        if (f < nf1) {
+            if (++cs == ns1) {  // next tile: i += G1
+                cs = 0;
+                u += G1q;
+                ut += G1r;
+                if (ut >= UT) {
+                    ut -= UT;
+                    ++u;
+                }
             }
-            st.npieces = nu_;
+        } else {
+            if (epp == 1) {
+                if (++csu == nsu) {
+                    csu = 0;
+                    ++u0;
+                }
+            } else {
+                u0 += epp;
+            }
+            if (++k2 == ns2) {  // next row tile
+                k2 = u0 = csu = 0;
+                rt += G1;
+            }
         }
-        st.tile_end = (f % ns2) == ns2 - 1;
+        ++f;
+    }
+
+    // Copy number `lane` of the current stage (all in registers: the producer
+    // issues one copy per lane): its source, size and offset in the stage;
+    // returns the number of copies of the stage (lanes at or above it have
+    // none) and sets the stage's total bytes.
+    __device__ int piece(int lane, const uint8_t*& src, uint32_t& bytes, uint32_t& off, uint32_t& total) const {
+        constexpr uint32_t row = 64 + Fp4Cfg<FMT>::kSbpg;  // bytes of one row of one K group
+        if (f < nf1) {
+            const int c0 = c0_1(), nc = nc_1();
+            uint32_t g = 0;
+            for (int c = c0; c < c0 + nc; ++c) g += fp4_chunk_groups(G1k, c);
+            total = static_cast<uint32_t>(kTileRows) * g * row;
+            src = plan[u].ptr + gu + static_cast<size_t>(ut) * gu_tile + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+            bytes = total;
+            off = 0;
+            return 1;
+        }
+        int rt_, u0_, nu_, c0, nc;
+        where2(rt_, u0_, nu_, c0, nc);
+        const size_t toff = d + static_cast<size_t>(rt_) * d_tile;
+        if (epp == 1) {
+            uint32_t g = 0;
+            for (int c = c0; c < c0 + nc; ++c) g += fp4_chunk_groups(G2k, c);
+            total = static_cast<uint32_t>(kTileRows) * g * row;
+            src = plan[u0_].ptr + toff + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+            bytes = total;
+            off = 0;
+            return 1;
+        }
+        const uint32_t pb = static_cast<uint32_t>(kTileRows) * G2k * row;
+        total = static_cast<uint32_t>(nu_) * pb;
+        const int p = lane < nu_ ? lane : 0;
+        src = plan[u0_ + p].ptr + toff;
+        bytes = pb;
+        off = static_cast<uint32_t>(p) * pb;
+        return nu_;
     }
 };
 
 template <int FMT, int ACT>
-__global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo) {
+__global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ CallArgs a, const __grid_constant__ DecGeom geo) {
     using C = Fp4Cfg<FMT>;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], p1bar;
@@ -485,6 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     // CTAs), h written (workers 1..G-1)
     const unsigned long long tgt0 = (a.dcall + 1) * static_cast<unsigned long long>(G);
     const unsigned long long tgt2 = (a.dcall + 1) * static_cast<unsigned long long>(G - 1);
+    // decode logits carry the call's sequence number (the entries of earlier
+    // calls and of the reset buffer, 0, never match it)
+    const uint32_t lseq = static_cast<uint32_t>(a.dcall + 1);
+    const unsigned long long tag = static_cast<unsigned long long>(lseq) << 32;
+    // Every CTA computes logits when E >= G: then a CTA's logits, stored with
+    // release semantics after it read its LRU table row, tell the cache-update
+    // CTA that the row was read, and no barrier is needed; else barrier 1.
+    const bool logits_barrier = E < G;
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -527,10 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         if (staged && tid == 0) {
             mbar_expect_tx(&p1bar, xbytes + static_cast<uint32_t>(nexp) * rbytes);
             bulk_g2s(ring, a.hidden, xbytes, &p1bar);
+            const uint64_t keep = l2_evict_last();
             for (int j = 0; j < nexp; ++j)
-                bulk_g2s(ring + xbytes + static_cast<size_t>(j) * rbytes,
-                         reinterpret_cast<const unsigned char*>(a.router_w) + static_cast<size_t>(b + j * G) * rbytes,
-                         rbytes, &p1bar);
+                bulk_g2s_hint(ring + xbytes + static_cast<size_t>(j) * rbytes,
+                              reinterpret_cast<const unsigned char*>(a.router_w) + static_cast<size_t>(b + j * G) * rbytes,
+                              rbytes, &p1bar, keep);
         }
         // this layer's table row before anything of this call changes it: CTA 0
         // rewrites entries of missed experts after the barrier below
@@ -542,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         __syncthreads();
         if (tid == 0) mark(10);
         // row maxima of the token rows (every CTA, from its own copy): warp t, token t
-        if (warp < T) {
-            const int t = warp;
+        if (kWarps - 1 - warp < T) {  // the last warps, beside the logit warps
+            const int t = kWarps - 1 - warp;
             float m = 0.f;
             for (int i = 8 * lane; i < H; i += 8 * 32) {
                 float v[8];
@@ -571,6 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         // router logits in the fixed order: lane l accumulates chunks l, l+32, ...
         // of 8 elements with fused multiply-adds, then the xor butterfly
         const int nchunk = H / 8;
+        // release: this CTA's LRU table read (above, complete at the barrier)
+        // precedes the tagged logits below, whose stores are then relaxed
+        if (warp < nexp && lane == 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
         for (int j = warp; j < nexp; j += kWarps) {
             const int e = b + j * G;
             const unsigned char* wrow = staged ? ring + xbytes + static_cast<size_t>(j) * rbytes
@@ -621,10 +736,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             }
 #pragma unroll
             for (int t = 0; t < kDecodeMaxT; ++t) {
-                float v = acc[t];
+                if (t < T) {
+                    float v = acc[t];
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-                if (lane == 0 && t < T) a.logits[static_cast<size_t>(t) * E + e] = v;
+                    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    if (lane == 0) st_relaxed_gpu64(a.dlog + static_cast<size_t>(t) * E + e, tag | __float_as_uint(v));
+                }
             }
         }
         __syncthreads();
@@ -635,28 +752,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         if (geo.act_bytes && b != 0) {
             const int xp = H * 2 + 16;
             const int h4 = H / 4;
-            for (int idx = tid; idx < T * h4; idx += kThreads) {
-                const int t = idx / h4;
-                const int p = 4 * (idx % h4);  // device position
-                const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
-                const size_t src = static_cast<size_t>(t) * H + 128 * j + 16 * s + 4 * q;
-                float v[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v[i] = ACT == ACT_BF16
-                               ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(xsrc)[src + i]) << 16)
-                               : reinterpret_cast<const float*>(xsrc)[src + i];
-                uint2 o;
-                o.x = f16x2_scaled(v[0], v[1], R.xsc[t]);
-                o.y = f16x2_scaled(v[2], v[3], R.xsc[t]);
-                *reinterpret_cast<uint2*>(act + t * xp + 2 * p) = o;
+            for (int t = 0; t < T; ++t) {
+                for (int i4 = tid; i4 < h4; i4 += kThreads) {
+                    const int p = 4 * i4;  // device position
+                    const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
+                    const size_t src = static_cast<size_t>(t) * H + 128 * j + 16 * s + 4 * q;
+                    float v[4];
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v[i] = ACT == ACT_BF16
+                                   ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(xsrc)[src + i]) << 16)
+                                   : reinterpret_cast<const float*>(xsrc)[src + i];
+                    uint2 o;
+                    o.x = f16x2_scaled(v[0], v[1], R.xsc[t]);
+                    o.y = f16x2_scaled(v[2], v[3], R.xsc[t]);
+                    *reinterpret_cast<uint2*>(act + t * xp + 2 * p) = o;
+                }
             }
         }
         __syncthreads();
         if (tid == 0) {
             mark(1);
-            bar_arrive(a.bar_cnt, 1);
-            R.ok = bar_wait(a, a.bar_cnt, tgt0, MOE_DEVERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+            R.ok = 1;
+            if (logits_barrier) {
+                bar_arrive(a.bar_cnt, 1);
+                R.ok = bar_wait(a, a.bar_cnt, tgt0, MOE_DEVERR_TIMEOUT_EPILOGUE) ? 1 : 0;
+            }
             mark(2);
         }
         __syncthreads();
@@ -664,96 +785,177 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
     if (!R.ok) return;  // every CTA gives up the same way; nothing is in flight
 
     // ---------------------------------------------------------------- P2: routing (every CTA)
-    if (warp < T) {
-        int sel;
-        float gv;
-        warp_topk<true>(a.logits + static_cast<size_t>(warp) * E, E, k, lane, sel, gv);
-        if (lane < k) {
-            R.tk[warp * k + lane] = sel;
-            R.g[warp * k + lane] = gv;
-        }
-    }
-    __syncthreads();
-    if (tid == 0) mark(12);
-    // stable order by expert: row of assignment i = #{j : e_j < e_i or (e_j == e_i and j < i)}
-    int my_first = 0;
-    for (int i = tid; i < n; i += kThreads) {
-        const int e = R.tk[i];
-        int rk = 0, first = 1;
-#pragma unroll 16
-        for (int j2 = 0; j2 < n; ++j2) {
-            const int f = R.tk[j2];
-            rk += (f < e) || (f == e && j2 < i);
-            first &= !(f == e && j2 < i);
-        }
-        R.rank[i] = rk;
-        R.first[i] = first;
-        R.rowtok[rk] = i / k;
-        my_first += first;
-    }
-    const int nu = __syncthreads_count(my_first);  // n <= 256 < threads: one assignment per thread
-    for (int i = tid; i < n; i += kThreads) {
-        const int e = R.tk[i];
-        int u = 0;
-#pragma unroll 16
-        for (int j2 = 0; j2 < n; ++j2) u += R.first[j2] && R.tk[j2] < e;
-        R.uidx[i] = u;
-        if (R.first[i]) R.members[u] = e;
-    }
-    if (tid == 0) {
-        R.nu = nu;
-        R.status = nu > a.S ? -4 : 0;  // MOE_ERR_CAPACITY: the call leaves the cache as it was
-    }
-    __syncthreads();
-    const int na = nu + ns;
-    for (int u = tid; u < na; u += kThreads) {
-        DecExpert& d = plan[u];
-        for (int t = 0; t < kDecodeMaxT; ++t) {
-            d.tok[t] = -1;
-            d.hrow[t] = -1;
-            d.gate[t] = 0.f;
-        }
-        d.cnt = 0;
-        if (u < nu) {
-            const int s = R.trow[R.members[u]];
-            R.mslot[u] = s;
-            R.hit[u] = s >= 0 ? 1 : 0;
-            d.ptr = s >= 0 ? a.pool + static_cast<size_t>(s) * B : nullptr;
-        } else {
-            const int sidx = u - nu;
-            d.ptr = a.shared_base + static_cast<size_t>(sidx) * B;
-            d.row0 = n + sidx * T;
-            d.cnt = T;
-            for (int t = 0; t < T; ++t) {
-                d.tok[t] = t;
-                d.hrow[t] = n + sidx * T + t;
-                d.gate[t] = 1.0f;
+    if (T == 1) {
+        // One token: its k experts are distinct, so the expert-major order is
+        // the ascending order of the selected experts and every expert has one
+        // row. Warp 0 builds the same records as the general path below from
+        // registers: lane j < k holds selection j and its rank r.
+        if (warp == 0) {
+            int sel;
+            float gv;
+            float* lrow = reinterpret_cast<float*>(ring);  // the staged rows are no longer needed
+            const bool got = __all_sync(0xffffffffu, poll_logits(a.dlog, E, lseq, lrow, lane, a.wait_ns));
+            if (!got && lane == 0) {
+                atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_EPILOGUE);
+                R.ok = 0;
+            }
+            __syncwarp();
+            warp_topk<false>(lrow, E, k, lane, sel, gv, R.tks[0]);
+            if (lane == 0) mark(12);
+            const bool live = lane < k;
+            int r = 0;
+            for (int i = 0; i < k; ++i) r += __shfl_sync(0xffffffffu, sel, i) < sel;
+            int slot = 0;
+            if (live) {
+                R.tk[lane] = sel;
+                R.g[lane] = gv;
+                R.rank[lane] = r;
+                R.first[lane] = 1;
+                R.uidx[lane] = r;
+                R.rowtok[r] = 0;
+                R.members[r] = sel;
+                slot = R.trow[sel];
+                R.mslot[r] = slot;
+                R.hit[r] = slot >= 0 ? 1 : 0;
+                DecExpert& d = plan[r];
+                d.ptr = slot >= 0 ? a.pool + static_cast<size_t>(slot) * B : nullptr;
+                d.row0 = r;
+                d.cnt = 1;
+#pragma unroll
+                for (int t = 0; t < kDecodeMaxT; ++t) {
+                    d.tok[t] = t == 0 ? 0 : -1;
+                    d.hrow[t] = t == 0 ? r : -1;
+                    d.gate[t] = t == 0 ? gv : 0.f;
+                }
+            }
+            // misses in member (rank) order
+            const bool miss = live && slot < 0;
+            const unsigned int mm = __reduce_or_sync(0xffffffffu, miss ? 1u << r : 0u);
+            if (miss) R.missr[__popc(mm & ((1u << r) - 1u))] = r;
+            for (int sidx = lane; sidx < ns; sidx += 32) {
+                DecExpert& d = plan[k + sidx];
+                d.ptr = a.shared_base + static_cast<size_t>(sidx) * B;
+                d.row0 = k + sidx;
+                d.cnt = 1;
+#pragma unroll
+                for (int t = 0; t < kDecodeMaxT; ++t) {
+                    d.tok[t] = t == 0 ? 0 : -1;
+                    d.hrow[t] = t == 0 ? k + sidx : -1;
+                    d.gate[t] = t == 0 ? 1.0f : 0.f;
+                }
+                R.rowtok[k + sidx] = 0;
+            }
+            if (lane == 0) {
+                R.nu = k;
+                R.status = k > a.S ? -4 : 0;  // MOE_ERR_CAPACITY
+                R.n_miss = __popc(mm);
             }
         }
-    }
-    for (int i = tid; i < ns * T; i += kThreads) R.rowtok[n + i] = i % T;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads)
-        if (R.first[i]) plan[R.uidx[i]].row0 = R.rank[i];
-    // the r-th missed member, in member order
-    for (int p = tid; p < nu; p += kThreads)
-        if (!R.hit[p]) {
-            int r = 0;
-#pragma unroll 16
-            for (int p2 = 0; p2 < p; ++p2) r += !R.hit[p2];
-            R.missr[r] = p;
+    } else {
+        if (warp < T) {
+            int sel;
+            float gv;
+            float* lrow = reinterpret_cast<float*>(ring) + static_cast<size_t>(warp) * E;
+            const bool got =
+                __all_sync(0xffffffffu, poll_logits(a.dlog + static_cast<size_t>(warp) * E, E, lseq, lrow, lane, a.wait_ns));
+            if (!got && lane == 0) {
+                atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_EPILOGUE);
+                R.ok = 0;
+            }
+            __syncwarp();
+            warp_topk<false>(lrow, E, k, lane, sel, gv, R.tks[warp]);
+            if (lane < k) {
+                R.tk[warp * k + lane] = sel;
+                R.g[warp * k + lane] = gv;
+            }
         }
-    const int n_miss_all = __syncthreads_count(tid < nu && !R.hit[tid]);
-    if (tid == 0) R.n_miss = n_miss_all;
-    for (int i = tid; i < n; i += kThreads) {
-        DecExpert& d = plan[R.uidx[i]];
-        const int t = i / k, nn = R.rank[i] - d.row0;
-        d.tok[nn] = t;
-        d.gate[nn] = R.g[i];
-        d.hrow[t] = R.rank[i];
-        atomicAdd(&d.cnt, 1);
+        __syncthreads();
+        if (tid == 0) mark(12);
+        // stable order by expert: row of assignment i = #{j : e_j < e_i or (e_j == e_i and j < i)}
+        int my_first = 0;
+        for (int i = tid; i < n; i += kThreads) {
+            const int e = R.tk[i];
+            int rk = 0, first = 1;
+    #pragma unroll 16
+            for (int j2 = 0; j2 < n; ++j2) {
+                const int f = R.tk[j2];
+                rk += (f < e) || (f == e && j2 < i);
+                first &= !(f == e && j2 < i);
+            }
+            R.rank[i] = rk;
+            R.first[i] = first;
+            R.rowtok[rk] = i / k;
+            my_first += first;
+        }
+        const int nu = __syncthreads_count(my_first);  // n <= 256 < threads: one assignment per thread
+        for (int i = tid; i < n; i += kThreads) {
+            const int e = R.tk[i];
+            int u = 0;
+    #pragma unroll 16
+            for (int j2 = 0; j2 < n; ++j2) u += R.first[j2] && R.tk[j2] < e;
+            R.uidx[i] = u;
+            if (R.first[i]) R.members[u] = e;
+        }
+        if (tid == 0) {
+            R.nu = nu;
+            R.status = nu > a.S ? -4 : 0;  // MOE_ERR_CAPACITY: the call leaves the cache as it was
+        }
+        __syncthreads();
+        const int na = nu + ns;
+        for (int u = tid; u < na; u += kThreads) {
+            DecExpert& d = plan[u];
+            for (int t = 0; t < kDecodeMaxT; ++t) {
+                d.tok[t] = -1;
+                d.hrow[t] = -1;
+                d.gate[t] = 0.f;
+            }
+            d.cnt = 0;
+            if (u < nu) {
+                const int s = R.trow[R.members[u]];
+                R.mslot[u] = s;
+                R.hit[u] = s >= 0 ? 1 : 0;
+                d.ptr = s >= 0 ? a.pool + static_cast<size_t>(s) * B : nullptr;
+            } else {
+                const int sidx = u - nu;
+                d.ptr = a.shared_base + static_cast<size_t>(sidx) * B;
+                d.row0 = n + sidx * T;
+                d.cnt = T;
+                for (int t = 0; t < T; ++t) {
+                    d.tok[t] = t;
+                    d.hrow[t] = n + sidx * T + t;
+                    d.gate[t] = 1.0f;
+                }
+            }
+        }
+        for (int i = tid; i < ns * T; i += kThreads) R.rowtok[n + i] = i % T;
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads)
+            if (R.first[i]) plan[R.uidx[i]].row0 = R.rank[i];
+        // the r-th missed member, in member order
+        for (int p = tid; p < nu; p += kThreads)
+            if (!R.hit[p]) {
+                int r = 0;
+    #pragma unroll 16
+                for (int p2 = 0; p2 < p; ++p2) r += !R.hit[p2];
+                R.missr[r] = p;
+            }
+        const int n_miss_all = __syncthreads_count(tid < nu && !R.hit[tid]);
+        if (tid == 0) R.n_miss = n_miss_all;
+        for (int i = tid; i < n; i += kThreads) {
+            DecExpert& d = plan[R.uidx[i]];
+            const int t = i / k, nn = R.rank[i] - d.row0;
+            d.tok[nn] = t;
+            d.gate[nn] = R.g[i];
+            d.hrow[t] = R.rank[i];
+            atomicAdd(&d.cnt, 1);
+        }
     }
     __syncthreads();
+    if (!R.ok) return;  // a logits wait gave up (the device error is set)
+    // CTA 0 rewrites LRU table entries below: every CTA's read of its table row
+    // happened before its release of the logits this CTA has now read
+    if (b == 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    const int nu = R.nu, na = nu + ns;
     const int n_miss = R.n_miss;
     const bool capacity_err = R.status != 0;
     if (tid == 0) mark(3);
@@ -820,12 +1022,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             if (tid == 0) sm.clock = __ldcg(a.clock);
             __syncthreads();
             LruView lv;
-            lv.a = &a;
+            lv.bind(a);
             lv.trow0 = trow;
             lv.trow1 = nullptr;
             lv.st_s = st_s;
             lv.own_s = own_s;
-            const int m = lru_batch(a, lv, sm, keys, a.layer, R.members, nu, nullptr, 0, 0);
+            const int m = lru_batch(lv, sm, keys, a.layer, R.members, nu, nullptr, 0, 0);
             // m == n_miss: the members that missed are those whose table entry was -1
             for (int r = tid; r < m; r += kThreads) {
                 const int p = sm.miss_p[r];
@@ -936,33 +1138,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         // ---------------------------------------------------------------- producer
         int stage = 0;
         uint32_t phase = 0;
-        int issued[kMaxStages];
-        for (int s = 0; s < kMaxStages; ++s) issued[s] = -1;
+        const uint64_t stream = l2_evict_first();
         bool ok = true;
-        Stage st;
-        for (int f = 0; f < nf1 + nf2 && ok; ++f) {
-            if (f < nf1) seq.stage1(f, st);
-            else seq.stage2(f - nf1, st);
+        const int nf = nf1 + nf2;
+        if (lane == 0) mark(20);
+        int f = 0;
+        for (; f < nf && ok; ++f) {
+            const uint8_t* src;
+            uint32_t bytes, off, total;
+            const int np = seq.piece(lane, src, bytes, off, total);
             int got = 1;
             if (lane == 0) {
                 got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns) && !*abort_flag;
-                if (got) {
-                    uint32_t tot = 0;
-                    for (int p = 0; p < st.npieces; ++p) tot += st.bytes[p];
-                    mbar_expect_tx(&full[stage], tot);
-                }
+                if (got) mbar_expect_tx(&full[stage], total);
             }
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 ok = false;
                 break;
             }
-            if (lane < st.npieces) {
-                uint32_t off = 0;
-                for (int p = 0; p < lane; ++p) off += st.bytes[p];
-                bulk_g2s(ring + stage * C::kStageBytes + off, st.src[lane], st.bytes[lane], &full[stage]);
-            }
-            issued[stage] = static_cast<int>(phase);
+            if (lane < np) bulk_g2s_hint(ring + stage * C::kStageBytes + off, src, bytes, &full[stage], stream);
+            if (lane == 0 && (f == 0 || f == nf1 - 1)) mark(f == 0 ? 16 : 17);
+            seq.advance();
             if (++stage == nst) {
                 stage = 0;
                 phase ^= 1u;
@@ -972,14 +1169,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
             atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_PRODUCER);
             *abort_flag = 1;
         }
-        // every copy this warp issued must land before the CTA may exit
-        if (lane == 0)
-            for (int s = 0; s < nst; ++s)
-                if (issued[s] >= 0) {
-                    const uint64_t t0 = gtimer();
-                    while (!mbar_test(&full[s], static_cast<uint32_t>(issued[s])) && gtimer() - t0 < a.wait_ns) {
-                    }
+        if (a.trace && lane == 0) {
+            // trace only: when the producer had issued everything, when phase 1's last stage landed
+            mark(18);
+            if (nf1 > 0 && nf1 <= f && f - nf1 < nst) {  // its slot has not been reused since
+                const uint64_t t0 = gtimer();
+                while (!mbar_test(&full[(nf1 - 1) % nst], static_cast<uint32_t>(((nf1 - 1) / nst) & 1)) &&
+                       gtimer() - t0 < a.wait_ns) {
                 }
+                mark(19);
+            }
+        }
+        // every copy this warp issued (stages 0 .. f-1) must land before the
+        // CTA may exit: the last use of each slot, with its phase parity
+        if (lane == 0)
+            for (int g2 = f > nst ? f - nst : 0; g2 < f; ++g2) {
+                const uint64_t t0 = gtimer();
+                while (!mbar_test(&full[g2 % nst], static_cast<uint32_t>((g2 / nst) & 1)) && gtimer() - t0 < a.wait_ns) {
+                }
+            }
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- consumers
@@ -1063,8 +1271,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
         {
             float acc[4][4] = {};  // four independent chains: (chunk half, even/odd step)
             for (int f = 0; f < nf1; ++f) {
-                int u, ut, c0, nc;
-                seq.where1(f, u, ut, c0, nc);
+                const int u = seq.u, ut = seq.ut, c0 = seq.c0_1(), nc = seq.nc_1();
+                const bool tile_end = seq.end1();
+                seq.advance();
                 const DecExpert& m = plan[u];
                 const int tok = m.tok[g];
                 const unsigned char* st = wait_full();
@@ -1084,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                     }
                 }
                 release();
-                if ((f % seq.ns1) == seq.ns1 - 1) {
+                if (tile_end) {
                     float v[4], part[4];
 #pragma unroll
                     for (int x = 0; x < 4; ++x) part[x] = ((acc[0][x] + acc[1][x]) + acc[2][x]) + acc[3][x];
@@ -1153,15 +1362,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                 }
                 consumer_sync();
             }
+            // with several experts per stage: this warp's expert and K group in each half
+            int p2[2], w2[2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int gs = w + kConsumers * half;  // group slot of this stage
+                p2[half] = seq.epp == 1 ? 0 : gs / seq.G2k;
+                w2[half] = gs - p2[half] * seq.G2k;
+            }
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int f = 0; f < nf2; ++f) {
                 int rt, u0, nu_, c0, nc;
-                seq.where2(f, rt, u0, nu_, c0, nc);
+                seq.where2(rt, u0, nu_, c0, nc);
+                const bool tile_end = seq.end2();
+                seq.advance();
                 const unsigned char* st = wait_full();
                 if (ct == 0 && f == nf2 - 1) mark(15);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const int gs = w + kConsumers * half;  // group slot of this stage
                     int u, c, ww, ng, off;
                     if (seq.epp == 1) {
                         u = u0;
@@ -1170,10 +1388,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                         ng = c < c0 + nc ? fp4_chunk_groups(seq.G2k, c) : 0;
                         off = half * C::kChunkBytes;
                     } else {
-                        const int p = gs / seq.G2k;
+                        const int p = p2[half];
                         u = u0 + p;
                         c = 0;
-                        ww = gs % seq.G2k;
+                        ww = w2[half];
                         ng = p < nu_ ? seq.G2k : 0;
                         off = p * kTileRows * seq.G2k * (64 + C::kSbpg);
                     }
@@ -1191,7 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(CallArgs a, DecGeom geo)
                     }
                 }
                 release();
-                if ((f % seq.ns2) == seq.ns2 - 1) {
+                if (tile_end) {
                     float v[4];
                     if (tile_reduce(acc, v)) {
                         const int r0 = rt * kTileRows;

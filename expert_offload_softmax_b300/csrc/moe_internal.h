@@ -118,8 +118,11 @@ constexpr int kDecPlanHeader = 128;
 // 4 cache updated (CTA 0), 5 misses copied, 6 phase 1 done, 7 barrier 2
 // passed, 8 phase 2 done, 9 end; 10 token and router rows staged, 11 logits
 // computed, 12 top-k done, 13 first phase-1 stage landed, 14 last phase-1
-// stage landed, 15 last phase-2 stage landed
-constexpr int kTracePoints = 16;
+// stage landed, 15 last phase-2 stage landed (all as the consumers saw them);
+// producer: 16 first stage issued, 17 last phase-1 stage issued, 18 every
+// stage issued, 19 last phase-1 stage landed, 20 producer set up, 21 first
+// stage described, 22 first stage's slot free
+constexpr int kTracePoints = 24;
 
 // Published by the CTA of the fused decode kernel that runs the cache lookup,
 // for the kernel's other CTAs: the pool slots chosen for the call's misses (in
@@ -142,6 +145,7 @@ struct CallArgs {
     // scratch (device)
     void* xh;              // [T][H] f16 (FP4) or bf16 (BF16), device K-order
     float* logits;         // [T][E]
+    unsigned long long* dlog;  // [kDecodeMaxT][E] decode logits: (call sequence << 32) | fp32 bits
     int32_t* topk;         // [T*k]
     float* gates;          // [T*k]
     int32_t* counts;       // [E]

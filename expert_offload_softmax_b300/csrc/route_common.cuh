@@ -88,10 +88,90 @@ __device__ __forceinline__ void warp_topk_n(const float* lrow, int E, int k, int
     gate = pj / psum;
 }
 
+// The same selection with one pass instead of k rounds, using 32 words of
+// warp-private scratch. Every logit becomes one 64-bit key, (ordered logit,
+// inverted index), so that a larger key means a larger logit or, on equal
+// logits, a lower index: the selection order above. The k-th largest of the
+// 32 lane maxima is a lower bound tau of the k-th largest key, since k lanes
+// hold a key >= tau; only keys >= tau can be selected (at least k, at most
+// k * KPER of them, usually a few more than k). When they fit in 32 they are
+// compacted into the scratch and each is ranked by counting the larger ones;
+// otherwise the function returns false and selects nothing.
+template <bool GLOBAL, int KPER>
+__device__ __forceinline__ bool warp_topk_pass(const float* lrow, int E, int k, int lane, unsigned long long* scr,
+                                               int& sel, float& gate) {
+    unsigned long long key[KPER];
+    unsigned long long lm = 0ull;
+#pragma unroll
+    for (int i = 0; i < KPER; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = 0ull;
+        if (e < E) {
+            float x = GLOBAL ? __ldcg(lrow + e) : lrow[e];
+            if (x != x) x = -INFINITY;
+            x = __fadd_rn(x, 0.0f);  // -0.0 -> +0.0
+            key[i] = (static_cast<unsigned long long>(ord_key(x)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+        }
+        lm = key[i] > lm ? key[i] : lm;
+    }
+    // rank of this lane's maximum among the 32 (keys of valid logits are distinct;
+    // lanes without one hold 0, below all of them, and k <= min(32, E))
+    int r = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r += __shfl_sync(0xffffffffu, lm, j) > lm;
+    const unsigned int bal = __ballot_sync(0xffffffffu, r == k - 1);
+    const unsigned long long tau = __shfl_sync(0xffffffffu, lm, __ffs(bal) - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < KPER; ++i) cnt += key[i] >= tau;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total > 32) return false;
+    int pos = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < KPER; ++i)
+        if (key[i] >= tau) scr[pos++] = key[i];
+    __syncwarp();
+    const unsigned long long mine = lane < total ? scr[lane] : 0ull;
+    int rank = 0;
+    for (int j = 0; j < total; ++j) rank += scr[j] > mine;
+    __syncwarp();
+    if (lane < total && rank < k) scr[rank] = mine;
+    __syncwarp();
+    const unsigned long long kj = scr[lane < k ? lane : 0];
+    const unsigned long long k0 = scr[0];
+    __syncwarp();  // the scratch may be reused after this
+    const uint32_t uj = static_cast<uint32_t>(kj >> 32), u0 = static_cast<uint32_t>(k0 >> 32);
+    const float vj = __uint_as_float((uj & 0x80000000u) ? (uj & 0x7FFFFFFFu) : ~uj);
+    const float mx = __uint_as_float((u0 & 0x80000000u) ? (u0 & 0x7FFFFFFFu) : ~u0);
+    // gates: softmax restricted to the k selected (the full softmax's
+    // denominator cancels in the renormalisation)
+    const float pj = (lane < k && vj != -INFINITY) ? expf(vj - mx) : 0.0f;
+    float psum = pj;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+    sel = lane < k ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(kj)) : 0;
+    gate = pj / psum;
+    return true;
+}
+
+// top-k of one row of E logits by one warp; lane j < k gets selection j.
+// scr: 32 words of scratch private to the warp, or null (round-based only)
 template <bool GLOBAL>
-__device__ __forceinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate) {
-    if (E <= 256) warp_topk_n<GLOBAL, 8>(lrow, E, k, lane, sel, gate);
-    else warp_topk_n<GLOBAL, kMaxExperts / 32>(lrow, E, k, lane, sel, gate);
+__device__ __forceinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate,
+                                          unsigned long long* scr = nullptr) {
+    if (E <= 256) {
+        if (scr && warp_topk_pass<GLOBAL, 8>(lrow, E, k, lane, scr, sel, gate)) return;
+        warp_topk_n<GLOBAL, 8>(lrow, E, k, lane, sel, gate);
+    } else {
+        if (scr && warp_topk_pass<GLOBAL, kMaxExperts / 32>(lrow, E, k, lane, scr, sel, gate)) return;
+        warp_topk_n<GLOBAL, kMaxExperts / 32>(lrow, E, k, lane, sel, gate);
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -123,30 +203,45 @@ struct LruShared {
 // pool and of the table rows of this layer and the next. Every write goes to
 // both.
 struct LruView {
-    const CallArgs* a;
-    int32_t* trow0;               // table row of a.layer
-    int32_t* trow1;               // table row of a.layer + 1 (prefill prefetch)
+    // the LRU arrays and sizes, copied out of the call's arguments (a load
+    // through a pointer to a kernel argument is a memory round trip)
+    int32_t* gtable;              // [L*E] -> slot
+    unsigned long long* gstamp;   // [S]
+    int32_t* gowner;              // [S]
+    unsigned long long* gclock;
+    int E, S, layer;
+    int32_t* trow0;               // table row of `layer`
+    int32_t* trow1;               // table row of layer + 1 (prefill prefetch)
     unsigned long long* st_s;     // [S] stamps, or null
     int32_t* own_s;               // [S] owners, or null
-    __device__ int table(int layer, int e) const {
-        if (layer == a->layer) return trow0[e];
-        if (trow1 && layer == a->layer + 1) return trow1[e];
-        return a->table[layer * a->E + e];
+    __device__ __forceinline__ void bind(const CallArgs& a) {
+        gtable = a.table;
+        gstamp = a.stamp;
+        gowner = a.owner;
+        gclock = a.clock;
+        E = a.E;
+        S = a.S;
+        layer = a.layer;
+    }
+    __device__ int table(int l, int e) const {
+        if (l == layer) return trow0[e];
+        if (trow1 && l == layer + 1) return trow1[e];
+        return gtable[l * E + e];
     }
     __device__ void set_table(int key, int v) const {
-        a->table[key] = v;
-        const int l = key / a->E, e = key % a->E;
-        if (l == a->layer) trow0[e] = v;
-        else if (trow1 && l == a->layer + 1) trow1[e] = v;
+        gtable[key] = v;
+        const int l = key / E, e = key - l * E;
+        if (l == layer) trow0[e] = v;
+        else if (trow1 && l == layer + 1) trow1[e] = v;
     }
-    __device__ unsigned long long stamp(int s) const { return st_s ? st_s[s] : a->stamp[s]; }
+    __device__ unsigned long long stamp(int s) const { return st_s ? st_s[s] : gstamp[s]; }
     __device__ void set_stamp(int s, unsigned long long v) const {
-        a->stamp[s] = v;
+        gstamp[s] = v;
         if (st_s) st_s[s] = v;
     }
-    __device__ int owner(int s) const { return own_s ? own_s[s] : a->owner[s]; }
+    __device__ int owner(int s) const { return own_s ? own_s[s] : gowner[s]; }
     __device__ void set_owner(int s, int v) const {
-        a->owner[s] = v;
+        gowner[s] = v;
         if (own_s) own_s[s] = v;
     }
 };
@@ -157,9 +252,9 @@ __device__ __forceinline__ unsigned long long slot_key(unsigned long long stamp,
 
 // members: the batch's experts (ascending), or nullptr for 0..n-1.
 // Returns the number of misses, or -1 (not enough slots; nothing changed).
-__device__ inline int lru_batch(const CallArgs& a, const LruView& lv, LruShared& sm, unsigned long long* keys, int layer,
+__device__ inline int lru_batch(const LruView& lv, LruShared& sm, unsigned long long* keys, int layer,
                          const int32_t* members, int n, const int32_t* protect, int n_protect, int protect_layer) {
-    const int tid = threadIdx.x, nthr = blockDim.x, S = a.S;
+    const int tid = threadIdx.x, nthr = blockDim.x, S = lv.S;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     for (int i = tid; i < (S + 31) / 32; i += nthr) sm.blocked[i] = 0u;
     if (tid == 0) sm.n_free = 0;
@@ -255,7 +350,7 @@ __device__ inline int lru_batch(const CallArgs& a, const LruView& lv, LruShared&
         const int p = sm.miss_p[r];
         const int v = sm.victim[r];
         const int e = members ? members[p] : p;
-        const int32_t key = layer * a.E + e;
+        const int32_t key = layer * lv.E + e;
         const int32_t old = lv.owner(v);
         if (old >= 0) lv.set_table(old, -1);
         lv.set_owner(v, key);
@@ -267,7 +362,7 @@ __device__ inline int lru_batch(const CallArgs& a, const LruView& lv, LruShared&
     __syncthreads();
     if (tid == 0) {
         sm.clock = c;
-        *a.clock = c;
+        *lv.gclock = c;
     }
     __syncthreads();
     return m;

@@ -238,6 +238,7 @@ struct RouteShared {
     float gates[kDecodeMaxT * kMaxTopK];
     int32_t scan_a[kRouteWarps], scan_b[kRouteWarps];
     int32_t nu;
+    unsigned long long tks[kDecodeMaxT][32];  // top-k scratch of token t's warp
     LruShared lru;
 };
 
@@ -298,7 +299,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     const bool pf_possible = a.prefetch && T > kDecodeMaxT && a.layer + 1 < a.L;
     const bool cached = S <= kLruCachedSlots;
     LruView lv;
-    lv.a = &a;
+    lv.bind(a);
     lv.trow0 = rs.trow[0];
     lv.trow1 = pf_possible ? rs.trow[1] : nullptr;
     unsigned long long* st_s = reinterpret_cast<unsigned long long*>(area + route_area_union(S, E));
@@ -356,7 +357,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         if (warp < T) {
             int sel;
             float g;
-            warp_topk<true>(a.logits + static_cast<size_t>(warp) * E, E, k, lane, sel, g);
+            warp_topk<true>(a.logits + static_cast<size_t>(warp) * E, E, k, lane, sel, g, rs.tks[warp]);
             if (lane < k) {
                 rs.topk[warp * k + lane] = sel;
                 rs.gates[warp * k + lane] = g;
@@ -543,7 +544,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     // LRU: demand batch of this layer's experts
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(area);
     const int nu = rs.nu;
-    const int m = lru_batch(a, lv, sm, keys, a.layer, rs.members, nu, nullptr, 0, 0);
+    const int m = lru_batch(lv, sm, keys, a.layer, rs.members, nu, nullptr, 0, 0);
     if (m < 0) {
         if (tid == 0) {
             info->n_uniq = nu;
@@ -587,7 +588,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     int n_pf = 0, m_pf = 0;
     const bool do_pf = pf_possible && a.S >= nu + E;
     if (do_pf) {
-        m_pf = lru_batch(a, lv, sm, keys, a.layer + 1, nullptr, E, rs.members, nu, a.layer);
+        m_pf = lru_batch(lv, sm, keys, a.layer + 1, nullptr, E, rs.members, nu, a.layer);
         n_pf = E;
         if (m_pf < 0) { m_pf = 0; n_pf = 0; }  // cannot happen when S >= nu + E
         for (int p = tid; p < n_pf; p += nthr) {
@@ -698,6 +699,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         float* lg = reinterpret_cast<float*>(route_smem + static_cast<size_t>(kPrefillTokTile) * H * esz);
         int32_t* s_tk = reinterpret_cast<int32_t*>(lg + static_cast<size_t>(kPrefillTokTile) * E);
         int32_t* s_cnt = s_tk + kPrefillTokTile * kMaxTopK;
+        unsigned long long* s_scr = reinterpret_cast<unsigned long long*>(
+            route_smem + (reinterpret_cast<unsigned char*>(s_cnt + E) - route_smem + 7) / 8 * 8);
         copy_g2s(route_smem, reinterpret_cast<const unsigned char*>(a.hidden) + static_cast<size_t>(t0) * H * esz,
                  static_cast<size_t>(nt) * H * esz / 16);
         for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
@@ -721,7 +724,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         if (warp < nt) {
             int sel;
             float g;
-            warp_topk<false>(lg + warp * E, E, k, lane, sel, g);
+            warp_topk<false>(lg + warp * E, E, k, lane, sel, g, s_scr + warp * 32);
             if (lane < k) {
                 const size_t o = static_cast<size_t>(t0 + warp) * k + lane;
                 a.topk[o] = sel;
@@ -793,7 +796,8 @@ static size_t route_smem_bytes(const CallArgs& a, bool decode) {
     const size_t phase_a = decode ? static_cast<size_t>(a.T) * a.H * esz
                                   : static_cast<size_t>(kPrefillTokTile) * a.H * esz +
                                         static_cast<size_t>(kPrefillTokTile) * a.E * 4 +
-                                        static_cast<size_t>(kPrefillTokTile) * kMaxTopK * 4 + static_cast<size_t>(a.E) * 4;
+                                        static_cast<size_t>(kPrefillTokTile) * kMaxTopK * 4 + static_cast<size_t>(a.E) * 4 +
+                                        8 + static_cast<size_t>(kPrefillTokTile) * 32 * 8;
     return std::max(phase_a, kRouteSharedBytes + route_area_bytes(a.S, a.E));
 }
 

@@ -726,6 +726,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
         {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
         {3 * 8, reinterpret_cast<void**>(&a.bar_cnt)},
+        {static_cast<size_t>(moe::kDecodeMaxT) * E * 8, reinterpret_cast<void**>(&a.dlog)},
         {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.xmax)},
         {static_cast<size_t>(h->num_sms) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
         {sizeof(moe::DecPub), reinterpret_cast<void**>(&a.pub)},
@@ -919,6 +920,7 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* po
     CK(h, cudaMemset(h->base.dev_err, 0, 4));
     CK(h, cudaMemset(h->base.route_done, 0, 4));
     CK(h, cudaMemset(h->base.bar_cnt, 0, 3 * 8));
+    CK(h, cudaMemset(h->base.dlog, 0, static_cast<size_t>(moe::kDecodeMaxT) * h->d.num_experts * 8));
     h->dcalls = 0;
 
     // the ready word continues from the last serviced call
