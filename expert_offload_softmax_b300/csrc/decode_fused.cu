@@ -564,7 +564,9 @@ struct StageSeq {
     }
 };
 
-template <int FMT, int ACT>
+// TT: the call's token count when it is fixed at compile time (1: single-token
+// decode, whose loops over tokens then fold away), else 0 (T from the call)
+template <int FMT, int ACT, int TT>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ CallArgs a, const __grid_constant__ DecGeom geo) {
     using C = Fp4Cfg<FMT>;
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -578,18 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     unsigned char* act = dsm + geo.act_off;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
-    const int T = a.T, E = a.E, k = a.k, H = a.H, I = a.I, ns = a.n_shared;
+    const int T = TT ? TT : a.T, E = a.E, k = a.k, H = a.H, I = a.I, ns = a.n_shared;
     const int n = T * k;
     const int nst = geo.nst;
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
     const size_t B = a.lay.bytes;
     volatile int* abort_flag = &s_abort;
-    // the call's grid barriers: logits written (all CTAs), misses copied (all
-    // CTAs), h written (workers 1..G-1)
+    // the call's grid barriers: logits written (all CTAs; only when E < G),
+    // misses copied (all CTAs), h written (workers 1..G-1)
     const unsigned long long tgt0 = (a.dcall + 1) * static_cast<unsigned long long>(G);
-    const unsigned long long tgt2 = (a.dcall + 1) * static_cast<unsigned long long>(G - 1);
     // decode logits carry the call's sequence number (the entries of earlier
     // calls and of the reset buffer, 0, never match it)
+    const unsigned long long tgt2 = (a.dcall + 1) * static_cast<unsigned long long>(G - 1);
     const uint32_t lseq = static_cast<uint32_t>(a.dcall + 1);
     const unsigned long long tag = static_cast<unsigned long long>(lseq) << 32;
     // Every CTA computes logits when E >= G: then a CTA's logits, stored with
@@ -1310,7 +1312,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                 hv = av * up * m.gate[nn];
                                 reinterpret_cast<__nv_bfloat16*>(a.hbuf)[static_cast<size_t>(r) * I + dpos(ut * 8 + g)] =
                                     __float2bfloat16_rn(hv);
-                                atomicMax(&R.hmax[t], __float_as_uint(fabsf(hv)));
                             }
                         }
                     }
@@ -1323,44 +1324,81 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         consumer_sync();
         if (ct == 0) mark(6);
         if (b != 0) {
-            // this CTA's largest |h| per token, then the barrier, then the maxima of all workers
-            if (ct < kDecodeMaxT) a.hmax[static_cast<size_t>(b) * kDecodeMaxT + ct] = R.hmax[ct];
-            consumer_sync();
             if (ct == 0) {
                 bar_arrive(a.bar_cnt + 2, 1);
                 R.ok = (bar_wait(a, a.bar_cnt + 2, tgt2, MOE_DEVERR_TIMEOUT_EPILOGUE) && !*abort_flag) ? 1 : 0;
             }
             consumer_sync();
             if (!R.ok) *abort_flag = 1;
-            if (w < T) {
-                unsigned int mx = 0u;
-                for (int c2 = 1 + lane; c2 < G; c2 += 32)
-                    mx = max(mx, __ldcg(a.hmax + static_cast<size_t>(c2) * kDecodeMaxT + w));
-                mx = __reduce_max_sync(0xffffffffu, mx);
-                if (lane == 0) pow2_scale(mx, R.hsc[w], R.hun[w]);
-            }
-            if (ct == 0) mark(7);
-            consumer_sync();
         }
         // ---------------- phase 2: down projection + combine
         if (nf2 > 0) {
             const int hrows = n + ns * T;
-            if (geo.act_bytes) {
-                // every h row of the call into shared memory as f16, scaled per token
+            // Every h row of the call (bf16, read once): each token's largest |h|
+            // from the rows themselves, then the rows into shared memory as f16,
+            // scaled by a power of two per token (in place, when they fit).
+            {
                 const int per_row = I / 8;
-                for (int i = ct; i < hrows * per_row; i += 32 * kConsumers) {
-                    const int r = i / per_row, c8 = i % per_row;
-                    const uint4 x = __ldcg(reinterpret_cast<const uint4*>(hb + static_cast<size_t>(r) * I) + c8);
-                    const float sc = R.hsc[R.rowtok[r]];
-                    const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-                    uint4 o;
-                    o.x = f16x2_scaled(__uint_as_float(wv[0] << 16), __uint_as_float(wv[0] & 0xFFFF0000u), sc);
-                    o.y = f16x2_scaled(__uint_as_float(wv[1] << 16), __uint_as_float(wv[1] & 0xFFFF0000u), sc);
-                    o.z = f16x2_scaled(__uint_as_float(wv[2] << 16), __uint_as_float(wv[2] & 0xFFFF0000u), sc);
-                    o.w = f16x2_scaled(__uint_as_float(wv[3] << 16), __uint_as_float(wv[3] & 0xFFFF0000u), sc);
-                    *reinterpret_cast<uint4*>(act + r * hp + 16 * c8) = o;
+                const float inv_pr = 1.0f / static_cast<float>(per_row);
+                unsigned int mxt[kDecodeMaxT];
+#pragma unroll
+                for (int t = 0; t < kDecodeMaxT; ++t) mxt[t] = 0u;
+                const int nvec = hrows * per_row;  // row r holds vectors [r * per_row, (r + 1) * per_row): h is contiguous
+                const uint4* hv = reinterpret_cast<const uint4*>(hb);
+                for (int i0 = ct; i0 < nvec; i0 += 4 * 32 * kConsumers) {
+                    uint4 x[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {  // four loads in flight
+                        const int i = i0 + j * 32 * kConsumers;
+                        x[j] = i < nvec ? __ldcg(hv + i) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int i = i0 + j * 32 * kConsumers;
+                        if (i < nvec) {
+                            int r = __float2int_rz(static_cast<float>(i) * inv_pr);
+                            r += (r + 1) * per_row <= i;
+                            r -= r * per_row > i;
+                            if (geo.act_bytes) *reinterpret_cast<uint4*>(act + r * hp + 16 * (i - r * per_row)) = x[j];
+                            const uint32_t wv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+                            unsigned int m = 0u;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                m = max(m, max(wv[e] << 17 >> 1, (wv[e] & 0x7FFF0000u)));  // |bf16| as fp32 bits, both halves
+                            const int t = R.rowtok[r];
+#pragma unroll
+                            for (int tt = 0; tt < kDecodeMaxT; ++tt) mxt[tt] = tt == t ? max(mxt[tt], m) : mxt[tt];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int tt = 0; tt < kDecodeMaxT; ++tt) {
+                    if (tt < T) {
+                        const unsigned int mw = __reduce_max_sync(0xffffffffu, mxt[tt]);
+                        if (lane == 0) atomicMax(&R.hmax[tt], mw);
+                    }
                 }
                 consumer_sync();
+                if (ct < T) pow2_scale(R.hmax[ct], R.hsc[ct], R.hun[ct]);
+                consumer_sync();
+                if (geo.act_bytes) {
+                    for (int i = ct; i < hrows * per_row; i += 32 * kConsumers) {
+                        int r = __float2int_rz(static_cast<float>(i) * inv_pr);
+                        r += (r + 1) * per_row <= i;
+                        r -= r * per_row > i;
+                        uint4* pp = reinterpret_cast<uint4*>(act + r * hp + 16 * (i - r * per_row));
+                        const uint4 x = *pp;
+                        const float sc = R.hsc[R.rowtok[r]];
+                        uint4 o;
+                        o.x = f16x2_scaled(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u), sc);
+                        o.y = f16x2_scaled(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xFFFF0000u), sc);
+                        o.z = f16x2_scaled(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xFFFF0000u), sc);
+                        o.w = f16x2_scaled(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xFFFF0000u), sc);
+                        *pp = o;
+                    }
+                    consumer_sync();
+                }
+                if (ct == 0) mark(7);
             }
             // with several experts per stage: this warp's expert and K group in each half
             int p2[2], w2[2];
@@ -1516,19 +1554,26 @@ cudaError_t launch_one(const CallArgs& a, int grid, cudaStream_t s, bool pdl) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_decode<FMT, ACT>, a, geo);
+    return a.T == 1 ? cudaLaunchKernelEx(&cfg, k_decode<FMT, ACT, 1>, a, geo)
+                    : cudaLaunchKernelEx(&cfg, k_decode<FMT, ACT, 0>, a, geo);
 }
 
 }  // namespace
 
-cudaError_t decode_set_attributes() {
+template <int FMT, int ACT>
+cudaError_t set_attr() {
     cudaError_t e;
     const int lim = kSmemLimit;
-    if ((e = cudaFuncSetAttribute(k_decode<FMT_NVFP4, ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
-    if ((e = cudaFuncSetAttribute(k_decode<FMT_NVFP4, ACT_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
-    if ((e = cudaFuncSetAttribute(k_decode<FMT_MXFP4, ACT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
-    if ((e = cudaFuncSetAttribute(k_decode<FMT_MXFP4, ACT_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
-    return cudaSuccess;
+    if ((e = cudaFuncSetAttribute(k_decode<FMT, ACT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim))) return e;
+    return cudaFuncSetAttribute(k_decode<FMT, ACT, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+}
+
+cudaError_t decode_set_attributes() {
+    cudaError_t e;
+    if ((e = set_attr<FMT_NVFP4, ACT_BF16>())) return e;
+    if ((e = set_attr<FMT_NVFP4, ACT_FP32>())) return e;
+    if ((e = set_attr<FMT_MXFP4, ACT_BF16>())) return e;
+    return set_attr<FMT_MXFP4, ACT_FP32>();
 }
 
 cudaError_t launch_decode(const CallArgs& a, int num_sms, cudaStream_t s, bool pdl) {

@@ -120,8 +120,7 @@ constexpr int kDecPlanHeader = 128;
 // computed, 12 top-k done, 13 first phase-1 stage landed, 14 last phase-1
 // stage landed, 15 last phase-2 stage landed (all as the consumers saw them);
 // producer: 16 first stage issued, 17 last phase-1 stage issued, 18 every
-// stage issued, 19 last phase-1 stage landed, 20 producer set up, 21 first
-// stage described, 22 first stage's slot free
+// stage issued, 19 last phase-1 stage landed, 20 producer set up
 constexpr int kTracePoints = 24;
 
 // Published by the CTA of the fused decode kernel that runs the cache lookup,

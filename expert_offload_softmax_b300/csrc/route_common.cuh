@@ -162,9 +162,11 @@ __device__ __forceinline__ bool warp_topk_pass(const float* lrow, int E, int k, 
 
 // top-k of one row of E logits by one warp; lane j < k gets selection j.
 // scr: 32 words of scratch private to the warp, or null (round-based only)
+// (not inlined: one copy of this code serves every call site of a kernel, which
+// keeps the kernel's instructions within the SM's instruction cache)
 template <bool GLOBAL>
-__device__ __forceinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate,
-                                          unsigned long long* scr = nullptr) {
+__device__ __noinline__ void warp_topk(const float* lrow, int E, int k, int lane, int& sel, float& gate,
+                                       unsigned long long* scr = nullptr) {
     if (E <= 256) {
         if (scr && warp_topk_pass<GLOBAL, 8>(lrow, E, k, lane, scr, sel, gate)) return;
         warp_topk_n<GLOBAL, 8>(lrow, E, k, lane, sel, gate);
@@ -252,7 +254,7 @@ __device__ __forceinline__ unsigned long long slot_key(unsigned long long stamp,
 
 // members: the batch's experts (ascending), or nullptr for 0..n-1.
 // Returns the number of misses, or -1 (not enough slots; nothing changed).
-__device__ inline int lru_batch(const LruView& lv, LruShared& sm, unsigned long long* keys, int layer,
+static __device__ __noinline__ int lru_batch(const LruView& lv, LruShared& sm, unsigned long long* keys, int layer,
                          const int32_t* members, int n, const int32_t* protect, int n_protect, int protect_layer) {
     const int tid = threadIdx.x, nthr = blockDim.x, S = lv.S;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
