@@ -618,8 +618,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     }
     // programmatic dependent launch: everything the previous call wrote is
     // visible after this; the next call's CTAs may be scheduled as ours exit
+    const uint64_t t_entry = a.trace ? gtimer() : 0;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // trace only: per call, the first CTA's entry, CTA 0's return from the
+    // dependency wait, the last CTA's exit
+    unsigned long long* tcall =
+        a.trace ? a.trace + static_cast<size_t>(G) * kTracePoints + (a.dcall % kTraceCalls) * 4 : nullptr;
+    if (tcall && tid == 0) {
+        atomicMin(tcall, static_cast<unsigned long long>(t_entry));
+        if (b == 0) {
+            tcall[1] = gtimer();
+            // the next call's slot: its CTAs start after every CTA of this one has exited
+            unsigned long long* nxt = a.trace + static_cast<size_t>(G) * kTracePoints + ((a.dcall + 1) % kTraceCalls) * 4;
+            nxt[0] = ~0ull;
+            nxt[2] = 0ull;
+        }
+    }
     __syncthreads();
     // optional phase timeline (MOE_TRACE): per CTA, %globaltimer at fixed points
     auto mark = [&](int point) {
@@ -1476,6 +1491,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     }
     __syncthreads();
     if (tid == 0) mark(9);
+    if (tcall && tid == 0) atomicMax(tcall + 2, static_cast<unsigned long long>(gtimer()));
 }
 
 template <int FMT>

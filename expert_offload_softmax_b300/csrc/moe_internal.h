@@ -122,6 +122,9 @@ constexpr int kDecPlanHeader = 128;
 // producer: 16 first stage issued, 17 last phase-1 stage issued, 18 every
 // stage issued, 19 last phase-1 stage landed, 20 producer set up
 constexpr int kTracePoints = 24;
+// calls whose entry / dependency-wait / exit times the trace buffer keeps
+// after the per-CTA marks (4 words each: first entry, wait returned, last exit, unused)
+constexpr int kTraceCalls = 64;
 
 // Published by the CTA of the fused decode kernel that runs the cache lookup,
 // for the kernel's other CTAs: the pool slots chosen for the call's misses (in

@@ -84,6 +84,7 @@ struct moe_handle {
     // host banks: per layer, E blobs (pinned); loaded flags
     std::vector<uint8_t*> bank;
     std::vector<uint8_t> loaded;
+    std::vector<uint8_t> layer_complete;  // 1 once every expert of the layer has been seen loaded (it stays so)
     std::vector<const uint8_t*> bank_dev;  // device views of the mapped banks
     bool banks_dirty = false;             // bank_dev changed since the device table was written
     // shared experts: device resident [L][n_shared] blobs
@@ -593,6 +594,16 @@ void service_loop(moe_handle* h) {
     }
 }
 
+// MOE_TRACE buffer: per-CTA phase marks, then per-call entry / wait / exit times
+size_t trace_words(const moe_handle* h) {
+    return static_cast<size_t>(h->num_sms) * moe::kTracePoints + moe::kTraceCalls * 4;
+}
+void reset_trace(moe_handle* h) {
+    std::vector<unsigned long long> t(trace_words(h), 0ull);
+    for (int c = 0; c < moe::kTraceCalls; ++c) t[static_cast<size_t>(h->num_sms) * moe::kTracePoints + c * 4] = ~0ull;
+    cudaMemcpy(h->trace, t.data(), t.size() * 8, cudaMemcpyHostToDevice);
+}
+
 // waits until the service thread has handled every enqueued call
 void drain(moe_handle* h) {
     std::unique_lock<std::mutex> lk(h->mu);
@@ -689,6 +700,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     h->bank.assign(L, nullptr);
     h->bank_dev.assign(L, nullptr);
     h->loaded.assign(static_cast<size_t>(L) * E, 0);
+    h->layer_complete.assign(L, 0);
     if (ns > 0) {
         if (cudaMalloc(&h->shared_dev, static_cast<size_t>(L) * ns * h->lay.bytes) != cudaSuccess) return bail(MOE_ERR_OOM);
         cudaMemset(h->shared_dev, 0, static_cast<size_t>(L) * ns * h->lay.bytes);
@@ -749,9 +761,8 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     }
     h->ready = a.ready;
     if (want_trace) {
-        if (cudaMalloc(&h->trace, static_cast<size_t>(h->num_sms) * moe::kTracePoints * 8) != cudaSuccess)
-            return bail(MOE_ERR_OOM);
-        cudaMemset(h->trace, 0, static_cast<size_t>(h->num_sms) * moe::kTracePoints * 8);
+        if (cudaMalloc(&h->trace, trace_words(h) * 8) != cudaSuccess) return bail(MOE_ERR_OOM);
+        reset_trace(h);
         a.trace = h->trace;
     }
     if (umma) {
@@ -1058,14 +1069,18 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(router_w) |
          reinterpret_cast<uintptr_t>(out)) & 15u)
         return fail(h, MOE_ERR_INVALID, "device buffers must be 16-byte aligned");
-    for (int e = 0; e < E; ++e)
-        if (!h->loaded[static_cast<size_t>(layer_id) * E + e]) return fail(h, MOE_ERR_STATE, "layer has unloaded experts");
+    // experts are never unloaded: a layer found complete once is complete for good
+    auto complete = [&](int l) {
+        if (h->layer_complete[l]) return true;
+        for (int e = 0; e < E; ++e)
+            if (!h->loaded[static_cast<size_t>(l) * E + e]) return false;
+        h->layer_complete[l] = 1;
+        return true;
+    };
+    if (!complete(layer_id)) return fail(h, MOE_ERR_STATE, "layer has unloaded experts");
     const bool decode = T <= moe::kDecodeMaxT;
     const bool want_pf = !decode && (h->flags & MOE_CACHE_PREFETCH_NEXT_LAYER) && layer_id + 1 < L;
-    if (want_pf)
-        for (int e = 0; e < E; ++e)
-            if (!h->loaded[static_cast<size_t>(layer_id + 1) * E + e])
-                return fail(h, MOE_ERR_STATE, "next layer has unloaded experts");
+    if (want_pf && !complete(layer_id + 1)) return fail(h, MOE_ERR_STATE, "next layer has unloaded experts");
     CK(h, cudaSetDevice(h->d.device));
     cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
     const uint64_t seq = h->submitted + 1;
@@ -1233,7 +1248,23 @@ int moe_sync(moe_handle* h) {
             line += buf;
         }
         std::fprintf(stderr, "%s\n", line.c_str());
-        CK(h, cudaMemset(h->trace, 0, t.size() * 8));
+        // the calls since the last report: entry, dependency wait, exit, and the gap to the previous exit
+        const size_t base = static_cast<size_t>(G) * P;
+        std::vector<unsigned long long> c(moe::kTraceCalls * 4);
+        CK(h, cudaMemcpy(c.data(), h->trace + base, c.size() * 8, cudaMemcpyDeviceToHost));
+        unsigned long long prev_exit = 0;
+        const unsigned long long n = std::min<unsigned long long>(h->dcalls, moe::kTraceCalls);
+        for (unsigned long long d = h->dcalls - n; d < h->dcalls; ++d) {
+            const unsigned long long* e = c.data() + (d % moe::kTraceCalls) * 4;
+            if (e[0] == ~0ull || e[2] == 0) continue;
+            char buf[160];
+            std::snprintf(buf, sizeof(buf), "[moe] call %llu entry->wait %.2f us, wait->exit %.2f us, gap after previous exit %.2f us",
+                          d, (e[1] - e[0]) * 1e-3, (e[2] - e[1]) * 1e-3,
+                          prev_exit ? (static_cast<double>(e[0]) - static_cast<double>(prev_exit)) * 1e-3 : 0.0);
+            std::fprintf(stderr, "%s\n", buf);
+            prev_exit = e[2];
+        }
+        reset_trace(h);
     }
     return take_error(h);
 }
