@@ -146,7 +146,9 @@ struct CallArgs {
     void* out;             // [T][H] act
     // scratch (device)
     void* xh;              // [T][H] f16 (FP4) or bf16 (BF16), device K-order
-    float* logits;         // [T][E]
+    float* logits;         // [T][E] (prefill with BF16 activations: the tensor cores' approximate logits)
+    float* wnorm;          // [E] router row norms, rounded up (prefill tensor-core routing)
+    int32_t tc_router;     // 1: this prefill call's logits come from the tensor cores
     unsigned long long* dlog;  // [kDecodeMaxT][E] decode logits: (call sequence << 32) | fp32 bits
     int32_t* topk;         // [T*k]
     float* gates;          // [T*k]
@@ -204,6 +206,7 @@ struct CallArgs {
     DecPub* pub;           // miss slots for the kernel's CTAs
     int device_misses;     // 1: the decode kernel copies its misses itself; 0: the host does
     unsigned long long* trace;  // optional [CTAs][kTracePoints] %globaltimer marks of the decode kernel
+    int32_t trace_ctas;         // CTAs of the decode kernel (the trace's per-call ring follows their marks)
 };
 
 // Bounded wait of the expert kernels for their call's weights (one thread);
@@ -259,6 +262,10 @@ bool umma_map_3d(UmmaMap* m, const void* base, uint64_t slots, uint64_t slot_byt
 cudaError_t umma_set_attributes();
 // gather + gate/up + down on the tensor cores (prefill, BF16 weights); records
 // ev_gu after the gate/up GEMM when non-null
+// prefill routing with BF16 activations: router row norms and approximate
+// logits on the tensor cores (the routing kernel makes the top-k exact)
+bool router_tc_eligible(const CallArgs& a);
+cudaError_t launch_router_tc(const CallArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s,
                                 cudaEvent_t ev_gu, int* launches);
 

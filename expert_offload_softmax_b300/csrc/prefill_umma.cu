@@ -594,6 +594,169 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
     }
 }
 
+// ------------------------------------------------------------------ router logits on the tensor cores
+// Approximate router logits of a prefill call, L~[t][e] = sum_h x[t][h] w[e][h]
+// with BF16 operands and fp32 accumulation in TMEM: one CTA per 128 tokens, all
+// E (<= 256, a multiple of 32) experts as the MMA's N, K = H in 64-element TMA
+// stages. The sums are not in the fixed order of the router's definition; the
+// routing kernel turns them into the exact top-k (it recomputes, in the fixed
+// order, every logit that their error bound leaves in contention).
+constexpr int kRouterStages = 4;
+constexpr int kRouterBTile = 256 * BK * 2;  // router rows of one stage (E <= 256)
+constexpr int kRouterStageBytes = kTileBytes + kRouterBTile;
+constexpr int kRouterSmem = kRouterStages * kRouterStageBytes + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_router_tc(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, CallArgs a) {
+    extern __shared__ unsigned char dyn_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kRouterStages], bar_empty[kRouterStages], bar_tfull, bar_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+    const int E = a.E, H = a.H, T = a.T;
+    const int n_kb = H / BK;
+    const int t0 = blockIdx.x * BM;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kRouterStages; ++st) {
+            mbar_init(&bar_full[st], 1);
+            mbar_init(&bar_empty[st], 1);
+        }
+        mbar_init(&bar_tfull, 1);
+        mbar_init(&bar_drain, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s_tmem)), "r"(256)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int* abort_flag = &s_abort;
+    auto fail = [&](int code) {
+        *abort_flag = 1;
+        atomicExch(a.dev_err, code);
+    };
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: token tile and router rows of each K stage
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[kRouterStages];
+#pragma unroll
+            for (int st = 0; st < kRouterStages; ++st) issued_phase[st] = -1;
+            bool ok = true;
+            for (int kb = 0; kb < n_kb; ++kb) {
+                if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag, a.wait_ns)) {
+                    fail(MOE_DEVERR_TIMEOUT_PRODUCER);
+                    ok = false;
+                    break;
+                }
+                unsigned char* st = smem + stage * kRouterStageBytes;
+                mbar_expect_tx(&bar_full[stage], static_cast<uint32_t>(kTileBytes + E * BK * 2));
+                tma_2d(st, &map_x, &bar_full[stage], kb * BK, t0);
+                tma_2d(st + kTileBytes, &map_w, &bar_full[stage], kb * BK, 0);
+                issued_phase[stage] = static_cast<int>(phase);
+                if (++stage == kRouterStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                for (int st = 0; st < kRouterStages; ++st)
+                    if (issued_phase[st] >= 0) {
+                        const uint64_t w0 = gtimer();
+                        while (!mbar_test(&bar_full[st], static_cast<uint32_t>(issued_phase[st])) && gtimer() - w0 < a.wait_ns) {
+                        }
+                    }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: D[128 tokens][E] += X_tile * W_tile^T
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16(BM, E);
+            for (int kb = 0; kb < n_kb; ++kb) {
+                if (!mbar_wait(&bar_full[stage], phase, abort_flag, a.wait_ns)) {
+                    fail(MOE_DEVERR_TIMEOUT_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = su32(smem + stage * kRouterStageBytes);
+                const uint32_t sb = sa + kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_bf16(tmem, sdesc(sa + 32 * kk), sdesc(sb + 32 * kk), idesc, (kb | kk) != 0);
+                umma_commit(&bar_empty[stage]);
+                if (++stage == kRouterStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) umma_commit(&bar_tfull);
+            umma_commit(&bar_drain);
+            const uint64_t w0 = gtimer();
+            while (!mbar_test(&bar_drain, 0) && gtimer() - w0 < a.wait_ns) {
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2-5): TMEM lane = token of the tile
+        const int quarter = warp & 3;
+        const int t = t0 + quarter * 32 + lane;
+        if (mbar_wait(&bar_tfull, 0, abort_flag, a.wait_ns)) {
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+            for (int c0 = 0; c0 < E; c0 += 32) {
+                float v[32];
+                tmem_ld32(tbase + c0, v);
+                if (t < T) {
+                    float4* dst = reinterpret_cast<float4*>(a.logits + static_cast<size_t>(t) * E + c0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+            }
+        } else {
+            fail(MOE_DEVERR_TIMEOUT_EPILOGUE);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+    }
+}
+
+// Euclidean norm of every router row (BF16), rounded up: the fp32 sum of the
+// exact squares of H terms is within H * 2^-24 of the true sum, and the factor
+// 1 + 2^-10 covers that and the square root's rounding.
+__global__ void __launch_bounds__(256) k_router_norms(const __nv_bfloat16* __restrict__ w, int E, int H, float* out) {
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (e >= E) return;
+    const uint4* row = reinterpret_cast<const uint4*>(w + static_cast<size_t>(e) * H);
+    float ss = 0.0f;
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 u = __ldg(row + c);
+        const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(q[j] << 16), hi = __uint_as_float(q[j] & 0xFFFF0000u);
+            ss = __fmaf_rn(lo, lo, ss);
+            ss = __fmaf_rn(hi, hi, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) out[e] = sqrtf(ss) * (1.0f + 1.0f / 1024.0f);
+}
+
 // X_perm[r, :] = hidden[row_tok[r], :] as bf16 in the library's K order
 template <int ACT>
 __global__ void __launch_bounds__(256) k_gather_x(CallArgs a, int rows) {
@@ -676,6 +839,11 @@ bool umma_map_3d(UmmaMap* m, const void* base, uint64_t slots, uint64_t slot_byt
 // also loads the gather kernel (see experts_preload for why every kernel is loaded up front)
 cudaError_t umma_set_attributes() {
     cudaError_t e;
+    if ((e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmem))) return e;
+    {
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_router_norms)))) return e;
+    }
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16>)))) return e;
     if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32>)))) return e;
@@ -710,6 +878,21 @@ static void launch_gemms(const CallArgs& a, const UmmaMaps& maps, int num_sms, c
     k_umma_grouped<MODE_GU, FMT><<<num_sms, threads, Cfg<MODE_GU, FMT != FMT_BF16>::kSmem, s>>>(pg, sg, as_map(maps.x), a);
     if (ev_gu) cudaEventRecord(ev_gu, s);
     k_umma_grouped<MODE_DOWN, FMT><<<num_sms, threads, Cfg<MODE_DOWN, FMT != FMT_BF16>::kSmem, s>>>(pd, sd, as_map(maps.h), a);
+}
+
+bool router_tc_eligible(const CallArgs& a) {
+    return a.act == ACT_BF16 && a.T > kDecodeMaxT && a.E % 32 == 0 && a.E <= 256 && a.H % BK == 0;
+}
+
+// norms of the router rows, then the approximate logits of every token
+cudaError_t launch_router_tc(const CallArgs& a, cudaStream_t s) {
+    UmmaMap mx, mw;
+    if (!umma_map_2d(&mx, a.hidden, static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.H), BM) ||
+        !umma_map_2d(&mw, a.router_w, static_cast<uint64_t>(a.E), static_cast<uint64_t>(a.H), static_cast<uint32_t>(a.E)))
+        return cudaErrorInvalidValue;
+    k_router_norms<<<(a.E + 7) / 8, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(a.router_w), a.E, a.H, a.wnorm);
+    k_router_tc<<<(a.T + BM - 1) / BM, kThreads, kRouterSmem, s>>>(as_map(mx), as_map(mw), a);
+    return cudaGetLastError();
 }
 
 // gather, gate/up + SwiGLU, down; the combine is launched by the caller

@@ -125,6 +125,12 @@ __device__ __forceinline__ void copy_g2s(unsigned char* dst, const unsigned char
 // chain over them in order, so a batch costs one memory round trip.
 // --------------------------------------------------------------------------
 
+__device__ __forceinline__ uint64_t route_gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 template <int ACT>
 struct RawChunk {
     uint4 v[ACT == ACT_BF16 ? 1 : 2];
@@ -666,6 +672,15 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     extern __shared__ __align__(16) unsigned char route_smem[];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // trace only (prefill): first CTA entry, last phase-A finish, phase-B end in
+    // the last slot of the per-call ring
+    unsigned long long* rtr = (!DECODE && a.trace) ? a.trace + static_cast<size_t>(a.trace_ctas) * kTracePoints +
+                                                        (kTraceCalls - 1) * 4
+                                                  : nullptr;
+    if (rtr && threadIdx.x == 0) atomicMin(rtr, static_cast<unsigned long long>(route_gtimer()));
+    // trace only: CTA 0's phase-A steps in the two slots before it
+    unsigned long long* rsub = (rtr && blockIdx.x == 0 && threadIdx.x == 0) ? rtr - 8 : nullptr;
+    if (rsub) rsub[0] = route_gtimer();
     const int T = a.T, E = a.E, H = a.H;
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
     // ---------------- phase A
@@ -701,12 +716,80 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         int32_t* s_cnt = s_tk + kPrefillTokTile * kMaxTopK;
         unsigned long long* s_scr = reinterpret_cast<unsigned long long*>(
             route_smem + (reinterpret_cast<unsigned char*>(s_cnt + E) - route_smem + 7) / 8 * 8);
+        float* lsel = reinterpret_cast<float*>(s_scr + kPrefillTokTile * 32);  // [8][E] logits the top-k reads
+        float* wn = lsel + static_cast<size_t>(kPrefillTokTile) * E;          // [E] router row norms
+        int32_t* cand = reinterpret_cast<int32_t*>(wn + E);                   // [8 E] (token << 16 | expert)
         copy_g2s(route_smem, reinterpret_cast<const unsigned char*>(a.hidden) + static_cast<size_t>(t0) * H * esz,
                  static_cast<size_t>(nt) * H * esz / 16);
         for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+        const bool tc = ACT == ACT_BF16 && a.tc_router;
+        if (tc) {
+            // The tensor cores' logits L~ differ from the fixed-order ones L by at
+            // most B_te = H 2^-21 ||x_t|| ||w_e|| (each sum's rounding is below
+            // H 2^-23 sum |x_h w_h| <= H 2^-23 ||x_t|| ||w_e||, with a factor 2 to
+            // spare). The k-th largest of L~ - B is a lower bound of the k-th
+            // largest L, so only experts with L~ + B reaching it can be selected:
+            // those get their exact logits, the others -inf, and the top-k below
+            // is the top-k of the exact logits.
+            // E is a multiple of 32: the CTA's logit rows are whole 16-byte vectors
+            const float4* src4 = reinterpret_cast<const float4*>(a.logits + static_cast<size_t>(t0) * E);
+            for (int i0 = threadIdx.x; i0 < nt * E / 4; i0 += 4 * blockDim.x) {
+                float4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i0 + j * blockDim.x < nt * E / 4) v[j] = __ldcg(src4 + i0 + j * blockDim.x);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i0 + j * blockDim.x < nt * E / 4) reinterpret_cast<float4*>(lg)[i0 + j * blockDim.x] = v[j];
+            }
+            for (int e = threadIdx.x; e < E; e += blockDim.x) wn[e] = __ldcg(a.wnorm + e);
+            if (threadIdx.x == 0) s_last = 0;  // candidate count (s_last is free until the hand-off)
+        }
         __syncthreads();
+        if (rsub) rsub[1] = route_gtimer();
+        if (tc) {
+            if (warp < nt) {
+                const int t = warp;
+                const unsigned char* xr = route_smem + static_cast<size_t>(t) * H * esz;
+                float ss = 0.0f;
+                for (int c = lane; c < H / 8; c += 32) {
+                    float xv[8];
+                    ld_act8<ACT>(xr, 8 * c, xv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ss = __fmaf_rn(xv[j], xv[j], ss);
+                }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float cb = ldexpf(static_cast<float>(H), -21) * sqrtf(ss) * (1.0f + 1.0f / 1024.0f);
+                const float* lrow = lg + static_cast<size_t>(t) * E;
+                float* orow = lsel + static_cast<size_t>(t) * E;
+                for (int e = lane; e < E; e += 32) orow[e] = lrow[e] - cb * wn[e];
+                __syncwarp();
+                int sel;
+                float gd;
+                warp_topk<false>(orow, E, k, lane, sel, gd, s_scr + warp * 32);
+                const float tau = orow[__shfl_sync(0xffffffffu, sel, k - 1)];
+                __syncwarp();
+                for (int e = lane; e < E; e += 32) {
+                    if (lrow[e] + cb * wn[e] >= tau) cand[atomicAdd(&s_last, 1)] = (t << 16) | e;
+                    orow[e] = -INFINITY;
+                }
+            }
+            __syncthreads();
+            if (rsub) rsub[2] = route_gtimer();
+            const int ncand = s_last;
+            if (rsub) rsub[7] = static_cast<unsigned long long>(ncand);
+            for (int p = warp; p < ncand; p += kRouteWarps) {
+                const int t = cand[p] >> 16, e = cand[p] & 0xFFFF;
+                float acc[1][8];
+                warp_logits<ACT, 1, 8>(a.router_w, route_smem + static_cast<size_t>(t) * H * esz, H, E, e, 1, lane, acc);
+                if (lane == 0) lsel[static_cast<size_t>(t) * E + e] = acc[0][0];
+            }
+            __syncthreads();
+            if (rsub) rsub[3] = route_gtimer();
+        }
         constexpr int kPass = kRouteWarps * kPrefillEpw;
-        for (int eb = 0; eb < E; eb += kPass) {
+        for (int eb = 0; eb < E && !tc; eb += kPass) {
             const int e0 = eb + warp * kPrefillEpw;
             if (e0 < E) {
                 float acc[kPrefillEpw][8];
@@ -724,7 +807,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         if (warp < nt) {
             int sel;
             float g;
-            warp_topk<false>(lg + warp * E, E, k, lane, sel, g, s_scr + warp * 32);
+            warp_topk<false>((tc ? lsel : lg) + warp * E, E, k, lane, sel, g, s_scr + warp * 32);
+            if (rsub) rsub[4] = route_gtimer();
             if (lane < k) {
                 const size_t o = static_cast<size_t>(t0 + warp) * k + lane;
                 a.topk[o] = sel;
@@ -761,6 +845,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     }
     // ---------------- hand-off: the last CTA to finish runs phase B
     __syncthreads();
+    if (rsub) rsub[5] = route_gtimer();
+    if (rtr && threadIdx.x == 0) atomicMax(rtr + 1, static_cast<unsigned long long>(route_gtimer()));
     if (threadIdx.x == 0) {
         __threadfence();
         const int prev = atomicAdd(a.route_done, 1);
@@ -772,6 +858,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     RouteShared& rs = *reinterpret_cast<RouteShared*>(route_smem);
     route_phase_b(a, rs, route_smem + kRouteSharedBytes, DECODE);
     if (threadIdx.x == 0) *a.route_done = 0;
+    if (rtr && threadIdx.x == 0) rtr[2] = route_gtimer();
 }
 
 // prefill: places every assignment of routing CTA b (8 tokens) at
@@ -797,7 +884,8 @@ static size_t route_smem_bytes(const CallArgs& a, bool decode) {
                                   : static_cast<size_t>(kPrefillTokTile) * a.H * esz +
                                         static_cast<size_t>(kPrefillTokTile) * a.E * 4 +
                                         static_cast<size_t>(kPrefillTokTile) * kMaxTopK * 4 + static_cast<size_t>(a.E) * 4 +
-                                        8 + static_cast<size_t>(kPrefillTokTile) * 32 * 8;
+                                        8 + static_cast<size_t>(kPrefillTokTile) * 32 * 8 +
+                                        static_cast<size_t>(kPrefillTokTile) * a.E * 4 * 2 + static_cast<size_t>(a.E) * 4;
     return std::max(phase_a, kRouteSharedBytes + route_area_bytes(a.S, a.E));
 }
 
@@ -814,9 +902,16 @@ cudaError_t launch_route(const CallArgs& a, cudaStream_t s) {
         else k_route<ACT_FP32, true><<<grid, kRouteThreads, smem, s>>>(a);
     } else {
         const int grid = (a.T + kPrefillTokTile - 1) / kPrefillTokTile;
-        if (a.act == ACT_BF16) k_route<ACT_BF16, false><<<grid, kRouteThreads, smem, s>>>(a);
-        else k_route<ACT_FP32, false><<<grid, kRouteThreads, smem, s>>>(a);
-        k_perm_rows<<<grid, 256, 0, s>>>(a);
+        CallArgs b = a;
+        b.tc_router = 0;
+        if (router_tc_eligible(a)) {
+            const cudaError_t e = launch_router_tc(a, s);
+            if (e != cudaSuccess) return e;
+            b.tc_router = 1;
+        }
+        if (b.act == ACT_BF16) k_route<ACT_BF16, false><<<grid, kRouteThreads, smem, s>>>(b);
+        else k_route<ACT_FP32, false><<<grid, kRouteThreads, smem, s>>>(b);
+        k_perm_rows<<<grid, 256, 0, s>>>(b);
     }
     return cudaGetLastError();
 }

@@ -715,6 +715,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
     std::vector<Part> parts = {
         {Tm * H * 2, &a.xh},
         {Tm * E * 4, reinterpret_cast<void**>(&a.logits)},
+        {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.wnorm)},
         {Tm * k * 4, reinterpret_cast<void**>(&a.topk)},
         {Tm * k * 4, reinterpret_cast<void**>(&a.gates)},
         {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.counts)},
@@ -764,6 +765,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         if (cudaMalloc(&h->trace, trace_words(h) * 8) != cudaSuccess) return bail(MOE_ERR_OOM);
         reset_trace(h);
         a.trace = h->trace;
+        a.trace_ctas = h->num_sms;
     }
     if (umma) {
         // TMA descriptors over the gathered activations, h, and the resident shared experts
@@ -1200,7 +1202,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
     if (tc && tc->has_combine) CK(h, cudaEventRecord(tc->f3, s));
     {
         std::lock_guard<std::mutex> lk(h->mu);
-        h->st.kernel_launches += (decode ? 1 : 2) + nl;
+        h->st.kernel_launches += (decode ? 1 : 2 + (moe::router_tc_eligible(a) ? 2 : 0)) + nl;
     }
     if (le != cudaSuccess) return cuda_fail(h, le, "expert kernel launch");
     return MOE_OK;
@@ -1226,6 +1228,20 @@ int moe_sync(moe_handle* h) {
     if (dev_err != 0)
         record_error(h, MOE_ERR_TIMEOUT, "a kernel gave up a bounded wait (device error " + std::to_string(dev_err) +
                                              "); call moe_cache_config to reset");
+    if (h->trace && !h->last_fused) {
+        const size_t base = static_cast<size_t>(h->num_sms) * moe::kTracePoints + (moe::kTraceCalls - 1) * 4;
+        unsigned long long r[4];
+        CK(h, cudaMemcpy(r, h->trace + base, sizeof(r), cudaMemcpyDeviceToHost));
+        if (r[0] != ~0ull && r[2] != 0)
+            std::fprintf(stderr, "[moe] route: phase A %.2f us, phase B %.2f us\n", (r[1] - r[0]) * 1e-3, (r[2] - r[1]) * 1e-3);
+        unsigned long long q[8];
+        CK(h, cudaMemcpy(q, h->trace + base - 8, sizeof(q), cudaMemcpyDeviceToHost));
+        if (q[0] && q[5] >= q[0])
+            std::fprintf(stderr, "[moe] route CTA 0: staged %.2f, candidates %.2f, exact %.2f, top-k %.2f, end %.2f us; %llu candidates\n",
+                         (q[1] - q[0]) * 1e-3, (q[2] - q[0]) * 1e-3, (q[3] - q[0]) * 1e-3, (q[4] - q[0]) * 1e-3,
+                         (q[5] - q[0]) * 1e-3, q[7]);
+        reset_trace(h);
+    }
     if (h->trace && h->last_fused) {
         // the last decode call's phase marks: min / median / max over CTAs, in us after the first start
         const int G = h->num_sms, P = moe::kTracePoints;
