@@ -92,6 +92,7 @@ struct DecRoute {
     int32_t red_gen[kRedSlots];   // uses of each slot finished
     int32_t nu, n_miss, status, ok;
     unsigned long long t_copy0;
+    unsigned long long seqbuf[24];  // T = 1: this CTA's stage sequence, set up while P1 waits for its rows
     unsigned long long tks[kDecodeMaxT][32];  // top-k scratch of token t's warp
 };
 
@@ -664,6 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // this layer's table row before anything of this call changes it: CTA 0
         // rewrites entries of missed experts after the barrier below
         for (int e = tid; e < E; e += kThreads) R.trow[e] = __ldcg(a.table + static_cast<size_t>(a.layer) * E + e);
+        if (TT == 1 && tid == 32) {
+            // at T = 1 the call has k + n_shared active experts whatever the routing:
+            // the stage sequence's divisions run here, off the path to P3
+            StageSeq<FMT> tmp;
+            tmp.init(a, plan, k + ns, b, G);
+            *reinterpret_cast<StageSeq<FMT>*>(R.seqbuf) = tmp;
+        }
         if (staged) {
             if (!mbar_wait(&p1bar, 0, abort_flag, a.wait_ns)) atomicExch(a.dev_err, MOE_DEVERR_TIMEOUT_PRODUCER);
             xsrc = ring;
@@ -838,6 +846,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 d.ptr = slot >= 0 ? a.pool + static_cast<size_t>(slot) * B : nullptr;
                 d.row0 = r;
                 d.cnt = 1;
+                // a resident expert's per-tensor scales, now rather than at P3
+                d.pad = slot >= 0 ? 1 : 0;
+                if (slot >= 0) {
+                    if constexpr (FMT == FMT_NVFP4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(d.ptr + a.lay.gsc));
+                        d.gs[0] = v.x;
+                        d.gs[1] = v.y;
+                        d.gs[2] = v.z;
+                    } else {
+                        d.gs[0] = d.gs[1] = d.gs[2] = 1.0f;
+                    }
+                }
 #pragma unroll
                 for (int t = 0; t < kDecodeMaxT; ++t) {
                     d.tok[t] = t == 0 ? 0 : -1;
@@ -854,6 +874,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 d.ptr = a.shared_base + static_cast<size_t>(sidx) * B;
                 d.row0 = k + sidx;
                 d.cnt = 1;
+                d.pad = 1;
+                if constexpr (FMT == FMT_NVFP4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(d.ptr + a.lay.gsc));
+                    d.gs[0] = v.x;
+                    d.gs[1] = v.y;
+                    d.gs[2] = v.z;
+                } else {
+                    d.gs[0] = d.gs[1] = d.gs[2] = 1.0f;
+                }
 #pragma unroll
                 for (int t = 0; t < kDecodeMaxT; ++t) {
                     d.tok[t] = t == 0 ? 0 : -1;
@@ -927,6 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 d.gate[t] = 0.f;
             }
             d.cnt = 0;
+            d.pad = 0;  // per-tensor scales not loaded yet
             if (u < nu) {
                 const int s = R.trow[R.members[u]];
                 R.mslot[u] = s;
@@ -1146,8 +1176,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
 
     if (tid == 0) mark(5);
     // ---------------------------------------------------------------- P3: experts
+    static_assert(sizeof(StageSeq<FMT>) <= sizeof(DecRoute::seqbuf), "stage sequence buffer");
     StageSeq<FMT> seq;
-    seq.init(a, plan, na, b, G);
+    if (TT == 1) seq = *reinterpret_cast<const StageSeq<FMT>*>(R.seqbuf);
+    else seq.init(a, plan, na, b, G);
     const int nf1 = seq.count1(), nf2 = seq.count2();
     const int xp = H * 2 + 16, hp = I * 2 + 16;
 
@@ -1212,6 +1244,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         const int g = lane >> 2, q = lane & 3;
         // NVFP4 per-tensor scales live in the blobs
         for (int u = ct; u < na; u += 32 * kConsumers) {
+            if (plan[u].pad) continue;  // loaded with the plan
             if constexpr (FMT == FMT_NVFP4) {
                 const float4 v = __ldcg(reinterpret_cast<const float4*>(plan[u].ptr + a.lay.gsc));  // may be this call's copy
                 plan[u].gs[0] = v.x; plan[u].gs[1] = v.y; plan[u].gs[2] = v.z;

@@ -108,7 +108,7 @@ struct DecExpert {
     int32_t hrow[kDecodeMaxT];   // h row of token t, else -1
     float gate[kDecodeMaxT];     // routing gate of the expert's row n
     float gs[3];                 // per-tensor scales (filled by the expert kernel)
-    int32_t pad;
+    int32_t pad;                 // decode kernel: 1 once gs holds the per-tensor scales
 };
 static_assert(sizeof(DecExpert) == 128, "decode plan record");
 constexpr int kDecPlanHeader = 128;
