@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-FP32, BF16, NVFP4, MXFP4 = 0, 1, 2, 3
+FP32, BF16, NVFP4, MXFP4, FP8 = 0, 1, 2, 3, 4
 DECODE_MAX_T = 8
 
 
@@ -112,6 +112,8 @@ def dequant(fmt: int, t: dict, N: int, K: int) -> np.ndarray:
         data, sc, g = _c(t["data"], np.float32), None, 1.0
     elif fmt == BF16:
         data, sc, g = _c(t["data"], np.uint16), None, 1.0
+    elif fmt == FP8:
+        data, sc, g = _c(t["codes"], np.uint8), None, t["gscale"]
     else:
         data, sc = _c(t["codes"], np.uint8), _c(t["scales"], np.uint8)
         g = t.get("gscale", 1.0)

@@ -98,7 +98,7 @@ void orc_f32_to_bf16(const float* in, size_t n, uint16_t* out) {
     for (size_t i = 0; i < n; ++i) out[i] = orc_bf16_rne(in[i]);
 }
 
-enum { ORC_FP32 = 0, ORC_BF16 = 1, ORC_NVFP4 = 2, ORC_MXFP4 = 3 };
+enum { ORC_FP32 = 0, ORC_BF16 = 1, ORC_NVFP4 = 2, ORC_MXFP4 = 3, ORC_FP8 = 4 };
 
 /* Dequantise one [N, K] weight tensor stored row-major along K.
  *  FP32:  data = float[N*K]
@@ -106,7 +106,9 @@ enum { ORC_FP32 = 0, ORC_BF16 = 1, ORC_NVFP4 = 2, ORC_MXFP4 = 3 };
  *  NVFP4: data = packed codes uint8[N*K/2] (element 2i in the low nibble of
  *         byte i), scales = E4M3 bytes [N*K/16]; w = code * scale * gscale
  *  MXFP4: data = packed codes as above, scales = E8M0 bytes [N*K/32];
- *         w = code * scale */
+ *         w = code * scale
+ *  FP8:   data = E4M3 (FN) bytes uint8[N*K], one per element; no block
+ *         scales; w = code * gscale (one fp32 scale per tensor, as NVFP4's) */
 void orc_dequant(int fmt, const void* data, const uint8_t* scales, float gscale,
                  int N, int K, float* out) {
     for (int n = 0; n < N; ++n) {
@@ -117,6 +119,8 @@ void orc_dequant(int fmt, const void* data, const uint8_t* scales, float gscale,
                 w = ((const float*)data)[i];
             } else if (fmt == ORC_BF16) {
                 w = orc_bf16(((const uint16_t*)data)[i]);
+            } else if (fmt == ORC_FP8) {
+                w = orc_e4m3fn(((const uint8_t*)data)[i]) * gscale;
             } else {
                 uint8_t byte = ((const uint8_t*)data)[i / 2];
                 unsigned code = (i & 1) ? (byte >> 4) : (byte & 0xF);

@@ -16,6 +16,8 @@ loader consume):
 * NVFP4 / MXFP4: ``codes`` uint8 ``[N, K/2]`` with element 2i in the low nibble
   of byte i; ``scales`` uint8 ``[N, K/16]`` (E4M3 bytes, NVFP4) or
   ``[N, K/32]`` (E8M0 bytes, MXFP4); NVFP4 also has one fp32 ``gscale``.
+* FP8: ``codes`` uint8 ``[N, K]``, one E4M3 (FN) byte per element, and one
+  fp32 ``gscale`` per tensor.
 """
 from __future__ import annotations
 
@@ -31,8 +33,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "libsynth.so")
 _lib = None
 
-FMT_FP32, FMT_BF16, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2, 3
-FMT_NAMES = {"fp32": FMT_FP32, "bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4}
+FMT_FP32, FMT_BF16, FMT_NVFP4, FMT_MXFP4, FMT_FP8 = 0, 1, 2, 3, 4
+FMT_NAMES = {"fp32": FMT_FP32, "bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4, "fp8": FMT_FP8}
 ACT_FP32, ACT_BF16 = 0, 1
 
 # tensor tags inside a (layer, expert) key
@@ -62,6 +64,7 @@ def _L():
         lib.synth_fill_tab16_f32.argtypes = [vp, sz, u64, vp, i32]
         lib.synth_fill_nibbles.argtypes = [vp, sz, u64, vp, i32]
         lib.synth_fill_bytes.argtypes = [vp, sz, u64, ctypes.c_uint, ctypes.c_uint, i32]
+        lib.synth_fill_tab8.argtypes = [vp, sz, u64, vp, i32]
         lib.synth_fill_uniform.argtypes = [vp, sz, u64]
         _lib = lib
     return _lib
@@ -154,6 +157,43 @@ NVFP4_GSCALE = 1.561e-4
 MXFP4_SCALE_BYTES = (118, 121)
 
 
+def e4m3_encode_rne(v: np.ndarray) -> np.ndarray:
+    """Harness quantiser for FP8 weights: non-negative values -> E4M3 (FN)
+    bytes, rounded to nearest (ties to even) and saturated at 448. Exponent e
+    (bias 7) and 3 mantissa bits; below 2^-6 the code is subnormal, m * 2^-9.
+    Used only to build the FP8 code table below."""
+    v = np.asarray(v, np.float64)
+    assert np.all(v >= 0)
+    out = np.zeros(v.shape, np.int64)
+    sub = v < 2.0 ** -6
+    out[sub] = np.rint(v[sub] / 2.0 ** -9).astype(np.int64)  # 8 carries into exponent 1
+    e = np.floor(np.log2(np.where(sub, 1.0, v))).astype(np.int64)
+    m = np.rint((np.where(sub, 1.0, v) / 2.0 ** e - 1.0) * 8).astype(np.int64)
+    out[~sub] = ((e + 7) * 8 + m)[~sub]  # m = 8 carries into the next exponent
+    return np.minimum(out, 0x7E).astype(np.uint8)
+
+
+# FP8 weights: each byte is a draw from 256 E4M3 codes, the RNE encodings of the
+# N(0, 1) quantiles at (j + 0.5) / 256 scaled so that the largest is 448 (the
+# E4M3 maximum); the sign bit of the lower half set. With the per-tensor scale
+# below the weights come out with a standard deviation of about 0.02.
+FP8_QMAX = 448.0
+
+
+def _fp8_table() -> np.ndarray:
+    if "fp8" not in _TABS:
+        q = _normal_table()[128::256].astype(np.float64)  # 256 quantiles, ascending
+        mag = e4m3_encode_rne(np.abs(q) * (FP8_QMAX / np.abs(q).max()))
+        _TABS["fp8"] = np.where(q < 0, mag | 0x80, mag).astype(np.uint8)
+    return _TABS["fp8"]
+
+
+def fp8_gscale(std: float) -> float:
+    """Per-tensor scale that maps the FP8 code table to weights of std ~ ``std``."""
+    q = _normal_table()[128::256].astype(np.float64)
+    return std * np.abs(q).max() / FP8_QMAX
+
+
 # Test-only block-scale tables: every finite E4M3 byte (all but the two NaN
 # codes 0x7F, 0xFF: subnormals, zeros and negative scales included), and E8M0
 # exponent bytes 100..154 (2^-27 .. 2^27).
@@ -182,6 +222,12 @@ def code_bytes(k: int, n: int, out: np.ndarray | None = None) -> np.ndarray:
     if out is None:
         out = np.empty(n, dtype=np.uint8)
     _L().synth_fill_nibbles(_ptr(out), n, k, _ptr(_code_table()), _nthreads())
+    return out
+
+
+def fp8_bytes(k: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    _L().synth_fill_tab8(_ptr(out), n, k, _ptr(_fp8_table()), _nthreads())
     return out
 
 
@@ -231,6 +277,8 @@ class Shape:
             return 2 * n
         if self.fmt == FMT_NVFP4:
             return n // 2 + n // 16 + 3 * 4
+        if self.fmt == FMT_FP8:
+            return n + 3 * 4
         return n // 2 + n // 32
 
 
@@ -254,6 +302,10 @@ def _tensor(shape: Shape, seed: int, layer: int, expert: int, tag: int, N: int, 
         return {"data": normal_f32(kd, N * K, shape.w_std).reshape(N, K)}
     if shape.fmt == FMT_BF16:
         return {"data": normal_bf16(kd, N * K, shape.w_std).reshape(N, K)}
+    if shape.fmt == FMT_FP8:
+        u = uniform(key(seed, layer, expert, tag * 4 + PART_GSCALE), 1)[0]
+        g = np.float32(fp8_gscale(shape.w_std) * (0.9 + 0.2 * u))
+        return {"codes": fp8_bytes(kd, N * K).reshape(N, K), "gscale": float(g)}
     codes = code_bytes(kd, N * K // 2).reshape(N, K // 2)
     ks = key(seed, layer, expert, tag * 4 + PART_SCALE)
     nblk = N * K // (16 if shape.fmt == FMT_NVFP4 else 32)

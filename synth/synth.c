@@ -160,6 +160,25 @@ void synth_fill_bytes(uint8_t* out, size_t n, uint64_t key, unsigned lo, unsigne
     run_parallel(fill_bytes_range, &c, n, 8, nthreads);
 }
 
+/* ---- byte-table fills: out[i] = tab256[byte_i] ----------------------------- */
+
+typedef struct { uint8_t* out; uint64_t key; const uint8_t* tab; } tab8_ctx;
+
+static void fill_tab8_range(void* c, size_t lo, size_t hi) {
+    tab8_ctx* x = (tab8_ctx*)c;
+    size_t i = lo;
+    while (i < hi) {
+        uint64_t w = stream_word(x->key, i >> 3);
+        for (unsigned l = (unsigned)(i & 7); l < 8 && i < hi; ++l, ++i)
+            x->out[i] = x->tab[(w >> (8 * l)) & 0xFF];
+    }
+}
+
+void synth_fill_tab8(uint8_t* out, size_t n, uint64_t key, const uint8_t* tab256, int nthreads) {
+    tab8_ctx c = { out, key, tab256 };
+    run_parallel(fill_tab8_range, &c, n, 8, nthreads);
+}
+
 /* Uniform doubles in [0, 1) from the top 53 bits of each stream word. */
 void synth_fill_uniform(double* out, size_t n, uint64_t key) {
     for (size_t i = 0; i < n; ++i)

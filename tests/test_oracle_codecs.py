@@ -134,6 +134,24 @@ def test_dequant_fp4_matches_independent_decode(fmt):
         assert np.array_equal(ours, ref.astype(np.float32))
 
 
+def test_dequant_fp8_matches_independent_decode():
+    """FP8 weights: every E4M3 byte decoded by torch's float8_e4m3fn dtype,
+    times the per-tensor scale, equals the oracle's dequantisation."""
+    import synth
+    shape = synth.Shape("t", L=1, E=1, k=1, H=256, I=64, fmt=oracle.FP8, act=1)
+    w = synth.expert_weights(shape, 7, 0, 0)
+    for name, (N, K) in (("gate", (64, 256)), ("down", (256, 64))):
+        t = w[name]
+        ours = oracle.dequant(oracle.FP8, t, N, K)
+        ref = torch.from_numpy(t["codes"]).view(torch.float8_e4m3fn).float().numpy() * np.float32(t["gscale"])
+        assert np.array_equal(ours, ref)
+    # all finite bytes (subnormals, zeros, negatives, +-448) in one row, scale 2^-3
+    b = np.array([x for x in range(256) if x & 0x7F != 0x7F], np.uint8).reshape(1, -1)
+    ours = oracle.dequant(oracle.FP8, {"codes": b, "gscale": 0.125}, 1, b.shape[1])
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy() * np.float32(0.125)
+    assert np.array_equal(ours, ref)
+
+
 def test_dequant_bf16_fp32_identity():
     import synth
     for fmt in (oracle.FP32, oracle.BF16):

@@ -11,7 +11,7 @@ import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-FORMATS = [synth.FMT_FP32, synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4]
+FORMATS = [synth.FMT_FP32, synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8]
 
 
 def _eye_tensor(fmt, N, K, alpha_log2):
@@ -27,6 +27,10 @@ def _eye_tensor(fmt, N, K, alpha_log2):
         d = np.zeros((N, K), np.uint16)
         d[np.arange(m), np.arange(m)] = synth.f32_to_bf16_bits(np.array([alpha], np.float32))[0]
         return {"data": d}
+    if fmt == synth.FMT_FP8:
+        codes = np.zeros((N, K), np.uint8)
+        codes[np.arange(m), np.arange(m)] = 0x38  # E4M3 1.0
+        return {"codes": codes, "gscale": alpha}
     codes = np.zeros((N, K // 2), np.uint8)
     for i in range(m):
         # E2M1 code 2 is 1.0 (golden table); low nibble = even element
