@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_OOM, MOE_ERR_CUDA = 0, -1, -2, -3
 MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT, MOE_ERR_STATE = -4, -5, -6
-MOE_FMT_FP32, MOE_FMT_BF16, MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1, 2, 3
+MOE_FMT_FP32, MOE_FMT_BF16, MOE_FMT_NVFP4, MOE_FMT_MXFP4, MOE_FMT_FP8 = 0, 1, 2, 3, 4
 MOE_ACT_FP32, MOE_ACT_BF16 = 0, 1
 MOE_MODE_SWIGLU, MOE_MODE_LINEAR_TEST = 0, 1
 MOE_DECODE_MAX_T = 8

@@ -1,4 +1,4 @@
-// Decode call of the routed MoE layer (T <= 8 tokens, FP4 expert weights) in
+// Decode call of the routed MoE layer (T <= 8 tokens, FP4 or FP8 expert weights) in
 // one cooperative launch: router logits, softmax / top-k / renormalisation,
 // the permutation by expert, the device LRU lookup of the expert cache, the
 // copy of missed experts from the pinned host banks into their pool slots,
@@ -35,7 +35,9 @@
 // are both widened to f16 and multiplied there: the product has at most 6
 // significant bits and lies in [2^-10, 2688], so it is exact in f16; the fp32
 // per-tensor scale is applied after the dot product. MXFP4: the E8M0 scale is
-// applied in fp32 to each 32-element partial sum. Activations: each token row
+// applied in fp32 to each 32-element partial sum. FP8: E4M3 codes are exact in
+// f16 (|code| in [2^-9, 448]); the per-tensor scale comes after the dot
+// product, as for NVFP4. Activations: each token row
 // is scaled by a power of two so that its largest |x| lies in [2^14, 2^15)
 // before rounding to f16 (exact for every element the f16 normal range holds),
 // and h rows likewise by their token's largest |h|; the power of two is undone
@@ -67,8 +69,9 @@ constexpr int kLruCached = 4096;                        // pools up to this size
 
 template <int FMT>
 struct Fp4Cfg {
-    static constexpr int kSbpg = FMT == FMT_NVFP4 ? 8 : 4;
-    static constexpr int kChunkBytes = kTileRows * kChunkGroups * (64 + kSbpg);
+    static constexpr int kSbpg = tiled_scale_bytes(FMT);
+    static constexpr int kRowBytes = tiled_row_bytes(FMT);  // one tile row of one K group
+    static constexpr int kChunkBytes = kTileRows * kChunkGroups * kRowBytes;
     static constexpr int kStageBytes = 2 * kChunkBytes;
 };
 
@@ -270,19 +273,6 @@ __device__ __forceinline__ uint32_t f16x2_scaled(float lo, float hi, float sc) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// eight E4M3 bytes -> four f16x2 (bytes 2i, 2i+1 -> word i); exact
-__device__ __forceinline__ void e4m3x8_to_f16x2(uint2 v, uint32_t (&o)[4]) {
-    asm("{\n.reg .b16 l0, h0, l1, h1;\n"
-        "mov.b32 {l0, h0}, %4;\n"
-        "mov.b32 {l1, h1}, %5;\n"
-        "cvt.rn.f16x2.e4m3x2 %0, l0;\n"
-        "cvt.rn.f16x2.e4m3x2 %1, h0;\n"
-        "cvt.rn.f16x2.e4m3x2 %2, l1;\n"
-        "cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
-        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-        : "r"(v.x), "r"(v.y));
-}
-
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
     return *reinterpret_cast<uint32_t*>(&r);
@@ -299,6 +289,27 @@ template <int FMT>
 __device__ __forceinline__ void mma_group(const unsigned char* chunk, int ng, int w, int g, int q,
                                           const uint32_t (&b)[16], float (&acc0)[4], float (&acc1)[4]) {
     constexpr int kSbpg = Fp4Cfg<FMT>::kSbpg;
+    if constexpr (FMT == FMT_FP8) {
+        // E4M3 codes widen to f16 exactly; the per-tensor scale comes after
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint4 ra = lds128(chunk + fp8_code_off(ng, g, w, q, hf));
+            const uint4 rb = lds128(chunk + fp8_code_off(ng, g + 8, w, q, hf));
+            uint32_t oa[8], ob[8];
+            e4m3x8_to_f16x2(make_uint2(ra.x, ra.y), *reinterpret_cast<uint32_t(*)[4]>(oa));
+            e4m3x8_to_f16x2(make_uint2(ra.z, ra.w), *reinterpret_cast<uint32_t(*)[4]>(oa + 4));
+            e4m3x8_to_f16x2(make_uint2(rb.x, rb.y), *reinterpret_cast<uint32_t(*)[4]>(ob));
+            e4m3x8_to_f16x2(make_uint2(rb.z, rb.w), *reinterpret_cast<uint32_t(*)[4]>(ob + 4));
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int s = 4 * hf + x;  // MMA step: word x of the half, elements i = 0, 1 | 2, 3
+                const uint32_t A[4] = {oa[2 * x], ob[2 * x], oa[2 * x + 1], ob[2 * x + 1]};
+                if (s & 1) mma_f16(acc1, A, b[2 * s], b[2 * s + 1], acc1);
+                else mma_f16(acc0, A, b[2 * s], b[2 * s + 1], acc0);
+            }
+        }
+        return;
+    }
     const uint4 ra = lds128(chunk + fp4_code_off(ng, g, w, q));
     const uint4 rb = lds128(chunk + fp4_code_off(ng, g + 8, w, q));
     const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
@@ -532,13 +543,13 @@ struct StageSeq {
     // returns the number of copies of the stage (lanes at or above it have
     // none) and sets the stage's total bytes.
     __device__ int piece(int lane, const uint8_t*& src, uint32_t& bytes, uint32_t& off, uint32_t& total) const {
-        constexpr uint32_t row = 64 + Fp4Cfg<FMT>::kSbpg;  // bytes of one row of one K group
+        constexpr uint32_t row = Fp4Cfg<FMT>::kRowBytes;  // bytes of one row of one K group
         if (f < nf1) {
             const int c0 = c0_1(), nc = nc_1();
             uint32_t g = 0;
             for (int c = c0; c < c0 + nc; ++c) g += fp4_chunk_groups(G1k, c);
             total = static_cast<uint32_t>(kTileRows) * g * row;
-            src = plan[u].ptr + gu + static_cast<size_t>(ut) * gu_tile + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+            src = plan[u].ptr + gu + static_cast<size_t>(ut) * gu_tile + tile_chunk_off(c0, Fp4Cfg<FMT>::kRowBytes);
             bytes = total;
             off = 0;
             return 1;
@@ -550,7 +561,7 @@ struct StageSeq {
             uint32_t g = 0;
             for (int c = c0; c < c0 + nc; ++c) g += fp4_chunk_groups(G2k, c);
             total = static_cast<uint32_t>(kTileRows) * g * row;
-            src = plan[u0_].ptr + toff + fp4_chunk_off(c0, Fp4Cfg<FMT>::kSbpg);
+            src = plan[u0_].ptr + toff + tile_chunk_off(c0, Fp4Cfg<FMT>::kRowBytes);
             bytes = total;
             off = 0;
             return 1;
@@ -849,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 // a resident expert's per-tensor scales, now rather than at P3
                 d.pad = slot >= 0 ? 1 : 0;
                 if (slot >= 0) {
-                    if constexpr (FMT == FMT_NVFP4) {
+                    if constexpr (FMT == FMT_NVFP4 || FMT == FMT_FP8) {
                         const float4 v = __ldcg(reinterpret_cast<const float4*>(d.ptr + a.lay.gsc));
                         d.gs[0] = v.x;
                         d.gs[1] = v.y;
@@ -875,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 d.row0 = k + sidx;
                 d.cnt = 1;
                 d.pad = 1;
-                if constexpr (FMT == FMT_NVFP4) {
+                if constexpr (FMT == FMT_NVFP4 || FMT == FMT_FP8) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(d.ptr + a.lay.gsc));
                     d.gs[0] = v.x;
                     d.gs[1] = v.y;
@@ -1242,10 +1253,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // ---------------------------------------------------------------- consumers
         const int w = warp - 1, ct = tid - 32;
         const int g = lane >> 2, q = lane & 3;
-        // NVFP4 per-tensor scales live in the blobs
+        // NVFP4 / FP8 per-tensor scales live in the blobs
         for (int u = ct; u < na; u += 32 * kConsumers) {
             if (plan[u].pad) continue;  // loaded with the plan
-            if constexpr (FMT == FMT_NVFP4) {
+            if constexpr (FMT == FMT_NVFP4 || FMT == FMT_FP8) {
                 const float4 v = __ldcg(reinterpret_cast<const float4*>(plan[u].ptr + a.lay.gsc));  // may be this call's copy
                 plan[u].gs[0] = v.x; plan[u].gs[1] = v.y; plan[u].gs[2] = v.z;
             } else {
@@ -1479,7 +1490,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         c = 0;
                         ww = w2[half];
                         ng = p < nu_ ? seq.G2k : 0;
-                        off = p * kTileRows * seq.G2k * (64 + C::kSbpg);
+                        off = p * kTileRows * seq.G2k * C::kRowBytes;
                     }
                     if (ww < ng && !dead) {
                         const int hr = plan[u].hrow[g];
@@ -1622,13 +1633,17 @@ cudaError_t decode_set_attributes() {
     if ((e = set_attr<FMT_NVFP4, ACT_BF16>())) return e;
     if ((e = set_attr<FMT_NVFP4, ACT_FP32>())) return e;
     if ((e = set_attr<FMT_MXFP4, ACT_BF16>())) return e;
-    return set_attr<FMT_MXFP4, ACT_FP32>();
+    if ((e = set_attr<FMT_MXFP4, ACT_FP32>())) return e;
+    if ((e = set_attr<FMT_FP8, ACT_BF16>())) return e;
+    return set_attr<FMT_FP8, ACT_FP32>();
 }
 
 cudaError_t launch_decode(const CallArgs& a, int num_sms, cudaStream_t s, bool pdl) {
     const bool bf = a.act == ACT_BF16;
     if (a.fmt == FMT_NVFP4)
         return bf ? launch_one<FMT_NVFP4, ACT_BF16>(a, num_sms, s, pdl) : launch_one<FMT_NVFP4, ACT_FP32>(a, num_sms, s, pdl);
+    if (a.fmt == FMT_FP8)
+        return bf ? launch_one<FMT_FP8, ACT_BF16>(a, num_sms, s, pdl) : launch_one<FMT_FP8, ACT_FP32>(a, num_sms, s, pdl);
     return bf ? launch_one<FMT_MXFP4, ACT_BF16>(a, num_sms, s, pdl) : launch_one<FMT_MXFP4, ACT_FP32>(a, num_sms, s, pdl);
 }
 

@@ -6,12 +6,12 @@
 // Hits of the cache "run on the GPU" (freetoken.wiki architecture page, decode
 // paragraph); the expert weights come in the formats the FreeToken pages list
 // (bhrtaym-blog post, section on supported models and quantisation formats:
-// MXFP4, NVFP4, BF16).
+// MXFP4, NVFP4, FP8, BF16).
 //
 // Here: decode with BF16 weights (mma.sync m16n8k16 in swap-AB form: the weight
 // rows are the M = 16 operand, the tokens routed to the expert the N = 8
 // columns; bf16 operands, fp32 accumulation), the prefill combine, and plain
-// SIMT kernels for FP32 weights. Decode with FP4 weights runs in the fused
+// SIMT kernels for FP32 weights. Decode with FP4 or FP8 weights runs in the fused
 // decode kernel, prefill in the tensor-core grouped GEMMs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -339,7 +339,7 @@ cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
         n = a.act == ACT_BF16 ? launch_bf16_decode<ACT_BF16>(a, s, ev_gu, ev_down)
                               : launch_bf16_decode<ACT_FP32>(a, s, ev_gu, ev_down);
     } else {
-        return cudaErrorInvalidValue;  // FP4 decode runs in the fused decode kernel
+        return cudaErrorInvalidValue;  // FP4 / FP8 decode runs in the fused decode kernel
     }
     if (launches) *launches = n;
     return cudaGetLastError();

@@ -40,6 +40,19 @@ __device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
         : "r"(w));
 }
 
+// eight E4M3 bytes -> four f16x2 (bytes 2i, 2i+1 -> word i); exact
+__device__ __forceinline__ void e4m3x8_to_f16x2(uint2 v, uint32_t (&o)[4]) {
+    asm("{\n.reg .b16 l0, h0, l1, h1;\n"
+        "mov.b32 {l0, h0}, %4;\n"
+        "mov.b32 {l1, h1}, %5;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, l0;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, h0;\n"
+        "cvt.rn.f16x2.e4m3x2 %2, l1;\n"
+        "cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(v.x), "r"(v.y));
+}
+
 // eight E4M3 bytes -> eight floats (byte i -> o[i]); exact
 __device__ __forceinline__ void e4m3x8_to_f32(uint2 v, float (&o)[8]) {
     uint32_t h[4];

@@ -15,7 +15,7 @@ constexpr int kGroupK = 128;       // K elements per device-order group
 constexpr int kMaxSlots = 16384;   // pool slots (slot index fits 14 bits)
 constexpr int kSortMax = 16384;    // bitonic sort size bound for victim selection
 
-enum Fmt { FMT_FP32 = 0, FMT_BF16 = 1, FMT_NVFP4 = 2, FMT_MXFP4 = 3 };
+enum Fmt { FMT_FP32 = 0, FMT_BF16 = 1, FMT_NVFP4 = 2, FMT_MXFP4 = 3, FMT_FP8 = 4 };
 enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 
 // Device layout of one expert ("blob"), identical in the pinned host bank and
@@ -24,7 +24,7 @@ enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 // Within every weight row, K is stored in "device order": each group of 128
 // consecutive elements is reordered so that position 32q + 4s + i holds
 // element 16s + 4q + i of the group (q < 4, s < 8, i < 4). A warp lane with
-// quad index q then finds, in one contiguous 16-byte (FP4) or 64-byte (BF16)
+// quad index q then finds, in one contiguous 16-byte (FP4), 32-byte (FP8) or 64-byte (BF16)
 // run, its operands for the eight m16n8k16 MMA steps s of the group, and step s
 // covers exactly one 16-element NVFP4 scale block (half of an MXFP4 block).
 // Activations fed to the same MMAs are stored in the same order.
@@ -33,28 +33,37 @@ enum Act { ACT_FP32 = 0, ACT_BF16 = 1 };
 //   gu : gate/up rows [2I][H]. Rows come in blocks of 128: 64 gate rows then
 //        the 64 up rows of the same intermediate units (FP32: plain [gate I][up I]).
 //   d  : down rows [H][I].
-// FP4 blobs (NVFP4, MXFP4) are tiled for streaming: the gu region is I/8 tiles
-// (tile u: rows 0-7 = gate units 8u..8u+7, rows 8-15 = their up units), the d
-// region H/16 tiles (tile r: down rows 16r..16r+15); a tile is a run of chunks
-// of up to 8 K-groups (1024 elements), and chunk c with ng groups is
+// FP4 and FP8 blobs (NVFP4, MXFP4, FP8) are tiled for streaming: the gu region
+// is I/8 tiles (tile u: rows 0-7 = gate units 8u..8u+7, rows 8-15 = their up
+// units), the d region H/16 tiles (tile r: down rows 16r..16r+15); a tile is a
+// run of chunks of up to 8 K-groups (1024 elements), and chunk c with ng groups
+// is, for FP4,
 //   codes  [16 rows][ng * 64 bytes]   (16-byte units of row r XOR-swizzled,
 //                                      see fp4_code_off)
 //   scales [16 rows][ng * sbpg bytes] (sbpg = 8 E4M3 (NVFP4) or 4 E8M0 (MXFP4)
 //                                      bytes per group, canonical order)
+// and for FP8 (one E4M3 byte per element, no block scales)
+//   codes  [16 rows][ng * 128 bytes]  (see fp8_code_off)
 // so that one 16-row x 1024-K slice of a projection is one contiguous run.
-//   gsc: float[4] per-tensor scales (gate, up, down, 1) - NVFP4; else 1.
+//   gsc: float[4] per-tensor scales (gate, up, down, 1) - NVFP4 and FP8; else 1.
 struct BlobLayout {
     size_t gu, d, gsc, bytes;
-    size_t gu_tile, d_tile;  // FP4: bytes of one tile of each region
-    int sbpg;                // FP4: scale bytes per 128-element group
+    size_t gu_tile, d_tile;  // tiled formats: bytes of one tile of each region
+    int sbpg;                // FP4: scale bytes per 128-element group (FP8: 0)
+    int rowb;                // tiled formats: bytes of one tile row of one K group
 };
 
 constexpr int kTileRows = 16;
 constexpr int kChunkGroups = 8;
 
-// FP4 tiles: offset of chunk c (all earlier chunks are full)
-__host__ __device__ inline size_t fp4_chunk_off(int c, int sbpg) {
-    return static_cast<size_t>(kTileRows) * kChunkGroups * c * (64 + sbpg);
+// tiled formats: bytes of one tile row of one 128-element K group (codes and
+// block scales)
+__host__ __device__ constexpr int tiled_scale_bytes(int fmt) { return fmt == FMT_NVFP4 ? 8 : fmt == FMT_MXFP4 ? 4 : 0; }
+__host__ __device__ constexpr int tiled_row_bytes(int fmt) { return fmt == FMT_FP8 ? 128 : 64 + tiled_scale_bytes(fmt); }
+
+// tiled formats: offset of chunk c (all earlier chunks are full)
+__host__ __device__ inline size_t tile_chunk_off(int c, int rowb) {
+    return static_cast<size_t>(kTileRows) * kChunkGroups * c * rowb;
 }
 __host__ __device__ inline int fp4_chunk_groups(int G, int c) {
     return G - kChunkGroups * c < kChunkGroups ? G - kChunkGroups * c : kChunkGroups;
@@ -69,6 +78,14 @@ __host__ __device__ inline int fp4_code_off(int ng, int r, int w, int q) {
 }
 __host__ __device__ inline int fp4_scale_off(int ng, int sbpg, int r, int w) {
     return kTileRows * ng * 64 + r * ng * sbpg + w * sbpg;
+}
+// FP8: offset, inside its chunk (ng groups), of half hf (MMA steps 4hf..4hf+3)
+// of the 32 code bytes of row r, group w, lane quad q. A row of a group is one
+// 128-byte bank window; odd rows swap the two halves of each quad's run, so the
+// 8 lanes of a quarter-warp (rows 2m, 2m+1, quads 0-3) hit 8 distinct 16-byte
+// bank groups.
+__host__ __device__ inline int fp8_code_off(int ng, int r, int w, int q, int hf) {
+    return (r * ng + w) * 128 + (((2 * q + hf) ^ (r & 1)) * 16);
 }
 
 // Written by the cache kernel into mapped host memory; read by the host after
@@ -281,7 +298,7 @@ cudaError_t launch_experts(const CallArgs& a, cudaStream_t s, cudaEvent_t ev_gu,
 // decode (T <= 8) with FP4 weights: the whole call (router, top-k,
 // permutation, cache lookup, miss copies, gate/up, down, combine) in one
 // cooperative kernel
-inline bool decode_fused(int fmt, int T) { return (fmt == FMT_NVFP4 || fmt == FMT_MXFP4) && T <= kDecodeMaxT; }
+inline bool decode_fused(int fmt, int T) { return fmt >= FMT_NVFP4 && T <= kDecodeMaxT; }
 cudaError_t decode_set_attributes();
 // smem_ok: false when the shape's cache-lookup scratch does not fit
 cudaError_t launch_decode(const CallArgs& a, int num_sms, cudaStream_t s, bool pdl);

@@ -45,7 +45,7 @@ constexpr int BM = 128;  // weight rows per accumulator (MMA M)
 constexpr int BN = 128;  // tokens per tile (MMA N at most)
 constexpr int BK = 64;   // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;                   // BF16 weights: producer, MMA, 4 epilogue warps
-constexpr int kXformWarps = 8;                  // FP4 weights: + warps that widen the A tiles to BF16
+constexpr int kXformWarps = 8;                  // FP4 / FP8 weights: + warps that widen the A tiles to BF16
 constexpr int kThreadsFp4 = kThreads + 32 * kXformWarps;
 constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand tile
 
@@ -195,60 +195,109 @@ __device__ __forceinline__ int find_expert(const TileSched& ts, int na, int t) {
     return lo;
 }
 
-// FP4 weights (NVFP4 / MXFP4): the A tile of a pipeline stage (one 64-element
-// K block of 128 weight rows, or 2 x 128 for gate/up) is written by two
-// transform warps, each owning half of its rows. Warp w serves stage w mod 4
-// and only that stage, so it is never more than one use ahead of the MMA (an
-// mbarrier parity wait cannot tell use n from use n-2). A warp loads its rows'
-// codes and block scales from the tiled blob (one position ahead, into a second
-// register buffer), widens code x scale to BF16 (exact: an E2M1 value times an
-// E4M3 or E8M0 scale has at most 6 significant bits) and stores them in the
-// layout a TMA load with 128-byte swizzling would have produced (row r at
-// r*128 bytes, its 16-byte chunk c at position c ^ (r mod 8)).
-template <int MODE>
+// FP4 and FP8 weights (NVFP4 / MXFP4 / FP8): the A tile of a pipeline stage
+// (one 64-element K block of 128 weight rows, or 2 x 128 for gate/up) is
+// written by two transform warps, each owning half of its rows. Warp w serves
+// stage w mod 4 and only that stage, so it is never more than one use ahead of
+// the MMA (an mbarrier parity wait cannot tell use n from use n-2). A warp
+// loads its rows' codes and block scales from the tiled blob (FP4: one
+// position ahead, into a second register buffer; FP8, whose codes take twice
+// the registers: one buffer, the next position's lines prefetched into L2),
+// widens them to BF16 (exact: an E2M1 value times an E4M3 or E8M0 scale has at
+// most 6 significant bits, an E4M3 value 4) and stores them in the layout a
+// TMA load with 128-byte swizzling would have produced (row r at r*128 bytes,
+// its 16-byte chunk c at position c ^ (r mod 8)). FP8's per-tensor scale, like
+// NVFP4's, is applied in the epilogue.
+template <int FMT, int MODE>
 struct XRows {
     static constexpr int kRows = MODE == MODE_GU ? 4 : 2;  // rows per lane: 128 / 32 or 64 / 32
-    uint4 codes[kRows][2];
+    static constexpr int kUnits = FMT == FMT_FP8 ? 4 : 2;  // 16-byte code units per row and K block
+    uint4 codes[kRows][kUnits];
     uint2 sc[kRows];
 };
+
+// tile row `trow` and tile base of row `lane + 32 i` of part `part` of M tile mt
+template <int MODE>
+__device__ __forceinline__ const uint8_t* xrow(const CallArgs& a, const uint8_t* blob, int mt, int part, int lane, int i,
+                                               int& trow) {
+    if constexpr (MODE == MODE_GU) {
+        const int unit = mt * BM + lane + 32 * i;
+        trow = 8 * part + unit % 8;  // gate rows 0-7, up rows 8-15 of the unit tile
+        return blob + a.lay.gu + static_cast<size_t>(unit / 8) * a.lay.gu_tile;
+    } else {
+        const int row = mt * BM + 64 * part + lane + 32 * i;
+        trow = row % kTileRows;
+        return blob + a.lay.d + static_cast<size_t>(row / kTileRows) * a.lay.d_tile;
+    }
+}
 
 // loads, for K block kb of M tile mt of the expert at blob, the rows of part
 // `part` (GU: 0 = gate, 1 = up; DOWN: rows 64*part ..) that this lane owns
 template <int FMT, int MODE>
 __device__ __forceinline__ void xload(const CallArgs& a, const uint8_t* blob, int mt, int kb, int part, int lane,
-                                      XRows<MODE>& x) {
-    constexpr int kSbpg = FMT == FMT_NVFP4 ? 8 : 4;
+                                      XRows<FMT, MODE>& x) {
+    constexpr int kSbpg = tiled_scale_bytes(FMT);
     const int G = (MODE == MODE_GU ? a.H : a.I) / kGroupK;
     const int j = kb >> 1, h = kb & 1;  // K group, half of it
     const int c = j / kChunkGroups, w = j % kChunkGroups, ng = fp4_chunk_groups(G, c);
 #pragma unroll
-    for (int i = 0; i < XRows<MODE>::kRows; ++i) {
-        const uint8_t* tile;
+    for (int i = 0; i < XRows<FMT, MODE>::kRows; ++i) {
         int trow;
-        if constexpr (MODE == MODE_GU) {
-            const int unit = mt * BM + lane + 32 * i;
-            tile = blob + a.lay.gu + static_cast<size_t>(unit / 8) * a.lay.gu_tile;
-            trow = 8 * part + unit % 8;  // gate rows 0-7, up rows 8-15 of the unit tile
+        const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, lane, i, trow) + tile_chunk_off(c, tiled_row_bytes(FMT));
+        if constexpr (FMT == FMT_FP8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)  // quad 2h + u/2, half u%2
+                x.codes[i][u] = __ldg(reinterpret_cast<const uint4*>(chunk + fp8_code_off(ng, trow, w, 2 * h + (u >> 1), u & 1)));
         } else {
-            const int row = mt * BM + 64 * part + lane + 32 * i;
-            tile = blob + a.lay.d + static_cast<size_t>(row / kTileRows) * a.lay.d_tile;
-            trow = row % kTileRows;
+            x.codes[i][0] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h)));
+            x.codes[i][1] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h + 1)));
+            if constexpr (FMT == FMT_NVFP4)
+                x.sc[i] = __ldg(reinterpret_cast<const uint2*>(chunk + fp4_scale_off(ng, kSbpg, trow, w)));
+            else
+                x.sc[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(chunk + fp4_scale_off(ng, kSbpg, trow, w))), 0u);
         }
-        const uint8_t* chunk = tile + fp4_chunk_off(c, kSbpg);
-        x.codes[i][0] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h)));
-        x.codes[i][1] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h + 1)));
-        if constexpr (FMT == FMT_NVFP4)
-            x.sc[i] = __ldg(reinterpret_cast<const uint2*>(chunk + fp4_scale_off(ng, kSbpg, trow, w)));
-        else
-            x.sc[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(chunk + fp4_scale_off(ng, kSbpg, trow, w))), 0u);
+    }
+}
+
+// FP8: asks L2 for the 128-byte lines that xload will read for this position
+template <int MODE>
+__device__ __forceinline__ void xprefetch_fp8(const CallArgs& a, const uint8_t* blob, int mt, int kb, int part, int lane) {
+    const int G = (MODE == MODE_GU ? a.H : a.I) / kGroupK;
+    const int j = kb >> 1;
+    const int c = j / kChunkGroups, w = j % kChunkGroups, ng = fp4_chunk_groups(G, c);
+#pragma unroll
+    for (int i = 0; i < XRows<FMT_FP8, MODE>::kRows; ++i) {
+        int trow;
+        const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, lane, i, trow) + tile_chunk_off(c, tiled_row_bytes(FMT_FP8));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(chunk + (trow * ng + w) * 128) : "memory");
     }
 }
 
 // widens the loaded rows into the stage's A tile
 template <int FMT, int MODE>
-__device__ __forceinline__ void xstore(const XRows<MODE>& x, unsigned char* st, int part, int lane) {
+__device__ __forceinline__ void xstore(const XRows<FMT, MODE>& x, unsigned char* st, int part, int lane) {
 #pragma unroll
-    for (int i = 0; i < XRows<MODE>::kRows; ++i) {
+    for (int i = 0; i < XRows<FMT, MODE>::kRows; ++i) {
+        const int r = (MODE == MODE_GU ? 0 : 64 * part) + lane + 32 * i;  // row of the 128-row A tile
+        unsigned char* rowp = st + (MODE == MODE_GU ? part * kTileBytes : 0) + r * 128;
+        if constexpr (FMT == FMT_FP8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // 16 codes = K positions 16u .. 16u+15 -> chunks 2u, 2u+1
+                uint32_t f[8];
+                e4m3x8_to_f16x2(make_uint2(x.codes[i][u].x, x.codes[i][u].y), *reinterpret_cast<uint32_t(*)[4]>(f));
+                e4m3x8_to_f16x2(make_uint2(x.codes[i][u].z, x.codes[i][u].w), *reinterpret_cast<uint32_t(*)[4]>(f + 4));
+                uint32_t o[8];
+#pragma unroll
+                for (int y = 0; y < 8; ++y) {
+                    const __half2 hv = *reinterpret_cast<const __half2*>(&f[y]);
+                    __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(hv), __high2float(hv));
+                    o[y] = *reinterpret_cast<uint32_t*>(&bv);
+                }
+                *reinterpret_cast<uint4*>(rowp + (((2 * u) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(rowp + (((2 * u + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            continue;
+        }
         float s8[8];
         if constexpr (FMT == FMT_NVFP4) {
             e4m3x8_to_f32(x.sc[i], s8);
@@ -256,8 +305,6 @@ __device__ __forceinline__ void xstore(const XRows<MODE>& x, unsigned char* st, 
 #pragma unroll
             for (int b = 0; b < 4; ++b) s8[2 * b] = s8[2 * b + 1] = e8m0_to_f32((x.sc[i].x >> (8 * b)) & 0xFFu);
         }
-        const int r = (MODE == MODE_GU ? 0 : 64 * part) + lane + 32 * i;  // row of the 128-row A tile
-        unsigned char* rowp = st + (MODE == MODE_GU ? part * kTileBytes : 0) + r * 128;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const uint32_t wv[4] = {x.codes[i][u].x, x.codes[i][u].y, x.codes[i][u].z, x.codes[i][u].w};
@@ -288,7 +335,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
     using C = Cfg<MODE, kFp4>;
     extern __shared__ unsigned char dyn_raw[];
     __shared__ TileSched ts;
-    __shared__ const uint8_t* s_ptr[kFp4 ? kMaxExperts + 1 : 1];  // blob of each active expert (FP4)
+    __shared__ const uint8_t* s_ptr[kFp4 ? kMaxExperts + 1 : 1];  // blob of each active expert (FP4 / FP8)
     __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_afull[C::kStages];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
     __shared__ uint32_t s_tmem;
@@ -466,7 +513,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             }
         }
     } else if (warp >= 6) {
-        // ---------------- A-tile transform (FP4 weights, warps 6-13)
+        // ---------------- A-tile transform (FP4 / FP8 weights, warps 6-13)
         if constexpr (kFp4) {
             const int xw = warp - 6;
             const int sidx = xw % C::kStages, part = xw / C::kStages;
@@ -487,7 +534,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 mt = local / n_nt;
                 blob = s_ptr[u];
             };
-            auto process = [&](long long P, const XRows<MODE>& x) -> bool {
+            auto process = [&](long long P, const XRows<FMT, MODE>& x) -> bool {
                 const uint32_t ph = static_cast<uint32_t>((P / C::kStages) & 1);
                 int got = 1;
                 if (lane == 0) got = mbar_wait(&bar_empty[sidx], ph ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
@@ -502,10 +549,28 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 if (lane == 0) mbar_arrive(&bar_afull[sidx]);
                 return true;
             };
-            XRows<MODE> xa, xb;
             const uint8_t* blob;
             int mt, kb;
             long long P = sidx;
+            if constexpr (FMT == FMT_FP8) {
+                XRows<FMT, MODE> xa;
+                if (ok && P < npos) {
+                    where(P, blob, mt, kb);
+                    xload<FMT, MODE>(a, blob, mt, kb, part, lane, xa);
+                }
+                while (ok && P < npos) {
+                    const long long P1 = P + C::kStages;
+                    if (P1 < npos) {
+                        where(P1, blob, mt, kb);
+                        xprefetch_fp8<MODE>(a, blob, mt, kb, part, lane);
+                    }
+                    ok = process(P, xa);
+                    if (!ok || P1 >= npos) break;
+                    xload<FMT, MODE>(a, blob, mt, kb, part, lane, xa);
+                    P = P1;
+                }
+            } else {
+            XRows<FMT, MODE> xa, xb;
             if (ok && P < npos) {
                 where(P, blob, mt, kb);
                 xload<FMT, MODE>(a, blob, mt, kb, part, lane, xa);
@@ -525,6 +590,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 }
                 ok = process(P1, xb);
                 P = P2;
+            }
             }
         }
     } else {
@@ -549,7 +615,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * C::kAccCols;
             float gsc0 = 1.0f, gsc1 = 1.0f;
-            if (a.fmt == FMT_NVFP4) {
+            if (a.fmt == FMT_NVFP4 || a.fmt == FMT_FP8) {
                 const float* g = reinterpret_cast<const float*>(a.act_ptr[u] + a.lay.gsc);
                 gsc0 = MODE == MODE_GU ? g[0] : g[2];
                 gsc1 = g[1];
@@ -857,6 +923,8 @@ cudaError_t umma_set_attributes() {
     MOE_UMMA_ATTR(MODE_DOWN, FMT_NVFP4)
     MOE_UMMA_ATTR(MODE_GU, FMT_MXFP4)
     MOE_UMMA_ATTR(MODE_DOWN, FMT_MXFP4)
+    MOE_UMMA_ATTR(MODE_GU, FMT_FP8)
+    MOE_UMMA_ATTR(MODE_DOWN, FMT_FP8)
 #undef MOE_UMMA_ATTR
     return cudaSuccess;
 }
@@ -870,7 +938,7 @@ static CUtensorMap as_map(const UmmaMap& m) {
 template <int FMT>
 static void launch_gemms(const CallArgs& a, const UmmaMaps& maps, int num_sms, cudaStream_t s, cudaEvent_t ev_gu) {
     constexpr int threads = FMT == FMT_BF16 ? kThreads : kThreadsFp4;
-    // FP4 weights do not use the pool / shared tensor maps (their A tiles are built in shared memory)
+    // FP4 / FP8 weights do not use the pool / shared tensor maps (their A tiles are built in shared memory)
     const CUtensorMap pg = as_map(FMT == FMT_BF16 ? maps.pool_gu : maps.x);
     const CUtensorMap sg = as_map(FMT == FMT_BF16 ? maps.shared_gu : maps.x);
     const CUtensorMap pd = as_map(FMT == FMT_BF16 ? maps.pool_d : maps.x);
@@ -907,6 +975,7 @@ cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num
         case FMT_BF16: launch_gemms<FMT_BF16>(a, maps, num_sms, s, ev_gu); break;
         case FMT_NVFP4: launch_gemms<FMT_NVFP4>(a, maps, num_sms, s, ev_gu); break;
         case FMT_MXFP4: launch_gemms<FMT_MXFP4>(a, maps, num_sms, s, ev_gu); break;
+        case FMT_FP8: launch_gemms<FMT_FP8>(a, maps, num_sms, s, ev_gu); break;
         default: return cudaErrorInvalidValue;
     }
     if (launches) *launches = 3;

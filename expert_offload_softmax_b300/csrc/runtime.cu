@@ -186,7 +186,7 @@ int validate_desc(const moe_model_desc* d, std::string* why) {
     if (d->num_experts < 1 || d->num_experts > moe::kMaxExperts) return bad("num_experts must be in 1..1024");
     if (d->num_shared < 0 || d->num_shared > 1) return bad("num_shared must be 0 or 1");
     if (d->top_k < 1 || d->top_k > moe::kMaxTopK || d->top_k > d->num_experts) return bad("top_k must be in 1..min(E, 32)");
-    if (d->weight_fmt < 0 || d->weight_fmt > 3) return bad("unknown weight_fmt");
+    if (d->weight_fmt < 0 || d->weight_fmt > 4) return bad("unknown weight_fmt");
     if (d->act_dtype < 0 || d->act_dtype > 1) return bad("unknown act_dtype");
     if (d->act_mode < 0 || d->act_mode > 1) return bad("unknown act_mode");
     if (d->max_tokens < 0) return bad("max_tokens must be >= 0");
@@ -218,9 +218,10 @@ BlobLayout layout_for(const moe_model_desc& d) {
             L.gsc = align_up(o, 256); o = L.gsc + 16;
             break;
         default: {
-            L.sbpg = d.weight_fmt == moe::FMT_NVFP4 ? 8 : 4;
-            L.gu_tile = static_cast<size_t>(moe::kTileRows) * (H / moe::kGroupK) * (64 + L.sbpg);
-            L.d_tile = static_cast<size_t>(moe::kTileRows) * (I / moe::kGroupK) * (64 + L.sbpg);
+            L.sbpg = moe::tiled_scale_bytes(d.weight_fmt);
+            L.rowb = moe::tiled_row_bytes(d.weight_fmt);
+            L.gu_tile = static_cast<size_t>(moe::kTileRows) * (H / moe::kGroupK) * L.rowb;
+            L.d_tile = static_cast<size_t>(moe::kTileRows) * (I / moe::kGroupK) * L.rowb;
             L.gu = 0; o = (I / 8) * L.gu_tile;
             L.d = align_up(o, 256); o = L.d + (H / moe::kTileRows) * L.d_tile;
             L.gsc = align_up(o, 256); o = L.gsc + 16;
@@ -246,6 +247,15 @@ void reorder_row_fp4(const uint8_t* src, uint8_t* dst, int K) {
     }
 }
 
+void reorder_row_fp8(const uint8_t* src, uint8_t* dst, int K) {
+    for (int j = 0; j < K / 128; ++j) {
+        const uint8_t* s = src + 128 * j;
+        uint8_t* d = dst + 128 * j;
+        for (int q = 0; q < 4; ++q)
+            for (int st = 0; st < 8; ++st) std::memcpy(d + 32 * q + 4 * st, s + 16 * st + 4 * q, 4);
+    }
+}
+
 void reorder_row_bf16(const uint16_t* src, uint16_t* dst, int K) {
     for (int j = 0; j < K / 128; ++j) {
         const uint16_t* s = src + 128 * j;
@@ -262,7 +272,8 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
     const moe_tensor_host* ts[3] = {&w->gate, &w->up, &w->down};
     for (int i = 0; i < 3; ++i) {
         if (!ts[i]->data) { *why = "expert tensor data is NULL"; return MOE_ERR_INVALID; }
-        if (d.weight_fmt >= moe::FMT_NVFP4 && !ts[i]->scales) { *why = "expert scales are NULL"; return MOE_ERR_INVALID; }
+        const bool scaled = d.weight_fmt == moe::FMT_NVFP4 || d.weight_fmt == moe::FMT_MXFP4;
+        if (scaled && !ts[i]->scales) { *why = "expert scales are NULL"; return MOE_ERR_INVALID; }
     }
     std::memset(blob, 0, L.bytes);
     float* gsc = reinterpret_cast<float*>(blob + L.gsc);
@@ -288,6 +299,39 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
                 reorder_row_bf16(src + static_cast<size_t>(r) * I, dd + static_cast<size_t>(r) * I, I);
             break;
         }
+        case moe::FMT_FP8: {
+            // device-order rows, scattered into 16-row tiles of 1024-element chunks
+            std::vector<uint8_t> drow(std::max(H, I));
+            auto put_row = [&](uint8_t* tile, int r, const uint8_t* codes, int K) {
+                reorder_row_fp8(codes, drow.data(), K);
+                const int G = K / moe::kGroupK;
+                for (int c = 0; c * moe::kChunkGroups < G; ++c) {
+                    const int ng = moe::fp4_chunk_groups(G, c);
+                    uint8_t* chunk = tile + moe::tile_chunk_off(c, L.rowb);
+                    for (int w = 0; w < ng; ++w) {
+                        const int j = c * moe::kChunkGroups + w;
+                        for (int q = 0; q < 4; ++q)
+                            for (int hf = 0; hf < 2; ++hf)
+                                std::memcpy(chunk + moe::fp8_code_off(ng, r, w, q, hf),
+                                            drow.data() + j * 128 + 32 * q + 16 * hf, 16);
+                    }
+                }
+            };
+            for (int which = 0; which < 2; ++which) {
+                const uint8_t* src = static_cast<const uint8_t*>(ts[which]->data);
+                for (int i = 0; i < I; ++i)
+                    put_row(blob + L.gu + static_cast<size_t>(i / 8) * L.gu_tile, 8 * which + i % 8,
+                            src + static_cast<size_t>(i) * H, H);
+            }
+            const uint8_t* src = static_cast<const uint8_t*>(w->down.data);
+            for (int r = 0; r < H; ++r)
+                put_row(blob + L.d + static_cast<size_t>(r / moe::kTileRows) * L.d_tile, r % moe::kTileRows,
+                        src + static_cast<size_t>(r) * I, I);
+            gsc[0] = w->gate.global_scale;
+            gsc[1] = w->up.global_scale;
+            gsc[2] = w->down.global_scale;
+            break;
+        }
         default: {
             // device-order rows, scattered into 16-row tiles of 1024-element chunks
             const int blk = d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
@@ -298,7 +342,7 @@ int repack_expert(const moe_model_desc& d, const BlobLayout& L, const moe_expert
                 const int G = K / moe::kGroupK;
                 for (int c = 0; c * moe::kChunkGroups < G; ++c) {
                     const int ng = moe::fp4_chunk_groups(G, c);
-                    uint8_t* chunk = tile + moe::fp4_chunk_off(c, sbpg);
+                    uint8_t* chunk = tile + moe::tile_chunk_off(c, L.rowb);
                     for (int w = 0; w < ng; ++w) {
                         const int j = c * moe::kChunkGroups + w;
                         for (int q = 0; q < 4; ++q)
@@ -530,6 +574,7 @@ void service_call(moe_handle* h, const PendingCall& pc) {
         switch (h->d.weight_fmt) {
             case moe::FMT_FP32: wgu = 2 * I * H * 4; wd = H * I * 4; break;
             case moe::FMT_BF16: wgu = 2 * I * H * 2; wd = H * I * 2; break;
+            case moe::FMT_FP8: wgu = 2 * I * H; wd = H * I; break;
             default: {
                 const uint64_t blk = h->d.weight_fmt == moe::FMT_NVFP4 ? 16 : 32;
                 wgu = 2 * I * H / 2 + 2 * I * H / blk;
@@ -880,7 +925,7 @@ int take_pool(moe_handle* h, size_t S, void* pool_dev, size_t pool_bytes, uint8_
 int build_pool_maps(moe_handle* h) {
     h->maps.have_pool = false;
     if (h->maps.have_io && h->d.weight_fmt != moe::FMT_BF16) {
-        h->maps.have_pool = true;  // FP4 prefill builds its weight tiles in shared memory: no pool maps
+        h->maps.have_pool = true;  // FP4 / FP8 prefill builds its weight tiles in shared memory: no pool maps
     } else if (h->maps.have_io) {
         const uint64_t H = h->d.hidden, I = h->d.inter, S = h->S;
         if (!moe::umma_map_3d(&h->maps.pool_gu, h->pool + h->lay.gu, S, h->lay.bytes, 2 * I, H, 64) ||

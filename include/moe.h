@@ -69,7 +69,8 @@ typedef enum moe_weight_fmt {
     MOE_FMT_FP32 = 0,   /* float32 rows */
     MOE_FMT_BF16 = 1,   /* bfloat16 rows */
     MOE_FMT_NVFP4 = 2,  /* E2M1 codes, E4M3 scale per 16 elements, fp32 scale per tensor */
-    MOE_FMT_MXFP4 = 3   /* E2M1 codes, E8M0 scale per 32 elements */
+    MOE_FMT_MXFP4 = 3,  /* E2M1 codes, E8M0 scale per 32 elements */
+    MOE_FMT_FP8 = 4     /* E4M3 codes, fp32 scale per tensor */
 } moe_weight_fmt;
 
 typedef enum moe_act_dtype { MOE_ACT_FP32 = 0, MOE_ACT_BF16 = 1 } moe_act_dtype;
@@ -111,7 +112,13 @@ typedef struct moe_model_desc {
  *  FP32 / BF16: data = N*K elements; scales unused.
  *  NVFP4: data = N*K/2 bytes, element 2i in the low nibble of byte i;
  *         scales = N*K/16 E4M3 bytes (row-major [N, K/16]); global_scale used.
- *  MXFP4: data as NVFP4; scales = N*K/32 E8M0 bytes ([N, K/32]). */
+ *  MXFP4: data as NVFP4; scales = N*K/32 E8M0 bytes ([N, K/32]).
+ *  FP8:   data = N*K E4M3 (FN) bytes, one per element; scales unused;
+ *         global_scale used (weight = code * global_scale). The bhrtaym-blog
+ *         post names FP8 among the supported formats (section on supported
+ *         models and quantisation formats) without a layout; this is the
+ *         per-tensor-scaled E4M3 reading, the same per-tensor scale NVFP4
+ *         carries. */
 typedef struct moe_tensor_host {
     const void* data;
     const uint8_t* scales;
@@ -178,7 +185,7 @@ int moe_expert_bytes(const moe_model_desc* desc, size_t* bytes);
  * Host-only (no device is touched); for tools that prepare or inspect blobs.
  * MOE_ERR_INVALID for a bad shape, NULL pointers or a short buffer. The
  * formats are those the bhrtaym-blog post lists (section on supported models
- * and quantisation formats: MXFP4, NVFP4, BF16). */
+ * and quantisation formats: MXFP4, NVFP4, FP8, BF16). */
 int moe_repack_expert(const moe_model_desc* desc, const moe_expert_host* w, void* blob, size_t blob_bytes);
 
 /* Copies one expert from the canonical host layout into the library's pinned

@@ -264,6 +264,7 @@ class Shape:
     zipf_s: float = 0.0  # router skew exponent (0 = none)
     act_mode: int = 0    # 0 = SwiGLU, 1 = linear stand-in (closed-form tests)
     scale_table: tuple = ()  # FP4 block-scale bytes to draw from (uniformly), instead of the default range
+    code_table: tuple = ()   # FP8 code bytes to draw from (uniformly), instead of the default table
 
     def elems_per_expert(self) -> int:
         return 3 * self.H * self.I
@@ -305,7 +306,12 @@ def _tensor(shape: Shape, seed: int, layer: int, expert: int, tag: int, N: int, 
     if shape.fmt == FMT_FP8:
         u = uniform(key(seed, layer, expert, tag * 4 + PART_GSCALE), 1)[0]
         g = np.float32(fp8_gscale(shape.w_std) * (0.9 + 0.2 * u))
-        return {"codes": fp8_bytes(kd, N * K).reshape(N, K), "gscale": float(g)}
+        if shape.code_table:
+            tab = np.asarray(shape.code_table, dtype=np.uint8)
+            codes = tab[range_bytes(kd, N * K, 0, len(tab) - 1)].reshape(N, K)
+        else:
+            codes = fp8_bytes(kd, N * K).reshape(N, K)
+        return {"codes": codes, "gscale": float(g)}
     codes = code_bytes(kd, N * K // 2).reshape(N, K // 2)
     ks = key(seed, layer, expert, tag * 4 + PART_SCALE)
     nblk = N * K // (16 if shape.fmt == FMT_NVFP4 else 32)

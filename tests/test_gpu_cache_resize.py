@@ -60,7 +60,7 @@ def test_caller_owned_pool(fmt):
     assert buf.numel() == cap * _blob(moe, s)  # still the caller's: nothing freed it
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("fmt", [synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8])
 def test_resize_between_calls_matches_oracle(fmt):
     import expert_offload_softmax_b300 as moe
     from moe_harness import GpuStack, OracleStack

@@ -55,7 +55,7 @@ def test_tiny_fp32_workload():
     assert max(e["out_err"] for e in errs) < 1e-5
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8])
 @pytest.mark.parametrize("T", [1, 3, 8])
 def test_small_decode_all_formats(fmt, T):
     s = synth.Shape("small", L=3, E=16, k=4, H=384, I=256, fmt=fmt, act=synth.ACT_BF16)
@@ -63,7 +63,7 @@ def test_small_decode_all_formats(fmt, T):
     _run(s, 11, 3, 10 if T < 8 else 20, calls)
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8])
 @pytest.mark.parametrize("T", [9, 37, 200])
 def test_small_prefill_all_formats(fmt, T):
     s = synth.Shape("small", L=3, E=16, k=4, H=384, I=256, fmt=fmt, act=synth.ACT_BF16)
@@ -85,6 +85,29 @@ def test_prefill_bf16_tensor_core_shared_expert_fp32_act():
     outside the pool) and fp32 activations converted to bf16 in the gather."""
     s = synth.Shape("umma-shared", L=2, E=16, k=4, H=256, I=256, fmt=synth.FMT_BF16, act=synth.ACT_FP32, shared=1)
     _run(s, 23, 2, 32, [(0, 300, 0), (1, 41, 0), (1, 2, 1)], max_tokens=512)
+
+
+def test_fp8_prefill_tensor_core_multi_tile_ragged_chunks():
+    """FP8 prefill: 8 experts x top-2 over 1000 tokens (two 128-token tiles per
+    expert, the second ragged); H = 1152 gives a full 8-group chunk and a
+    1-group chunk per gate/up row and I = 384 one 3-group down chunk."""
+    s = synth.Shape("fp8-umma", L=2, E=8, k=2, H=1152, I=384, fmt=synth.FMT_FP8, act=synth.ACT_BF16)
+    _run(s, 24, 2, 16, [(0, 1000, 0), (1, 130, 1), (0, 17, 2), (1, 1, 3), (0, 8, 4)], max_tokens=1000)
+
+
+def test_fp8_shared_expert_fp32_activations_and_host_copied_misses():
+    """FP8 decode and prefill with an always-on shared expert and fp32
+    activations; then the same with the host's copy engines serving the
+    decode misses."""
+    s = synth.Shape("fp8-shared", L=2, E=16, k=4, H=256, I=256, fmt=synth.FMT_FP8, act=synth.ACT_FP32, shared=1)
+    calls = [(0, 1, 0), (1, 8, 0), (0, 300, 1), (1, 5, 2), (0, 1, 3)]
+    _run(s, 25, 2, 16, calls, max_tokens=512)  # 16 slots: one layer's experts, so every layer switch misses
+    _run(s, 25, 2, 16, calls, flags=8, max_tokens=512)
+
+
+def test_fp8_linear_mode():
+    s = synth.Shape("lin8", L=1, E=8, k=3, H=256, I=128, fmt=synth.FMT_FP8, act=synth.ACT_BF16, act_mode=1)
+    _run(s, 26, 1, 8, [(0, 6, 0), (0, 40, 1), (0, 1, 2)])
 
 
 def test_prefill_prefetch_next_layer():
@@ -200,6 +223,19 @@ def test_workload_decode_nvfp4_layer_subset():
     cap = synth.capacity_slots(synth.Shape("x", L=L, E=s.E, k=s.k, H=s.H, I=s.I, fmt=s.fmt, act=s.act), 0.25)
     calls = [(l, T, st) for st, T in enumerate((1, 8, 1, 8, 1)) for l in range(L)]
     _run(s, 0, L, cap, calls)
+
+
+def test_workload_decode_shape_fp8_layer_subset():
+    """The decode workload's shape (H2048, E256, k8, I512, Zipf s=1.0) with FP8
+    experts on 3 of its layers, pool of 300 slots; decode
+    T=1 and T=8, then one T=512 prefill call with outputs on 64 tokens."""
+    d = synth.DECODE_NVFP4
+    s = synth.Shape("decode-40L-H2048-E256-k8-I512-fp8", L=40, E=d.E, k=d.k, H=d.H, I=d.I, fmt=synth.FMT_FP8,
+                    act=synth.ACT_BF16, zipf_s=1.0)
+    L = 3
+    cap = 300  # 39% of those layers' experts: room for one prefill call's unique experts
+    calls = [(l, T, st) for st, T in enumerate((1, 8, 1)) for l in range(L)] + [(0, 512, 9)]
+    _run(s, 0, L, cap, calls, sample=64, max_tokens=512)
 
 
 def test_workload_prefill_bf16_layer_subset():

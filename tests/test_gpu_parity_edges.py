@@ -100,7 +100,7 @@ def _scaled_rows(shape, seed, layer, T, step):
     return synth.f32_to_bf16_bits(x)
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_NVFP4, synth.FMT_MXFP4])
+@pytest.mark.parametrize("fmt", [synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8])
 @pytest.mark.parametrize("T", [3, 8, 40])
 def test_activation_range(fmt, T):
     from moe_harness import GpuStack, OracleStack, compare, rel_err_rows, TOL
@@ -132,6 +132,26 @@ def test_every_block_scale_byte(fmt, table, T):
     try:
         for step in range(3):
             x = synth.hidden_states(s, 47, 0, T, step)
+            compare(g.forward(0, x), o.forward(0, x))
+    finally:
+        g.close()
+
+
+@pytest.mark.parametrize("T", [1, 8, 37])
+def test_every_fp8_code_byte(T):
+    """FP8 weights drawn from every finite E4M3 byte (zeros of both signs,
+    subnormals down to 2^-9, +-448): each widens to f16 / bf16 exactly."""
+    from moe_harness import GpuStack, OracleStack, compare
+    s = synth.Shape("codes8", L=1, E=16, k=4, H=512, I=256, fmt=synth.FMT_FP8, act=synth.ACT_BF16,
+                    code_table=synth.E4M3_FINITE_BYTES)
+    w = synth.expert_weights(s, 48, 0, 0)
+    drawn = set(np.unique(np.concatenate([w[p]["codes"].ravel() for p in ("gate", "up", "down")])).tolist())
+    assert drawn == set(synth.E4M3_FINITE_BYTES)
+    g = GpuStack(s, 48, 1, 16, max_tokens=64)
+    o = OracleStack(s, 48, 1, 16, prefetch=False)
+    try:
+        for step in range(3):
+            x = synth.hidden_states(s, 48, 0, T, step)
             compare(g.forward(0, x), o.forward(0, x))
     finally:
         g.close()

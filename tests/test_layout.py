@@ -18,7 +18,12 @@ Layout (one expert, sections 256-byte aligned, blob 1024-byte aligned):
     r*ng*64 + 16*((4w + q) ^ x), with x = 4 for odd r when ng is even, else 0.
     The device K order on FP4 codes: byte 16q + 2s + b of a group's 64 bytes
     holds canonical byte 8s + 2q + b.
-  * Then 4 fp32: the NVFP4 per-tensor scales of gate, up, down and 1.0
+  * FP8: the same 16-row tiles of chunks of up to 8 groups, each chunk
+    codes[16][ng*128 B] (one E4M3 byte per element, no block scales). Half
+    hf of the 32-byte run of quad q of group w of row r sits at
+    (r*ng + w)*128 + 16*((2q + hf) ^ (r & 1)); within a group the bytes are in
+    the device K order above.
+  * Then 4 fp32: the NVFP4 / FP8 per-tensor scales of gate, up, down and 1.0
     (all 1.0 for the other formats)."""
 import numpy as np
 import pytest
@@ -75,6 +80,22 @@ def _fp4_row(rd, tile, r, K, sb):
     return canon, scales
 
 
+def _fp8_row(rd, tile, r, K):
+    """Canonical E4M3 codes (K bytes) of tile row r."""
+    G = K // 128
+    dev = np.empty(K, np.uint8)
+    for c in range((G + 7) // 8):
+        ng = min(8, G - 8 * c)
+        chunk = tile + 16 * 8 * c * 128
+        for w in range(ng):
+            j = 8 * c + w
+            for q in range(4):
+                for hf in range(2):
+                    dev[128 * j + 32 * q + 16 * hf:128 * j + 32 * q + 16 * hf + 16] = \
+                        rd.take(chunk + (r * ng + w) * 128 + 16 * ((2 * q + hf) ^ (r & 1)), 16)
+    return _canon_from_device_k(dev, 1)
+
+
 def _decode(fmt, H, I, blob):
     rd = Reader(blob)
     out = {"gate": {}, "up": {}, "down": {}}
@@ -98,6 +119,18 @@ def _decode(fmt, H, I, blob):
             dn[row] = _canon_from_device_k(rd.take(d + row * I * 2, I * 2).view(np.uint16), 2)
         out["gate"]["data"], out["up"]["data"], out["down"]["data"] = g, u, dn
         gsc = _a(d + H * I * 2, 256)
+    elif fmt == synth.FMT_FP8:
+        gu_tile, d_tile = 16 * H, 16 * I
+        for name in ("gate", "up"):
+            out[name]["codes"] = np.empty((I, H), np.uint8)
+        for unit in range(I):
+            for which, name in ((0, "gate"), (1, "up")):
+                out[name]["codes"][unit] = _fp8_row(rd, (unit // 8) * gu_tile, 8 * which + unit % 8, H)
+        d = _a((I // 8) * gu_tile, 256)
+        out["down"]["codes"] = np.empty((H, I), np.uint8)
+        for row in range(H):
+            out["down"]["codes"][row] = _fp8_row(rd, d + (row // 16) * d_tile, row % 16, I)
+        gsc = _a(d + (H // 16) * d_tile, 256)
     else:
         sb = 8 if fmt == synth.FMT_NVFP4 else 4
         gu_tile = 16 * (H // 128) * (64 + sb)
@@ -127,6 +160,7 @@ def _decode(fmt, H, I, blob):
     (synth.FMT_NVFP4, 1152, 256),   # gate/up rows: a full 8-group chunk and a 1-group chunk
     (synth.FMT_MXFP4, 1152, 384),   # down rows: one 3-group chunk (odd ng: no swizzle)
     (synth.FMT_NVFP4, 256, 1152),
+    (synth.FMT_FP8, 1152, 384),     # gate/up: an 8-group and a 1-group chunk; down: one 3-group chunk
 ])
 def test_repacked_blob_decodes_to_the_canonical_weights(fmt, H, I):
     act = synth.ACT_FP32 if fmt == synth.FMT_FP32 else synth.ACT_BF16
@@ -143,7 +177,7 @@ def test_repacked_blob_decodes_to_the_canonical_weights(fmt, H, I):
             if key in w[name]:
                 np.testing.assert_array_equal(got[name][key], np.asarray(w[name][key]).reshape(got[name][key].shape))
     want = [1.0, 1.0, 1.0, 1.0]
-    if fmt == synth.FMT_NVFP4:
+    if fmt in (synth.FMT_NVFP4, synth.FMT_FP8):
         want = [w["gate"]["gscale"], w["up"]["gscale"], w["down"]["gscale"], 1.0]
     np.testing.assert_array_equal(got["gsc"], np.array(want, np.float32))
 
