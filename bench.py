@@ -12,7 +12,7 @@ once with every expert resident and once with a pool of 50% and next-layer
 prefetch.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|decode8|prefill|large|large_prefill|stress]
+                    [--workload decode|decode8|prefill|large|large_prefill|stress|decode_fp8|prefill_fp8]
 
 Three passes run over the same step sequence, each from the same cache state
 (the pool is rebuilt and the same W warm-up steps run first): the timed pass
@@ -52,6 +52,8 @@ WORKLOADS = {
     "large": (synth.LARGE_MXFP4, 1, 0.2, 0, 24, 0.0),
     "large_prefill": (synth.LARGE_MXFP4, 2048, 0.2, 0, 24, 0.0),
     "stress": (synth.STRESS_NVFP4, 1, 0.10, 0, 16, 0.7),
+    "decode_fp8": (synth.DECODE_FP8, 1, 0.25, 0, 40, 0.0),
+    "prefill_fp8": (synth.PREFILL_FP8, 4096, 0.5, 1, 40, 0.0),
 }
 
 PREFILL_LAYERS = 4  # layers of the prefill stack in the default line's prefill object
@@ -466,6 +468,21 @@ def prefill_section(pre):
     return out
 
 
+def _dtype_str(fmt, T):
+    """The arithmetic the path computes in, for the JSON line's dtype."""
+    if fmt == synth.FMT_BF16:
+        return "bf16 x bf16, fp32 accumulate"
+    if fmt == synth.FMT_FP32:
+        return "fp32"
+    wide = "f16" if T <= 8 else "bf16"
+    w = {synth.FMT_NVFP4: "nvfp4 weights (E2M1 code x E4M3 block scale, exact in %s)" % wide,
+         synth.FMT_MXFP4: "mxfp4 weights (E2M1 code exact in %s, E8M0 block scale %s)" % (
+             wide, "in fp32 per 32-element partial sum" if T <= 8 else "folded in, exact in bf16"),
+         synth.FMT_FP8: "fp8 weights (E4M3 code exact in %s, per-tensor scale after the dot product)" % wide}[fmt]
+    act = ("activations scaled by a power of two per token row into f16" if T <= 8 else "bf16 activations")
+    return w + " x " + act + ", fp32 accumulate"
+
+
 def make_line(args, world, meas, blob_bytes):
     """The bench's JSON line from one run's measurements: meas holds the timed
     and end-to-end durations (ms, max over ranks), the library's timing and
@@ -485,7 +502,7 @@ def make_line(args, world, meas, blob_bytes):
             "down": (timing["down_ms"], timing["down_bytes"])}
     if timing["combine_ms"] > 0:
         kern["combine"] = (timing["combine_ms"], timing["combine_bytes"])
-    fused_decode = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4)
+    fused_decode = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8)
     if fused_decode:
         # one kernel does the whole call: routing, cache lookup, gate/up, down, combine
         kern = {"gate_up": (timing["gate_up_ms"], timing["gate_up_bytes"] + timing["down_bytes"])}
@@ -511,15 +528,11 @@ def make_line(args, world, meas, blob_bytes):
     cpu = cpu_baseline(shape, T, L, budget_s=args.cpu_budget) if world == 1 else None
     ws_bytes = (stats["hits"] + stats["misses"]) * blob // max(1, K)
     cap_hits = stats["hits"] + stats["misses"]
-    dev_copies = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4) and not (flags & 8)
+    dev_copies = T <= 8 and shape.fmt in (synth.FMT_NVFP4, synth.FMT_MXFP4, synth.FMT_FP8) and not (flags & 8)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("bf16 x bf16, fp32 accumulate" if shape.fmt == synth.FMT_BF16 else
-                                       "%s weights (code x block scale exact in %s) x activations scaled by "
-                                       "a power of two per token row into %s, fp32 accumulate" % (
-                                           "nvfp4" if shape.fmt == synth.FMT_NVFP4 else "mxfp4",
-                                           "f16" if T <= 8 else "bf16", "f16" if T <= 8 else "bf16")),
+        "vs_baseline": None, "dtype": _dtype_str(shape.fmt, T),
         "data": "synthetic (seeded; random weights of the stated shape)",
         "config": {"workload": shape.name,
                    "T": T, "layers": L, "pool_slots": S, "pool_frac": frac,

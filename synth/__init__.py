@@ -294,7 +294,14 @@ LARGE_MXFP4 = Shape("large-24L-H4096-E256+1-k8-I2048-mxfp4", L=24, E=256, k=8, H
 STRESS_NVFP4 = Shape("stress-16L-H6144-E160-k8-I2048-nvfp4", L=16, E=160, k=8, H=6144, I=2048,
                      fmt=FMT_NVFP4, act=ACT_BF16, zipf_s=1.1)
 
-SHAPES = {s.name: s for s in (TINY_FP32, DECODE_NVFP4, PREFILL_BF16, LARGE_MXFP4, STRESS_NVFP4)}
+# The decode and prefill stacks' shape with FP8 experts (the fourth weight format).
+DECODE_FP8 = Shape("decode-40L-H2048-E256-k8-I512-fp8", L=40, E=256, k=8, H=2048, I=512,
+                   fmt=FMT_FP8, act=ACT_BF16, zipf_s=1.0)
+PREFILL_FP8 = Shape("prefill-40L-H2048-E256-k8-I512-fp8", L=40, E=256, k=8, H=2048, I=512,
+                    fmt=FMT_FP8, act=ACT_BF16)
+
+SHAPES = {s.name: s for s in (TINY_FP32, DECODE_NVFP4, PREFILL_BF16, LARGE_MXFP4, STRESS_NVFP4,
+                              DECODE_FP8, PREFILL_FP8)}
 
 
 def _tensor(shape: Shape, seed: int, layer: int, expert: int, tag: int, N: int, K: int) -> dict:
