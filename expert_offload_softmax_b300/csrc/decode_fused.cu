@@ -252,21 +252,6 @@ __device__ __forceinline__ bool bar_wait(const CallArgs& a, const unsigned long 
     return true;
 }
 
-// power of two p with max|v| * p in [2^14, 2^15) (1 for 0 or non-finite), and 1/p
-__device__ __forceinline__ void pow2_scale(unsigned int maxbits, float& sc, float& un) {
-    const int be = static_cast<int>((maxbits >> 23) & 0xFFu);
-    if (maxbits == 0u || be == 0xFF) {
-        sc = 1.0f;
-        un = 1.0f;
-        return;
-    }
-    int s = 141 - be;  // |v| < 2^(be - 126): |v| * 2^s < 2^15
-    s = s > 127 ? 127 : s;
-    sc = __uint_as_float(static_cast<unsigned int>(127 + s) << 23);
-    const int u = -s;  // >= -127
-    un = u >= -126 ? __uint_as_float(static_cast<unsigned int>(127 + u) << 23) : __uint_as_float(0x00400000u);
-}
-
 // f16 of v * sc, two at a time (round to nearest)
 __device__ __forceinline__ uint32_t f16x2_scaled(float lo, float hi, float sc) {
     __half2 h = __floats2half2_rn(lo * sc, hi * sc);

@@ -40,6 +40,21 @@ __device__ __forceinline__ void fp4x8_to_f16x2(uint32_t w, uint32_t (&o)[4]) {
         : "r"(w));
 }
 
+// power of two p with max|v| * p in [2^14, 2^15) (1 for 0 or non-finite), and 1/p
+__device__ __forceinline__ void pow2_scale(unsigned int maxbits, float& sc, float& un) {
+    const int be = static_cast<int>((maxbits >> 23) & 0xFFu);
+    if (maxbits == 0u || be == 0xFF) {
+        sc = 1.0f;
+        un = 1.0f;
+        return;
+    }
+    int s = 141 - be;  // |v| < 2^(be - 126): |v| * 2^s < 2^15
+    s = s > 127 ? 127 : s;
+    sc = __uint_as_float(static_cast<unsigned int>(127 + s) << 23);
+    const int u = -s;  // >= -127
+    un = u >= -126 ? __uint_as_float(static_cast<unsigned int>(127 + u) << 23) : __uint_as_float(0x00400000u);
+}
+
 // eight E4M3 bytes -> four f16x2 (bytes 2i, 2i+1 -> word i); exact
 __device__ __forceinline__ void e4m3x8_to_f16x2(uint2 v, uint32_t (&o)[4]) {
     asm("{\n.reg .b16 l0, h0, l1, h1;\n"

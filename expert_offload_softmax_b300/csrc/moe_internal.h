@@ -182,7 +182,10 @@ struct CallArgs {
     int32_t* e2u;          // [E] active index of routed expert e, or -1
     int32_t* tok_row;      // [(E + n_shared) * 8] decode: h row of (active u, token t) or -1
     int32_t* act_slot;     // [E + n_shared]  pool slot of the active expert; shared: -(1 + layer*n_shared + s)
-    void* xperm;           // [T*k + T*n_shared][H] bf16 gathered activations, device K-order (prefill, BF16)
+    void* xperm;           // [T*k + T*n_shared][H] gathered activations, device K-order (prefill): bf16,
+                           // or f16 scaled per token row (NVFP4 / FP8 weights)
+    float* xsc;            // [T] prefill, NVFP4 / FP8 weights: power of two of each token row in xperm
+    float* xunr;           // [T*k + T*n_shared] its inverse, per gathered row
     int32_t* dev_err;      // [1] sticky device error word (bounded waits that gave up)
     int32_t* route_done;   // [1] routing CTAs finished in this call (0 between calls)
     // prefill permutation, computed in parts: each routing CTA b (8 tokens)

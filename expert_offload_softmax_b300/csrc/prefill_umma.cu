@@ -45,7 +45,7 @@ constexpr int BM = 128;  // weight rows per accumulator (MMA M)
 constexpr int BN = 128;  // tokens per tile (MMA N at most)
 constexpr int BK = 64;   // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;                   // BF16 weights: producer, MMA, 4 epilogue warps
-constexpr int kXformWarps = 8;                  // FP4 / FP8 weights: + warps that widen the A tiles to BF16
+constexpr int kXformWarps = 16;                 // FP4 / FP8 weights: + warps that widen the A tiles (4 per stage)
 constexpr int kThreadsFp4 = kThreads + 32 * kXformWarps;
 constexpr int kTileBytes = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand tile
 
@@ -55,7 +55,7 @@ template <int MODE, bool FP4 = false>
 struct Cfg {
     static constexpr int kATiles = MODE == MODE_GU ? 2 : 1;           // gate + up, or down
     static constexpr int kStageBytes = (kATiles + 1) * kTileBytes;   // A tiles + B tile
-    // FP4: 4 stages, each written by two transform warps (see xform_rows)
+    // FP4 / FP8: 4 stages, each written by four transform warps (see XPart)
     static constexpr int kStages = (MODE == MODE_GU || FP4) ? 4 : 6;
     static constexpr int kAccCols = kATiles * BN;                    // TMEM columns per accumulator set
     static constexpr int kTmemCols = 2 * kAccCols;                   // double-buffered: 512 / 256
@@ -141,6 +141,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// the same for f16 A and B (A/B type fields 0)
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// gate/up with NVFP4 or FP8 weights runs on f16 operands: the codes (times
+// NVFP4's E4M3 block scale) widen to f16 exactly in one conversion, and each
+// token row of X is scaled by a power of two into f16's range (exact for every
+// element of the row within 2^29 of its largest); everything else is bf16
+template <int FMT, int MODE>
+__host__ __device__ constexpr bool f16_operands() {
+    return MODE == MODE_GU && (FMT == FMT_NVFP4 || FMT == FMT_FP8);
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n.reg .pred p;\n"
@@ -153,6 +167,21 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                  : "memory");
+}
+
+// this thread's TMEM lane, 16 consecutive fp32 columns starting at taddr
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // this thread's TMEM lane, 32 consecutive fp32 columns starting at taddr
@@ -197,7 +226,7 @@ __device__ __forceinline__ int find_expert(const TileSched& ts, int na, int t) {
 
 // FP4 and FP8 weights (NVFP4 / MXFP4 / FP8): the A tile of a pipeline stage
 // (one 64-element K block of 128 weight rows, or 2 x 128 for gate/up) is
-// written by two transform warps, each owning half of its rows. Warp w serves
+// written by four transform warps, each owning a quarter of its rows. Warp w serves
 // stage w mod 4 and only that stage, so it is never more than one use ahead of
 // the MMA (an mbarrier parity wait cannot tell use n from use n-2). A warp
 // loads its rows' codes and block scales from the tiled blob (FP4: one
@@ -208,31 +237,40 @@ __device__ __forceinline__ int find_expert(const TileSched& ts, int na, int t) {
 // TMA load with 128-byte swizzling would have produced (row r at r*128 bytes,
 // its 16-byte chunk c at position c ^ (r mod 8)). FP8's per-tensor scale, like
 // NVFP4's, is applied in the epilogue.
+// the rows of a stage's A tiles that transform warp `part` (0..3) writes: GU
+// tile part % 2 (gate, up), rows 64 (part / 2) .. + 63; DOWN rows 32 part .. + 31
+template <int MODE>
+struct XPart {
+    static constexpr int kParts = kXformWarps / 4;
+    static constexpr int kRows = (MODE == MODE_GU ? 2 * BM : BM) / kParts;
+    __device__ static int tile(int part) { return MODE == MODE_GU ? part & 1 : 0; }
+    __device__ static int row0(int part) { return MODE == MODE_GU ? (part >> 1) * kRows : part * kRows; }
+};
+
 template <int FMT, int MODE>
 struct XRows {
-    static constexpr int kRows = MODE == MODE_GU ? 4 : 2;  // rows per lane: 128 / 32 or 64 / 32
+    static constexpr int kRows = XPart<MODE>::kRows / 32;  // rows per lane
     static constexpr int kUnits = FMT == FMT_FP8 ? 4 : 2;  // 16-byte code units per row and K block
-    uint4 codes[kRows][kUnits];
+    uint4 codes[kRows][kUnits];  // FP8: piece 4i + j = codes[i][j], see xload
     uint2 sc[kRows];
 };
 
-// tile row `trow` and tile base of row `lane + 32 i` of part `part` of M tile mt
+// tile row `trow` and tile base of row `rl` of part `part` of M tile mt
 template <int MODE>
-__device__ __forceinline__ const uint8_t* xrow(const CallArgs& a, const uint8_t* blob, int mt, int part, int lane, int i,
-                                               int& trow) {
+__device__ __forceinline__ const uint8_t* xrow(const CallArgs& a, const uint8_t* blob, int mt, int part, int rl, int& trow) {
     if constexpr (MODE == MODE_GU) {
-        const int unit = mt * BM + lane + 32 * i;
-        trow = 8 * part + unit % 8;  // gate rows 0-7, up rows 8-15 of the unit tile
+        const int unit = mt * BM + XPart<MODE>::row0(part) + rl;
+        trow = 8 * XPart<MODE>::tile(part) + unit % 8;  // gate rows 0-7, up rows 8-15 of the unit tile
         return blob + a.lay.gu + static_cast<size_t>(unit / 8) * a.lay.gu_tile;
     } else {
-        const int row = mt * BM + 64 * part + lane + 32 * i;
+        const int row = mt * BM + XPart<MODE>::row0(part) + rl;
         trow = row % kTileRows;
         return blob + a.lay.d + static_cast<size_t>(row / kTileRows) * a.lay.d_tile;
     }
 }
 
 // loads, for K block kb of M tile mt of the expert at blob, the rows of part
-// `part` (GU: 0 = gate, 1 = up; DOWN: rows 64*part ..) that this lane owns
+// `part` (see XPart) that this lane owns
 template <int FMT, int MODE>
 __device__ __forceinline__ void xload(const CallArgs& a, const uint8_t* blob, int mt, int kb, int part, int lane,
                                       XRows<FMT, MODE>& x) {
@@ -240,15 +278,21 @@ __device__ __forceinline__ void xload(const CallArgs& a, const uint8_t* blob, in
     const int G = (MODE == MODE_GU ? a.H : a.I) / kGroupK;
     const int j = kb >> 1, h = kb & 1;  // K group, half of it
     const int c = j / kChunkGroups, w = j % kChunkGroups, ng = fp4_chunk_groups(G, c);
+    if constexpr (FMT == FMT_FP8) {
+        // FP8: step i of lane l takes 16-byte unit l & 3 of the K block (quad 2h + (l & 3) / 2, half
+        // (l & 3) % 2) of row 8i + l / 4, so each load instruction covers 8 whole 64-byte row segments
+        const int u = lane & 3;
 #pragma unroll
-    for (int i = 0; i < XRows<FMT, MODE>::kRows; ++i) {
-        int trow;
-        const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, lane, i, trow) + tile_chunk_off(c, tiled_row_bytes(FMT));
-        if constexpr (FMT == FMT_FP8) {
+        for (int i = 0; i < XRows<FMT, MODE>::kRows * 4; ++i) {
+            int trow;
+            const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, 8 * i + (lane >> 2), trow) + tile_chunk_off(c, tiled_row_bytes(FMT));
+            x.codes[i >> 2][i & 3] = __ldg(reinterpret_cast<const uint4*>(chunk + fp8_code_off(ng, trow, w, 2 * h + (u >> 1), u & 1)));
+        }
+    } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)  // quad 2h + u/2, half u%2
-                x.codes[i][u] = __ldg(reinterpret_cast<const uint4*>(chunk + fp8_code_off(ng, trow, w, 2 * h + (u >> 1), u & 1)));
-        } else {
+        for (int i = 0; i < XRows<FMT, MODE>::kRows; ++i) {
+            int trow;
+            const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, lane + 32 * i, trow) + tile_chunk_off(c, tiled_row_bytes(FMT));
             x.codes[i][0] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h)));
             x.codes[i][1] = __ldg(reinterpret_cast<const uint4*>(chunk + fp4_code_off(ng, trow, w, 2 * h + 1)));
             if constexpr (FMT == FMT_NVFP4)
@@ -265,10 +309,11 @@ __device__ __forceinline__ void xprefetch_fp8(const CallArgs& a, const uint8_t* 
     const int G = (MODE == MODE_GU ? a.H : a.I) / kGroupK;
     const int j = kb >> 1;
     const int c = j / kChunkGroups, w = j % kChunkGroups, ng = fp4_chunk_groups(G, c);
+    if ((lane & 3) != 0) return;
 #pragma unroll
-    for (int i = 0; i < XRows<FMT_FP8, MODE>::kRows; ++i) {
+    for (int i = 0; i < XRows<FMT_FP8, MODE>::kRows * 4; ++i) {
         int trow;
-        const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, lane, i, trow) + tile_chunk_off(c, tiled_row_bytes(FMT_FP8));
+        const uint8_t* chunk = xrow<MODE>(a, blob, mt, part, 8 * i + (lane >> 2), trow) + tile_chunk_off(c, tiled_row_bytes(FMT_FP8));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(chunk + (trow * ng + w) * 128) : "memory");
     }
 }
@@ -278,23 +323,52 @@ template <int FMT, int MODE>
 __device__ __forceinline__ void xstore(const XRows<FMT, MODE>& x, unsigned char* st, int part, int lane) {
 #pragma unroll
     for (int i = 0; i < XRows<FMT, MODE>::kRows; ++i) {
-        const int r = (MODE == MODE_GU ? 0 : 64 * part) + lane + 32 * i;  // row of the 128-row A tile
-        unsigned char* rowp = st + (MODE == MODE_GU ? part * kTileBytes : 0) + r * 128;
+        const int r = XPart<MODE>::row0(part) + lane + 32 * i;  // row of the 128-row A tile
+        unsigned char* rowp = st + XPart<MODE>::tile(part) * kTileBytes + r * 128;
         if constexpr (FMT == FMT_FP8) {
+            // pieces as xload took them: 16 codes = K positions 16u .. 16u+15 of row 8i' + lane / 4 -> chunks 2u, 2u+1
+            const int u = lane & 3;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {  // 16 codes = K positions 16u .. 16u+15 -> chunks 2u, 2u+1
+            for (int i2 = 0; i2 < 4; ++i2) {
+                const int ip = 4 * i + i2;
+                const int rr = XPart<MODE>::row0(part) + 8 * ip + (lane >> 2);
+                unsigned char* rp = st + XPart<MODE>::tile(part) * kTileBytes + rr * 128;
                 uint32_t f[8];
-                e4m3x8_to_f16x2(make_uint2(x.codes[i][u].x, x.codes[i][u].y), *reinterpret_cast<uint32_t(*)[4]>(f));
-                e4m3x8_to_f16x2(make_uint2(x.codes[i][u].z, x.codes[i][u].w), *reinterpret_cast<uint32_t(*)[4]>(f + 4));
-                uint32_t o[8];
+                e4m3x8_to_f16x2(make_uint2(x.codes[i][i2].x, x.codes[i][i2].y), *reinterpret_cast<uint32_t(*)[4]>(f));
+                e4m3x8_to_f16x2(make_uint2(x.codes[i][i2].z, x.codes[i][i2].w), *reinterpret_cast<uint32_t(*)[4]>(f + 4));
+                if constexpr (!f16_operands<FMT, MODE>()) {
 #pragma unroll
-                for (int y = 0; y < 8; ++y) {
-                    const __half2 hv = *reinterpret_cast<const __half2*>(&f[y]);
-                    __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(hv), __high2float(hv));
-                    o[y] = *reinterpret_cast<uint32_t*>(&bv);
+                    for (int y = 0; y < 8; ++y) {
+                        const __half2 hv = *reinterpret_cast<const __half2*>(&f[y]);
+                        __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(hv), __high2float(hv));
+                        f[y] = *reinterpret_cast<uint32_t*>(&bv);
+                    }
                 }
-                *reinterpret_cast<uint4*>(rowp + (((2 * u) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(rowp + (((2 * u + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                *reinterpret_cast<uint4*>(rp + (((2 * u) ^ (rr & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4*>(rp + (((2 * u + 1) ^ (rr & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+            }
+            continue;
+        } else if constexpr (FMT == FMT_NVFP4 && f16_operands<FMT, MODE>()) {
+            // code x block scale in f16: at most 6 significant bits, within [2^-10, 2688]
+            uint32_t sh[4];
+            e4m3x8_to_f16x2(x.sc[i], sh);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t wv[4] = {x.codes[i][u].x, x.codes[i][u].y, x.codes[i][u].z, x.codes[i][u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // 4 code bytes -> 8 elements -> one 16-byte chunk
+                    uint32_t f[4];
+                    fp4x8_to_f16x2(wv[q], f);
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        const int st = (4 * q + y) >> 1;  // K step of this pair: its block scale
+                        const uint32_t sc2 = __byte_perm(sh[st >> 1], 0u, (st & 1) ? 0x3232u : 0x1010u);
+                        __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&f[y]), *reinterpret_cast<const __half2*>(&sc2));
+                        f[y] = *reinterpret_cast<uint32_t*>(&v);
+                    }
+                    const int c16 = 4 * u + q;
+                    *reinterpret_cast<uint4*>(rowp + ((c16 ^ (r & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                }
             }
             continue;
         }
@@ -351,7 +425,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
-            mbar_init(&bar_afull[s], 2);
+            mbar_init(&bar_afull[s], kXformWarps / C::kStages);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_tfull[s], 1);
@@ -472,7 +546,8 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
                 const int n_nt = (a.act_cnt[u] + BN - 1) / BN;
                 const int nt = local % n_nt;
                 const int rows = min(BN, a.act_cnt[u] - nt * BN);
-                const uint32_t idesc = idesc_bf16(BM, (rows + 15) & ~15);
+                const uint32_t idesc = f16_operands<FMT, MODE>() ? idesc_f16(BM, (rows + 15) & ~15)
+                                                                 : idesc_bf16(BM, (rows + 15) & ~15);
                 const int acc = it & 1;
                 const uint32_t aph = (it >> 1) & 1;
                 if (!mbar_wait(&bar_tempty[acc], aph ^ 1u, abort_flag, a.wait_ns)) {
@@ -513,7 +588,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             }
         }
     } else if (warp >= 6) {
-        // ---------------- A-tile transform (FP4 / FP8 weights, warps 6-13)
+        // ---------------- A-tile transform (FP4 / FP8 weights, warps 6-21)
         if constexpr (kFp4) {
             const int xw = warp - 6;
             const int sidx = xw % C::kStages, part = xw / C::kStages;
@@ -623,28 +698,32 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             if constexpr (MODE == MODE_GU) {
                 const int unit = mt * BM + row_in_tile;
                 __nv_bfloat16* hrow = reinterpret_cast<__nv_bfloat16*>(a.hbuf) + kpos(unit);
-                for (int c0 = 0; c0 < rows; c0 += 32) {
-                    float g[32], up[32];
-                    tmem_ld32(tbase + c0, g);
-                    tmem_ld32(tbase + BN + c0, up);
+                // 16 columns at a time: the FP4 / FP8 kernels run 22 warps on 80 registers
+                for (int c0 = 0; c0 < rows; c0 += 16) {
+                    float g[16], up[16];
+                    tmem_ld16(tbase + c0, g);
+                    tmem_ld16(tbase + BN + c0, up);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         if (c0 + j < rows) {
                             const int r = r0 + c0 + j;
-                            const float gv = g[j] * gsc0;
+                            // f16 operands: undo the row's power of two first (exact)
+                            const float un = f16_operands<FMT, MODE>() ? a.xunr[r] : 1.0f;
+                            const float gv = (g[j] * un) * gsc0;
                             const float act = a.mode == 1 ? gv : gv / (1.0f + expf(-gv));
-                            hrow[static_cast<size_t>(r) * a.I] = __float2bfloat16_rn(act * (up[j] * gsc1) * a.row_gate[r]);
+                            hrow[static_cast<size_t>(r) * a.I] =
+                                __float2bfloat16_rn(act * ((up[j] * un) * gsc1) * a.row_gate[r]);
                         }
                     }
                 }
             } else {
                 const int hr = mt * BM + row_in_tile;
                 __nv_bfloat16* ycol = reinterpret_cast<__nv_bfloat16*>(a.ybuf) + hr;
-                for (int c0 = 0; c0 < rows; c0 += 32) {
-                    float y[32];
-                    tmem_ld32(tbase + c0, y);
+                for (int c0 = 0; c0 < rows; c0 += 16) {
+                    float y[16];
+                    tmem_ld16(tbase + c0, y);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
+                    for (int j = 0; j < 16; ++j)
                         if (c0 + j < rows) ycol[static_cast<size_t>(r0 + c0 + j) * a.H] = __float2bfloat16_rn(y[j] * gsc0);
                 }
             }
@@ -824,7 +903,40 @@ __global__ void __launch_bounds__(256) k_router_norms(const __nv_bfloat16* __res
 }
 
 // X_perm[r, :] = hidden[row_tok[r], :] as bf16 in the library's K order
+// per token row t: the power of two xsc[t] with max_h |x[t,h]| * xsc[t] in
+// [2^14, 2^15) (1 for an all-zero row); one warp per token
 template <int ACT>
+__global__ void __launch_bounds__(256) k_xscale(CallArgs a) {
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    unsigned int m = 0u;
+    if constexpr (ACT == ACT_BF16) {
+        const uint4* x = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.hidden) + static_cast<size_t>(t) * a.H);
+        for (int i = lane; i < a.H / 8; i += 32) {
+            const uint4 v = x[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m = max(m, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
+        }
+    } else {
+        const float4* x = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.hidden) + static_cast<size_t>(t) * a.H);
+        for (int i = lane; i < a.H / 4; i += 32) {
+            const float4 v = x[i];
+            m = max(m, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                           max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
+        }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) {
+        float sc, un;
+        pow2_scale(m, sc, un);
+        a.xsc[t] = sc;
+    }
+}
+
+// X_perm[r] = hidden[row_tok[r]] in the weights' K order: bf16, or (F16) f16
+// of the row times its token's power of two, whose inverse goes to xunr[r]
+template <int ACT, bool F16>
 __global__ void __launch_bounds__(256) k_gather_x(CallArgs a, int rows) {
     const int H = a.H;
     const size_t n8 = static_cast<size_t>(rows) * H / 8;
@@ -833,23 +945,42 @@ __global__ void __launch_bounds__(256) k_gather_x(CallArgs a, int rows) {
         const int r = static_cast<int>(idx / (H / 8));
         const int p = 8 * static_cast<int>(idx % (H / 8));  // destination position
         const int j = p >> 7, w = p & 127, q = w >> 5, s = (w & 31) >> 2;
-        const size_t src = static_cast<size_t>(a.row_tok[r]) * H + 128 * j + 16 * s + 4 * q;
+        const int tok = a.row_tok[r];
+        const size_t src = static_cast<size_t>(tok) * H + 128 * j + 16 * s + 4 * q;
+        float v[8];
         uint32_t o[4];
         if constexpr (ACT == ACT_BF16) {
             const uint16_t* x = reinterpret_cast<const uint16_t*>(a.hidden);
             const uint2 lo = *reinterpret_cast<const uint2*>(x + src);
             const uint2 hi = *reinterpret_cast<const uint2*>(x + src + 16);
             o[0] = lo.x; o[1] = lo.y; o[2] = hi.x; o[3] = hi.y;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(o[i] << 16);
+                v[2 * i + 1] = __uint_as_float(o[i] & 0xFFFF0000u);
+            }
         } else {
             const float* x = reinterpret_cast<const float*>(a.hidden);
             const float4 lo = *reinterpret_cast<const float4*>(x + src);
             const float4 hi = *reinterpret_cast<const float4*>(x + src + 16);
-            const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+            v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+            if constexpr (!F16) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                    o[i] = *reinterpret_cast<uint32_t*>(&b);
+                }
+            }
+        }
+        if constexpr (F16) {
+            const float sc = a.xsc[tok];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                o[i] = *reinterpret_cast<uint32_t*>(&b);
+                __half2 hv = __floats2half2_rn(v[2 * i] * sc, v[2 * i + 1] * sc);
+                o[i] = *reinterpret_cast<uint32_t*>(&hv);
             }
+            if (p == 0) a.xunr[r] = 1.0f / sc;  // a power of two: exact
         }
         *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.xperm) + static_cast<size_t>(r) * H + p) =
             make_uint4(o[0], o[1], o[2], o[3]);
@@ -911,8 +1042,12 @@ cudaError_t umma_set_attributes() {
         if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_router_norms)))) return e;
     }
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16>)))) return e;
-    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16, false>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32, false>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_BF16, true>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_gather_x<ACT_FP32, true>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_xscale<ACT_BF16>)))) return e;
+    if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&k_xscale<ACT_FP32>)))) return e;
 #define MOE_UMMA_ATTR(MODE, FMT)                                                                         \
     if ((e = cudaFuncSetAttribute(k_umma_grouped<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                   Cfg<MODE, FMT != FMT_BF16>::kSmem)))                                   \
@@ -969,8 +1104,20 @@ cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num
     const int rows = a.T * (a.k + a.n_shared);
     const size_t n8 = static_cast<size_t>(rows) * a.H / 8;
     const int gb = static_cast<int>(std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(num_sms) * 16));
-    if (a.act == ACT_BF16) k_gather_x<ACT_BF16><<<gb, 256, 0, s>>>(a, rows);
-    else k_gather_x<ACT_FP32><<<gb, 256, 0, s>>>(a, rows);
+    const bool f16 = a.fmt == FMT_NVFP4 || a.fmt == FMT_FP8;  // gate/up on f16 operands
+    int n = 3;
+    if (f16) {
+        if (a.act == ACT_BF16) k_xscale<ACT_BF16><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+        else k_xscale<ACT_FP32><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+        ++n;
+    }
+    if (a.act == ACT_BF16) {
+        if (f16) k_gather_x<ACT_BF16, true><<<gb, 256, 0, s>>>(a, rows);
+        else k_gather_x<ACT_BF16, false><<<gb, 256, 0, s>>>(a, rows);
+    } else {
+        if (f16) k_gather_x<ACT_FP32, true><<<gb, 256, 0, s>>>(a, rows);
+        else k_gather_x<ACT_FP32, false><<<gb, 256, 0, s>>>(a, rows);
+    }
     switch (a.fmt) {
         case FMT_BF16: launch_gemms<FMT_BF16>(a, maps, num_sms, s, ev_gu); break;
         case FMT_NVFP4: launch_gemms<FMT_NVFP4>(a, maps, num_sms, s, ev_gu); break;
@@ -978,7 +1125,7 @@ cudaError_t launch_prefill_umma(const CallArgs& a, const UmmaMaps& maps, int num
         case FMT_FP8: launch_gemms<FMT_FP8>(a, maps, num_sms, s, ev_gu); break;
         default: return cudaErrorInvalidValue;
     }
-    if (launches) *launches = 3;
+    if (launches) *launches = n;
     return cudaGetLastError();
 }
 

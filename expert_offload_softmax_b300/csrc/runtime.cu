@@ -777,6 +777,8 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {static_cast<size_t>(E + ns) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.tok_row)},
         {static_cast<size_t>(E + ns) * 4, reinterpret_cast<void**>(&a.act_slot)},
         {umma ? rows * H * 2 : 16, &a.xperm},
+        {umma ? Tm * 4 : 16, reinterpret_cast<void**>(&a.xsc)},
+        {umma ? rows * 4 : 16, reinterpret_cast<void**>(&a.xunr)},
         {4, reinterpret_cast<void**>(&a.dev_err)},
         {4, reinterpret_cast<void**>(&a.route_done)},
         {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.cacc)},
