@@ -52,6 +52,12 @@ def _L():
         lib.orc_bf16_to_f32.argtypes = [vp, sz, vp]
         lib.orc_f32_to_bf16.argtypes = [vp, sz, vp]
         lib.orc_dequant.argtypes = [i32, vp, vp, f32, i32, i32, vp]
+        lib.orc_e4m3_rne.restype = f32
+        lib.orc_e4m3_rne.argtypes = [f32]
+        lib.orc_e2m1_rne.restype = f32
+        lib.orc_e2m1_rne.argtypes = [f32]
+        lib.orc_quant_act.argtypes = [i32, vp, i32, vp]
+        lib.orc_expert_ffn_q.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
         lib.orc_router_logits.argtypes = [vp, vp, i32, i32, i32, vp]
         lib.orc_router_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         lib.orc_permute.restype = i32
@@ -245,6 +251,36 @@ def expert_ffn(x: np.ndarray, Wg, Wu, Wd, mode: int = 0):
     _L().orc_expert_ffn(_p(x), _p(_c(Wg, np.float32)), _p(_c(Wu, np.float32)),
                         _p(_c(Wd, np.float32)), H, I, mode, _p(y), _p(h))
     return y, h
+
+
+QUANT_MXFP8, QUANT_NVFP4 = 1, 2
+
+
+def e4m3_rne(v: float) -> float:
+    return float(_L().orc_e4m3_rne(ctypes.c_float(v)))
+
+
+def e2m1_rne(v: float) -> float:
+    return float(_L().orc_e2m1_rne(ctypes.c_float(v)))
+
+
+def quant_act(kind: int, x: np.ndarray) -> np.ndarray:
+    """Activation quantiser of a block-scaled MMA (see orc_quant_act)."""
+    x = _c(x, np.float32)
+    out = np.empty_like(x)
+    _L().orc_quant_act(kind, _p(x), x.size, _p(out))
+    return out
+
+
+def expert_ffn_q(x: np.ndarray, Wg, Wu, Wd, kind: int, mode: int = 0) -> np.ndarray:
+    """expert_ffn with x and h quantised by quant_act(kind)."""
+    x = _c(x, np.float32)
+    H = x.size
+    I = Wg.shape[0]
+    y = np.empty(H, np.float32)
+    _L().orc_expert_ffn_q(_p(x), _p(_c(Wg, np.float32)), _p(_c(Wu, np.float32)),
+                          _p(_c(Wd, np.float32)), H, I, mode, kind, _p(y))
+    return y
 
 
 def combine(gates_row: np.ndarray, ys) -> np.ndarray:

@@ -366,6 +366,108 @@ void orc_combine(int H, int k, int n_shared, const float* gates, const float* co
 }
 
 /* ------------------------------------------------------------------------- */
+/* Activation quantisers (for the tolerance study of block-scaled MMA)       */
+/* ------------------------------------------------------------------------- */
+/* A block-scaled tensor-core MMA (OCP MX formats, NVFP4) multiplies two
+ * narrow operands, so the activations would have to be quantised on the fly.
+ * These functions define that quantisation; orc_expert_ffn_q evaluates an
+ * expert with it, so that its distance from orc_expert_ffn can be measured.
+ * Nothing in the layer as specified uses them. */
+
+/* nearest E4M3 (FN) value, ties to the even code, saturating at +-448 */
+float orc_e4m3_rne(float v) {
+    float a = fabsf(v);
+    if (a >= 448.0f) a = 448.0f;
+    else {
+        int e;
+        frexpf(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+        int ue = e - 1;                  /* a in [2^ue, 2^(ue+1)) */
+        if (ue < -6) ue = -6;            /* subnormals share the spacing of 2^-6 */
+        float q = ldexpf(1.0f, ue - 3);  /* 3 mantissa bits */
+        a = rintf(a / q) * q;            /* rintf: ties to even under the default mode */
+        if (a > 448.0f) a = 448.0f;
+    }
+    return v < 0 ? -a : a;
+}
+
+/* nearest E2M1 value, ties to the even code, saturating at +-6:
+ * grid 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7; even codes 0, 1, 2, 4) */
+float orc_e2m1_rne(float v) {
+    static const float grid[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    float a = fabsf(v), best = 0.0f;
+    int bc = 0;
+    for (int c = 0; c < 8; ++c) {
+        float d = fabsf(a - grid[c]), db = fabsf(a - best);
+        if (d < db || (d == db && (c & 1) == 0 && (bc & 1) == 1)) {
+            best = grid[c];
+            bc = c;
+        }
+    }
+    return v < 0 ? -best : best;
+}
+
+/* kind 1, MXFP8 (OCP MX v1.0, E4M3 elements): blocks of 32 consecutive
+ * elements share X = 2^(floor(log2 amax) - 8), 8 being E4M3's largest
+ * exponent; each element becomes X * e4m3_rne(x / X) (values above 448 X
+ * saturate, as the specification allows). An all-zero block stays zero.
+ * kind 2, NVFP4: g = amax(x) / (448 * 6) over the vector; blocks of 16 share
+ * s = e4m3_rne(amax_blk / (6 g)); each element becomes
+ * e2m1_rne(x / (s g)) * s * g. n is a multiple of the block size. */
+void orc_quant_act(int kind, const float* x, int n, float* out) {
+    if (kind == 1) {
+        for (int b = 0; b < n; b += 32) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[b + i]));
+            if (amax == 0.0f) {
+                for (int i = 0; i < 32; ++i) out[b + i] = 0.0f;
+                continue;
+            }
+            int e;
+            frexpf(amax, &e);
+            float X = ldexpf(1.0f, (e - 1) - 8);
+            for (int i = 0; i < 32; ++i) out[b + i] = orc_e4m3_rne(x[b + i] / X) * X;
+        }
+    } else {
+        float amax = 0.0f;
+        for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        if (amax == 0.0f) {
+            for (int i = 0; i < n; ++i) out[i] = 0.0f;
+            return;
+        }
+        float g = amax / (448.0f * 6.0f);
+        for (int b = 0; b < n; b += 16) {
+            float ab = 0.0f;
+            for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(x[b + i]));
+            float sc = orc_e4m3_rne(ab / (6.0f * g));
+            float d = sc * g;
+            for (int i = 0; i < 16; ++i) out[b + i] = d == 0.0f ? 0.0f : orc_e2m1_rne(x[b + i] / d) * d;
+        }
+    }
+}
+
+/* orc_expert_ffn with the activations quantised by orc_quant_act(kind): x
+ * before gate/up, h before down (the two operands a block-scaled MMA would
+ * take in a narrow format) */
+void orc_expert_ffn_q(const float* x, const float* Wg, const float* Wu, const float* Wd,
+                      int H, int I, int mode, int kind, float* y) {
+    float* xq = (float*)malloc(sizeof(float) * (size_t)H);
+    float* h = (float*)malloc(sizeof(float) * (size_t)I);
+    float* hq = (float*)malloc(sizeof(float) * (size_t)I);
+    orc_quant_act(kind, x, H, xq);
+    for (int i = 0; i < I; ++i) {
+        float g = dot(Wg + (size_t)i * H, xq, H);
+        float u = dot(Wu + (size_t)i * H, xq, H);
+        float a = mode == 1 ? g : g / (1.0f + expf(-g));
+        h[i] = a * u;
+    }
+    orc_quant_act(kind, h, I, hq);
+    for (int r = 0; r < H; ++r) y[r] = dot(Wd + (size_t)r * I, hq, I);
+    free(xq);
+    free(h);
+    free(hq);
+}
+
+/* ------------------------------------------------------------------------- */
 /* Resizing the pool at a safe point                                         */
 /* ------------------------------------------------------------------------- */
 
