@@ -902,7 +902,6 @@ __global__ void __launch_bounds__(256) k_router_norms(const __nv_bfloat16* __res
     if (lane == 0) out[e] = sqrtf(ss) * (1.0f + 1.0f / 1024.0f);
 }
 
-// X_perm[r, :] = hidden[row_tok[r], :] as bf16 in the library's K order
 // per token row t: the power of two xsc[t] with max_h |x[t,h]| * xsc[t] in
 // [2^14, 2^15) (1 for an all-zero row); one warp per token
 template <int ACT>
