@@ -410,6 +410,7 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
     extern __shared__ unsigned char dyn_raw[];
     __shared__ TileSched ts;
     __shared__ const uint8_t* s_ptr[kFp4 ? kMaxExperts + 1 : 1];  // blob of each active expert (FP4 / FP8)
+    __shared__ int s_nnt[kFp4 ? kMaxExperts + 1 : 1];             // its token tiles (FP4 / FP8)
     __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_afull[C::kStages];
     __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_drain;
     __shared__ uint32_t s_tmem;
@@ -460,7 +461,10 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
         if (lane == 0) ts.start[na] = carry;
     }
     if constexpr (kFp4)
-        for (int u = threadIdx.x; u < na; u += blockDim.x) s_ptr[u] = a.act_ptr[u];
+        for (int u = threadIdx.x; u < na; u += blockDim.x) {
+            s_ptr[u] = a.act_ptr[u];
+            s_nnt[u] = (a.act_cnt[u] + BN - 1) / BN;
+        }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -599,14 +603,13 @@ __global__ void __launch_bounds__(FMT == FMT_BF16 ? kThreads : kThreadsFp4, 1)
             // this warp's positions: sidx, sidx + 4, ... over this CTA's tiles (n_kb each)
             const int my_tiles = blockIdx.x < total ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
             const long long npos = static_cast<long long>(my_tiles) * n_kb;
+            // everything from shared memory: a position costs no memory round trip
             auto where = [&](long long P, const uint8_t*& blob, int& mt, int& kb) {
-                const int i = static_cast<int>(P / n_kb);
-                kb = static_cast<int>(P % n_kb);
+                const int i = static_cast<int>(P) / n_kb;
+                kb = static_cast<int>(P) - i * n_kb;
                 const int t = blockIdx.x + i * gridDim.x;
                 const int u = find_expert(ts, na, t);
-                const int local = t - ts.start[u];
-                const int n_nt = (a.act_cnt[u] + BN - 1) / BN;
-                mt = local / n_nt;
+                mt = (t - ts.start[u]) / s_nnt[u];
                 blob = s_ptr[u];
             };
             auto process = [&](long long P, const XRows<FMT, MODE>& x) -> bool {
