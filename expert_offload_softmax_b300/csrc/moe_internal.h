@@ -190,12 +190,12 @@ struct CallArgs {
     int32_t* route_done;   // [1] routing CTAs finished in this call (0 between calls)
     // prefill permutation, computed in parts: each routing CTA b (8 tokens)
     // ranks its assignments among those of the same expert and adds its
-    // per-expert counts; the column scans give every CTA its base row per expert
+    // per-expert counts; the permutation kernel sums each column over the
+    // earlier CTAs to get every CTA's base row per expert
     int32_t* cacc;         // [E] per-expert assignment counts (0 between calls)
     int16_t* cntT;         // [E][nb] per-CTA counts of each expert (nb = ceil(max_tokens / 8))
-    int32_t* baseT;        // [E][nb] rows of expert e before CTA b's (exclusive scan over b)
     int16_t* lrank;        // [T*k] rank of assignment a among its CTA's assignments to the same expert
-    int nb_max;            // column stride of cntT / baseT
+    int nb_max;            // column stride of cntT
     unsigned long long* bar_cnt;     // [3] arrival counters of the decode kernel's grid barriers
     unsigned long long dcall;        // decode kernel launches before this one since the counters were reset
     unsigned char* dplan;  // decode plan: header + (E + n_shared) records

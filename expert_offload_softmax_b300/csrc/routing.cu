@@ -296,8 +296,13 @@ __host__ __device__ inline size_t route_area_bytes(int S, int E) {
 // phase B: everything after the logits (and, for prefill, the top-k)
 // --------------------------------------------------------------------------
 
-__device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char* area, bool decode) {
+// bmark (trace only, prefill): times of the steps below, written by thread 0
+__device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char* area, bool decode,
+                              unsigned long long* bmark) {
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    auto bm = [&](int i) {
+        if (bmark && tid == 0) bmark[i] = route_gtimer();
+    };
     const int T = a.T, E = a.E, k = a.k, n = T * k, S = a.S;
     CallInfo* info = a.info;
     LruShared& sm = rs.lru;
@@ -373,6 +378,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         }
         for (int i = tid; i < (E + a.n_shared) * kDecodeMaxT; i += nthr) a.tok_row[i] = -1;
     }
+    bm(0);
     if (decode) {
         for (int e = tid; e < E; e += nthr) rs.cnt[e] = 0;
     } else {
@@ -430,65 +436,9 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         }
     }
     __syncthreads();
-    if (!decode) {
-        // prefill: rows of expert e before CTA b = exclusive scan of its count
-        // column over b; a follow-up kernel places the assignments
-        const int nwarps = nthr >> 5;
-        const int nb = (T + kPrefillTokTile - 1) / kPrefillTokTile;
-        // 16 consecutive columns per lane, read as two 16-byte vectors (nb_max is a
-        // multiple of 16; columns past nb hold stale counts and are masked)
-        constexpr int kPerLane = 16, kBatch = 4;
-        for (int e0 = warp * kBatch; e0 < E; e0 += nwarps * kBatch) {
-            int carry[kBatch] = {0, 0, 0, 0};
-            for (int b0 = 0; b0 < nb; b0 += 32 * kPerLane) {
-                int v[kBatch][kPerLane];
-                const int bl = b0 + lane * kPerLane;
-                uint4 raw[kBatch][2];
-#pragma unroll
-                for (int x = 0; x < kBatch; ++x)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        raw[x][h] = (e0 + x < E && bl < nb)
-                                        ? __ldcg(reinterpret_cast<const uint4*>(a.cntT + static_cast<size_t>(e0 + x) * a.nb_max + bl) + h)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int x = 0; x < kBatch; ++x)
-#pragma unroll
-                    for (int i = 0; i < kPerLane; ++i) {
-                        const uint4 r = raw[x][i / 8];
-                        const uint32_t w = (i % 8) < 2 ? r.x : (i % 8) < 4 ? r.y : (i % 8) < 6 ? r.z : r.w;
-                        const int c = static_cast<int>((i & 1) ? (w >> 16) : (w & 0xFFFFu));
-                        v[x][i] = bl + i < nb ? c : 0;
-                    }
-#pragma unroll
-                for (int x = 0; x < kBatch; ++x) {
-                    int tot = 0;
-#pragma unroll
-                    for (int i = 0; i < kPerLane; ++i) tot += v[x][i];
-                    int incl = tot;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    int run = carry[x] + incl - tot;
-                    if (e0 + x < E && bl < nb) {
-                        int o[kPerLane];
-#pragma unroll
-                        for (int i = 0; i < kPerLane; ++i) {
-                            o[i] = run;
-                            run += v[x][i];
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(a.baseT + static_cast<size_t>(e0 + x) * a.nb_max + bl);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h)
-                            dst[h] = make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
-                    }
-                    carry[x] += __shfl_sync(0xffffffffu, incl, 31);
-                }
-            }
-        }
-    }
+    bm(1);
+    // prefill: the rows of expert e before routing CTA b (the sum of e's count
+    // column over earlier CTAs) are summed by k_perm_rows, one CTA per column
     // decode: stable permutation, warp w owns the contiguous assignment range [w*chunk, (w+1)*chunk)
     if (decode) {
         int32_t* wc = reinterpret_cast<int32_t*>(area);  // [kRouteWarps][E]
@@ -547,10 +497,12 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         }
     }
     __syncthreads();
+    bm(2);
     // LRU: demand batch of this layer's experts
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(area);
     const int nu = rs.nu;
     const int m = lru_batch(lv, sm, keys, a.layer, rs.members, nu, nullptr, 0, 0);
+    bm(3);
     if (m < 0) {
         if (tid == 0) {
             info->n_uniq = nu;
@@ -591,6 +543,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         info->miss_slot[r] = sm.member_slot[p];
     }
     __syncthreads();
+    bm(4);
     int n_pf = 0, m_pf = 0;
     const bool do_pf = pf_possible && a.S >= nu + E;
     if (do_pf) {
@@ -644,6 +597,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
     }
     if (decode && tid == 0) *reinterpret_cast<int32_t*>(a.dplan) = nu + a.n_shared;
     __syncthreads();
+    bm(5);
     if (tid == 0) {
         *a.n_active = nu + a.n_shared;
         info->n_uniq = nu;
@@ -661,6 +615,7 @@ __device__ void route_phase_b(const CallArgs& a, RouteShared& rs, unsigned char*
         __threadfence_system();
         info->done = a.seq;
     }
+    bm(6);
 }
 
 // --------------------------------------------------------------------------
@@ -856,25 +811,74 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     if (!s_last) return;
     __threadfence();
     RouteShared& rs = *reinterpret_cast<RouteShared*>(route_smem);
-    route_phase_b(a, rs, route_smem + kRouteSharedBytes, DECODE);
+    // trace only: phase B's steps in the two ring slots before CTA 0's phase-A marks
+    route_phase_b(a, rs, route_smem + kRouteSharedBytes, DECODE, rtr ? rtr - 16 : nullptr);
     if (threadIdx.x == 0) *a.route_done = 0;
     if (rtr && threadIdx.x == 0) rtr[2] = route_gtimer();
 }
 
 // prefill: places every assignment of routing CTA b (8 tokens) at
-// offsets[e] + rows of e in earlier CTAs + its rank among CTA b's assignments to e
+// offsets[e] + rows of e in earlier CTAs + its rank among CTA b's assignments
+// to e. The rows of e in earlier CTAs are the sum of e's count column over
+// b' < b: a warp per assignment, 8 assignments per warp in flight at once.
 __global__ void __launch_bounds__(256) k_perm_rows(CallArgs a) {
+    constexpr int kPerWarp = 8;
+    __shared__ int s_base[kPrefillTokTile * kMaxTopK];
     const int b = blockIdx.x, k = a.k;
     const int t0 = b * kPrefillTokTile, nt = min(kPrefillTokTile, a.T - t0);
-    const int i = threadIdx.x;
-    if (i >= nt * k) return;
-    const int asg = t0 * k + i;
-    const int e = a.topk[asg];
-    const int row = a.offsets[e] + a.baseT[static_cast<size_t>(e) * a.nb_max + b] + a.lrank[asg];
-    a.perm[row] = asg;
-    a.inv_perm[asg] = row;
-    a.row_tok[row] = asg / k;
-    a.row_gate[row] = a.gates[asg];
+    const int n = nt * k;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int i0 = warp * kPerWarp; i0 < n; i0 += nwarps * kPerWarp) {
+        uint4 v[kPerWarp][2];
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            const int i = i0 + j;
+            const int16_t* col = i < n ? a.cntT + static_cast<size_t>(a.topk[t0 * k + i]) * a.nb_max : nullptr;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // columns 256 h + 8 lane .. + 7 (nb <= 512 per pass)
+                const int c0 = 256 * h + 8 * lane;
+                v[j][h] = col && c0 < b ? __ldcg(reinterpret_cast<const uint4*>(col + c0)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            const int i = i0 + j;
+            int sum = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c0 = 256 * h + 8 * lane;
+                const uint32_t w[4] = {v[j][h].x, v[j][h].y, v[j][h].z, v[j][h].w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int x = static_cast<int>((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xFFFFu));
+                    sum += c0 + q < b ? x : 0;
+                }
+            }
+            // columns past 512 (T > 4096): the rest of the row, one vector per lane per step
+            const int16_t* col = i < n ? a.cntT + static_cast<size_t>(a.topk[t0 * k + i]) * a.nb_max : nullptr;
+            for (int c0 = 512 + 8 * lane; col && c0 < b; c0 += 256) {
+                const uint4 u = __ldcg(reinterpret_cast<const uint4*>(col + c0));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int x = static_cast<int>((q & 1) ? (w[q >> 1] >> 16) : (w[q >> 1] & 0xFFFFu));
+                    sum += c0 + q < b ? x : 0;
+                }
+            }
+            sum = __reduce_add_sync(0xffffffffu, sum);
+            if (lane == 0 && i < n) s_base[i] = sum;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int asg = t0 * k + i;
+        const int e = a.topk[asg];
+        const int row = a.offsets[e] + s_base[i] + a.lrank[asg];
+        a.perm[row] = asg;
+        a.inv_perm[asg] = row;
+        a.row_tok[row] = asg / k;
+        a.row_gate[row] = a.gates[asg];
+    }
 }
 
 // dynamic shared memory of one k_route launch

@@ -783,7 +783,6 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {4, reinterpret_cast<void**>(&a.route_done)},
         {static_cast<size_t>(E) * 4, reinterpret_cast<void**>(&a.cacc)},
         {static_cast<size_t>(E) * nb_max * 2, reinterpret_cast<void**>(&a.cntT)},
-        {static_cast<size_t>(E) * nb_max * 4, reinterpret_cast<void**>(&a.baseT)},
         {Tm * k * 2, reinterpret_cast<void**>(&a.lrank)},
         {3 * 8, reinterpret_cast<void**>(&a.bar_cnt)},
         {static_cast<size_t>(moe::kDecodeMaxT) * E * 8, reinterpret_cast<void**>(&a.dlog)},
@@ -1287,6 +1286,14 @@ int moe_sync(moe_handle* h) {
             std::fprintf(stderr, "[moe] route CTA 0: staged %.2f, candidates %.2f, exact %.2f, top-k %.2f, end %.2f us; %llu candidates\n",
                          (q[1] - q[0]) * 1e-3, (q[2] - q[0]) * 1e-3, (q[3] - q[0]) * 1e-3, (q[4] - q[0]) * 1e-3,
                          (q[5] - q[0]) * 1e-3, q[7]);
+        unsigned long long b[8];
+        CK(h, cudaMemcpy(b, h->trace + base - 16, sizeof(b), cudaMemcpyDeviceToHost));
+        if (r[0] != ~0ull && r[2] != 0 && b[0] >= r[1] && b[6] >= b[0])
+            std::fprintf(stderr,
+                         "[moe] route phase B (us after its start): state loaded %.2f, offsets %.2f, permutation %.2f, "
+                         "LRU batch %.2f, events %.2f, prefetch batch and shared rows %.2f, end %.2f\n",
+                         (b[0] - r[1]) * 1e-3, (b[1] - r[1]) * 1e-3, (b[2] - r[1]) * 1e-3, (b[3] - r[1]) * 1e-3,
+                         (b[4] - r[1]) * 1e-3, (b[5] - r[1]) * 1e-3, (b[6] - r[1]) * 1e-3);
         reset_trace(h);
     }
     if (h->trace && h->last_fused) {
