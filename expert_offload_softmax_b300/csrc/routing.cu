@@ -633,8 +633,9 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
                                                         (kTraceCalls - 1) * 4
                                                   : nullptr;
     if (rtr && threadIdx.x == 0) atomicMin(rtr, static_cast<unsigned long long>(route_gtimer()));
-    // trace only: CTA 0's phase-A steps in the two slots before it
-    unsigned long long* rsub = (rtr && blockIdx.x == 0 && threadIdx.x == 0) ? rtr - 8 : nullptr;
+    // trace only: the last CTA's phase-A steps in the two slots before it (it
+    // runs in the last wave, after its SM has run routing CTAs already)
+    unsigned long long* rsub = (rtr && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) ? rtr - 8 : nullptr;
     if (rsub) rsub[0] = route_gtimer();
     const int T = a.T, E = a.E, H = a.H;
     const size_t esz = ACT == ACT_BF16 ? 2 : 4;
@@ -703,6 +704,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
         __syncthreads();
         if (rsub) rsub[1] = route_gtimer();
         if (tc) {
+            // trace only: warp 0's sub-steps (norm, bounds, top-k of the bounds, candidates)
+            unsigned long long* csub = (rsub && lane == 0 && warp == 0) ? rsub - 8 : nullptr;
             if (warp < nt) {
                 const int t = warp;
                 const unsigned char* xr = route_smem + static_cast<size_t>(t) * H * esz;
@@ -716,19 +719,23 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float cb = ldexpf(static_cast<float>(H), -21) * sqrtf(ss) * (1.0f + 1.0f / 1024.0f);
+                if (csub) csub[0] = route_gtimer();
                 const float* lrow = lg + static_cast<size_t>(t) * E;
                 float* orow = lsel + static_cast<size_t>(t) * E;
                 for (int e = lane; e < E; e += 32) orow[e] = lrow[e] - cb * wn[e];
                 __syncwarp();
+                if (csub) csub[1] = route_gtimer();
                 int sel;
                 float gd;
                 warp_topk<false>(orow, E, k, lane, sel, gd, s_scr + warp * 32);
                 const float tau = orow[__shfl_sync(0xffffffffu, sel, k - 1)];
                 __syncwarp();
+                if (csub) csub[2] = route_gtimer();
                 for (int e = lane; e < E; e += 32) {
                     if (lrow[e] + cb * wn[e] >= tau) cand[atomicAdd(&s_last, 1)] = (t << 16) | e;
                     orow[e] = -INFINITY;
                 }
+                if (csub) csub[3] = route_gtimer();
             }
             __syncthreads();
             if (rsub) rsub[2] = route_gtimer();
@@ -811,8 +818,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
     if (!s_last) return;
     __threadfence();
     RouteShared& rs = *reinterpret_cast<RouteShared*>(route_smem);
-    // trace only: phase B's steps in the two ring slots before CTA 0's phase-A marks
-    route_phase_b(a, rs, route_smem + kRouteSharedBytes, DECODE, rtr ? rtr - 16 : nullptr);
+    // trace only: phase B's steps two ring slots before the phase-A marks
+    route_phase_b(a, rs, route_smem + kRouteSharedBytes, DECODE, rtr ? rtr - 24 : nullptr);
     if (threadIdx.x == 0) *a.route_done = 0;
     if (rtr && threadIdx.x == 0) rtr[2] = route_gtimer();
 }

@@ -1283,11 +1283,16 @@ int moe_sync(moe_handle* h) {
         unsigned long long q[8];
         CK(h, cudaMemcpy(q, h->trace + base - 8, sizeof(q), cudaMemcpyDeviceToHost));
         if (q[0] && q[5] >= q[0])
-            std::fprintf(stderr, "[moe] route CTA 0: staged %.2f, candidates %.2f, exact %.2f, top-k %.2f, end %.2f us; %llu candidates\n",
+            std::fprintf(stderr, "[moe] route, last CTA: staged %.2f, candidates %.2f, exact %.2f, top-k %.2f, end %.2f us; %llu candidates\n",
                          (q[1] - q[0]) * 1e-3, (q[2] - q[0]) * 1e-3, (q[3] - q[0]) * 1e-3, (q[4] - q[0]) * 1e-3,
                          (q[5] - q[0]) * 1e-3, q[7]);
+        unsigned long long w0[4];
+        CK(h, cudaMemcpy(w0, h->trace + base - 16, sizeof(w0), cudaMemcpyDeviceToHost));
+        if (q[0] && w0[3] >= w0[0] && w0[0] >= q[0])
+            std::fprintf(stderr, "[moe] route, last CTA, warp 0: norm %.2f, bounds %.2f, top-k of the bounds %.2f, candidates %.2f us\n",
+                         (w0[0] - q[0]) * 1e-3, (w0[1] - q[0]) * 1e-3, (w0[2] - q[0]) * 1e-3, (w0[3] - q[0]) * 1e-3);
         unsigned long long b[8];
-        CK(h, cudaMemcpy(b, h->trace + base - 16, sizeof(b), cudaMemcpyDeviceToHost));
+        CK(h, cudaMemcpy(b, h->trace + base - 24, sizeof(b), cudaMemcpyDeviceToHost));
         if (r[0] != ~0ull && r[2] != 0 && b[0] >= r[1] && b[6] >= b[0])
             std::fprintf(stderr,
                          "[moe] route phase B (us after its start): state loaded %.2f, offsets %.2f, permutation %.2f, "
