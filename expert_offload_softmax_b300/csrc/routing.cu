@@ -11,7 +11,7 @@
 //
 // k_route runs in two phases:
 //  A (every CTA)  router logits in the fixed fp32 order. Decode (T <= 8, BF16
-//                 or FP32 weights; FP4 decode runs in the fused decode kernel):
+//                 or FP32 weights; FP4 / FP8 decode runs in the fused decode kernel):
 //                 one warp per expert for all tokens, the activations are also
 //                 reordered for the expert kernels. Prefill: one CTA per 8
 //                 tokens over all experts, followed by that CTA's softmax/top-k.

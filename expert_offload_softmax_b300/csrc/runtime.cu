@@ -1159,7 +1159,7 @@ int moe_layer_forward(moe_handle* h, const void* hidden, const void* router_w, i
         tc->seq = seq;
     }
     if (moe::decode_fused(h->d.weight_fmt, T)) {
-        // decode with FP4 weights: one kernel does the whole call, including the
+        // decode with FP4 or FP8 weights: one kernel does the whole call, including the
         // copies of its misses (unless MOE_CACHE_HOST_MISSES); it never waits for
         // the host except in that mode
         if (h->banks_dirty) {

@@ -22,7 +22,7 @@
  * (T > 8) are copied into the pool with cudaMemcpyAsync on side streams, and
  * with MOE_CACHE_PREFETCH_NEXT_LAYER all experts of layer+1 also stream into
  * the pool while this layer computes, when the pool has room for both. Decode
- * calls (T <= 8) with FP4 weights run as one kernel that copies its own misses
+ * calls (T <= 8) with FP4 or FP8 weights run as one kernel that copies its own misses
  * from the mapped banks (or, with MOE_CACHE_HOST_MISSES, waits for the host's
  * cudaMemcpyAsync copies).
  *
@@ -87,7 +87,7 @@ typedef enum moe_act_mode { MOE_MODE_SWIGLU = 0, MOE_MODE_LINEAR_TEST = 1 } moe_
                                              calling thread waits for the routing kernel and
                                              the copies); for debugging and for tools that
                                              serialise launches */
-#define MOE_CACHE_HOST_MISSES 8u          /* decode calls with FP4 weights: the host copies
+#define MOE_CACHE_HOST_MISSES 8u          /* decode calls with FP4/FP8 weights: the host copies
                                              their misses with cudaMemcpyAsync on a side stream
                                              and the decode kernel waits (bounded) for its
                                              release; by default that kernel copies its misses
@@ -148,7 +148,7 @@ typedef struct moe_stats_t {
 typedef struct moe_timing_t {
     uint64_t calls;
     double route_ms;      /* routing kernel: router, top-k, permutation, cache lookup (all calls) */
-    double gate_up_ms;    /* gate/up projection + SwiGLU (decode with FP4 weights: the whole
+    double gate_up_ms;    /* gate/up projection + SwiGLU (decode with FP4/FP8 weights: the whole
                              expert kernel, gate/up and down+combine) */
     double down_ms;       /* down projection (+ combine, decode) */
     double combine_ms;    /* prefill combine */
@@ -249,7 +249,7 @@ int moe_cache_resize(moe_handle* h, int capacity_slots, void* pool_dev, size_t p
  * Returns without waiting for the device; the host blocks only when 16 calls
  * are already waiting for the service thread (with MOE_CACHE_SYNC_MISSES it
  * also blocks until the call's host-copied misses have landed). out is
- * complete once `stream` has passed the call. Decode (T <= 8) with FP4 weights
+ * complete once `stream` has passed the call. Decode (T <= 8) with FP4/FP8 weights
  * is one kernel that also copies the call's misses from the mapped banks
  * (unless MOE_CACHE_HOST_MISSES). A call whose experts exceed the pool leaves
  * the cache unchanged and out unwritten; the next moe_layer_forward or
