@@ -233,6 +233,52 @@ __device__ __forceinline__ void warp_logits(const void* __restrict__ router_w, c
         }
 }
 
+// Fixed-order logits of two (token, expert) pairs at once (b optional), the
+// same operations in the same order as warp_logits<ACT, 1, 8> with one token:
+// lane l accumulates chunks l, l + 32, ... in increasing order, then the
+// partials are combined by xor-halving. Both rows' loads are issued together.
+template <int ACT>
+__device__ __forceinline__ void pair_logits(const void* __restrict__ router_w, const unsigned char* xs, int H, int ea,
+                                            int ta, int eb, int tb, bool has_b, int lane, float& la, float& lb) {
+    constexpr int NB = 8;
+    float sa = 0.0f, sb = 0.0f;
+    const int nchunk = H / 8;
+    for (int cb = lane; cb < nchunk; cb += 32 * NB) {
+        RawChunk<ACT> ra[NB], rb[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int c = cb + 32 * i;
+            if (c < nchunk) {
+                ld_chunk<ACT>(router_w, static_cast<size_t>(ea) * H + 8 * c, ra[i]);
+                if (has_b) ld_chunk<ACT>(router_w, static_cast<size_t>(eb) * H + 8 * c, rb[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int c = cb + 32 * i;
+            if (c >= nchunk) break;
+            float wv[8], xv[8];
+            cvt_chunk<ACT>(ra[i], wv);
+            ld_act8<ACT>(xs, static_cast<size_t>(ta) * H + 8 * c, xv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sa = __fmaf_rn(xv[j], wv[j], sa);
+            if (has_b) {
+                cvt_chunk<ACT>(rb[i], wv);
+                ld_act8<ACT>(xs, static_cast<size_t>(tb) * H + 8 * c, xv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sb = __fmaf_rn(xv[j], wv[j], sb);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        sa = __fadd_rn(sa, __shfl_xor_sync(0xffffffffu, sa, o));
+        sb = __fadd_rn(sb, __shfl_xor_sync(0xffffffffu, sb, o));
+    }
+    la = sa;
+    lb = sb;
+}
+
 // phase-B shared memory; the work area follows it
 struct RouteShared {
     int32_t cnt[kMaxExperts];
@@ -741,11 +787,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(CallArgs a) {
             if (rsub) rsub[2] = route_gtimer();
             const int ncand = s_last;
             if (rsub) rsub[7] = static_cast<unsigned long long>(ncand);
-            for (int p = warp; p < ncand; p += kRouteWarps) {
-                const int t = cand[p] >> 16, e = cand[p] & 0xFFFF;
-                float acc[1][8];
-                warp_logits<ACT, 1, 8>(a.router_w, route_smem + static_cast<size_t>(t) * H * esz, H, E, e, 1, lane, acc);
-                if (lane == 0) lsel[static_cast<size_t>(t) * E + e] = acc[0][0];
+            // two candidates per warp and pass, their router rows in flight together
+            for (int p = warp; p < ncand; p += 2 * kRouteWarps) {
+                const int q = p + kRouteWarps;
+                const bool has_b = q < ncand;
+                const int ta = cand[p] >> 16, ea = cand[p] & 0xFFFF;
+                const int tb = has_b ? cand[q] >> 16 : ta, eb = has_b ? cand[q] & 0xFFFF : ea;
+                float la, lb;
+                pair_logits<ACT>(a.router_w, route_smem, H, ea, ta, eb, tb, has_b, lane, la, lb);
+                if (lane == 0) {
+                    lsel[static_cast<size_t>(ta) * E + ea] = la;
+                    if (has_b) lsel[static_cast<size_t>(tb) * E + eb] = lb;
+                }
             }
             __syncthreads();
             if (rsub) rsub[3] = route_gtimer();
