@@ -23,12 +23,12 @@
 //      the call record the host reads for its statistics. With misses, all
 //      CTAs copy the missed blobs (host -> pool slot) in parallel; barrier.
 //  P3  warp 0 of each CTA streams 16-row weight tiles with cp.async.bulk into
-//      a ring of shared-memory stages (mbarriers); warps 1-8 consume them with
+//      a ring of shared-memory stages (mbarriers); warps 1-16 consume them with
 //      mma.sync m16n8k16 (swap-AB: 16 weight rows x 8 token columns). Phase 1:
 //      h = gate * silu(W_gate x) * (W_up x); barrier (the producer keeps
 //      streaming phase-2 tiles across it); phase 2: out[t] = sum over experts
-//      of W_down h. Each tile's K range is split over the 8 consumer warps; the
-//      warp that finishes a tile last sums the 8 partials in warp order and
+//      of W_down h. Each tile's K range is split over the 16 consumer warps; the
+//      warp that finishes a tile last sums the 16 partials in warp order and
 //      writes the result, so the reduction order is fixed.
 //
 // Exact arithmetic of the operands. NVFP4: code (E2M1) and block scale (E4M3)
@@ -55,14 +55,16 @@
 namespace moe {
 namespace {
 
-constexpr int kConsumers = 8;
+constexpr int kConsumers = 16;
 constexpr int kWarps = kConsumers + 1;
 constexpr int kThreads = 32 * kWarps;
 static_assert(kDecodeMaxT * kMaxTopK < 32 * kWarps, "one assignment per thread in the routing counts");
 constexpr int kStageGroups = 2 * kChunkGroups;  // K groups (16 rows x 128) per pipeline stage
 constexpr int kMaxStages = 12;
 constexpr int kMaxAssign = kDecodeMaxT * kMaxTopK;
-constexpr int kRedSlotBytes = kConsumers * 32 * 4 * 4;  // one tile's 8 partial accumulators
+constexpr int kSlotsPerWarp = kStageGroups / kConsumers;  // K groups of a stage per consumer warp
+static_assert(kStageGroups % kConsumers == 0, "a stage's groups split evenly over the consumer warps");
+constexpr int kRedSlotBytes = kConsumers * 32 * 4 * 4;  // one tile's partial accumulators, one per consumer warp
 constexpr int kRedSlots = 4;                            // tiles whose reduction can be in flight
 constexpr int kSmemLimit = 220 * 1024;                  // dynamic bytes; a few KB static sit beside it
 constexpr int kLruCached = 4096;                        // pools up to this size cache stamps/owners in smem
@@ -1194,7 +1196,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
             const int np = seq.piece(lane, src, bytes, off, total);
             int got = 1;
             if (lane == 0) {
-                got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns) && !*abort_flag;
+                // a slot's first use needs no wait: the ring starts empty
+                got = (f < nst || mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns)) && !*abort_flag;
                 if (got) mbar_expect_tx(&full[stage], total);
             }
             got = __shfl_sync(0xffffffffu, got, 0);
@@ -1315,7 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         };
         // ---------------- phase 1: gate/up + SwiGLU
         {
-            float acc[4][4] = {};  // four independent chains: (chunk half, even/odd step)
+            float acc[2 * kSlotsPerWarp][4] = {};  // independent chains: (group slot, even/odd step)
             for (int f = 0; f < nf1; ++f) {
                 const int u = seq.u, ut = seq.ut, c0 = seq.c0_1(), nc = seq.nc_1();
                 const bool tile_end = seq.end1();
@@ -1325,16 +1328,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 const unsigned char* st = wait_full();
                 if (ct == 0 && (f == 0 || f == nf1 - 1)) mark(f == 0 ? 13 : 14);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int h = 0; h < kSlotsPerWarp; ++h) {
+                    const int gs = w + kConsumers * h;  // group slot of this stage: chunk gs / 8, group gs % 8
+                    const int half = gs / kChunkGroups, ww = gs % kChunkGroups;
                     const int c = c0 + half;
                     if (half < nc) {
                         const int ng = fp4_chunk_groups(seq.G1k, c);
-                        if (w < ng && !dead) {
-                            const int j = c * kChunkGroups + w;
+                        if (ww < ng && !dead) {
+                            const int j = c * kChunkGroups + ww;
                             uint32_t bq[16];
                             if (geo.act_bytes) load_b_smem(act, xp, tok, j, q, bq);
                             else load_b_xglobal<ACT>(a.hidden, H, tok, j, q, tok >= 0 ? R.xsc[tok] : 1.f, bq);
-                            mma_group<FMT>(st + half * C::kChunkBytes, ng, w, g, q, bq, acc[2 * half], acc[2 * half + 1]);
+                            mma_group<FMT>(st + half * C::kChunkBytes, ng, ww, g, q, bq, acc[2 * h], acc[2 * h + 1]);
                         }
                     }
                 }
@@ -1342,7 +1347,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 if (tile_end) {
                     float v[4], part[4];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) part[x] = ((acc[0][x] + acc[1][x]) + acc[2][x]) + acc[3][x];
+                    for (int x = 0; x < 4; ++x) {
+                        part[x] = acc[0][x];
+#pragma unroll
+                        for (int y = 1; y < 2 * kSlotsPerWarp; ++y) part[x] += acc[y][x];
+                    }
                     if (tile_reduce(part, v)) {
 #pragma unroll
                         for (int h2 = 0; h2 < 2; ++h2) {
@@ -1360,7 +1369,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                         }
                     }
 #pragma unroll
-                    for (int y = 0; y < 4; ++y) acc[y][0] = acc[y][1] = acc[y][2] = acc[y][3] = 0.f;
+                    for (int y = 0; y < 2 * kSlotsPerWarp; ++y) acc[y][0] = acc[y][1] = acc[y][2] = acc[y][3] = 0.f;
                 }
             }
         }
@@ -1444,13 +1453,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 }
                 if (ct == 0) mark(7);
             }
-            // with several experts per stage: this warp's expert and K group in each half
-            int p2[2], w2[2];
+            // with several experts per stage: this warp's expert and K group in each of its slots
+            int p2[kSlotsPerWarp], w2[kSlotsPerWarp];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int gs = w + kConsumers * half;  // group slot of this stage
-                p2[half] = seq.epp == 1 ? 0 : gs / seq.G2k;
-                w2[half] = gs - p2[half] * seq.G2k;
+            for (int h = 0; h < kSlotsPerWarp; ++h) {
+                const int gs = w + kConsumers * h;  // group slot of this stage
+                p2[h] = seq.epp == 1 ? 0 : gs / seq.G2k;
+                w2[h] = gs - p2[h] * seq.G2k;
             }
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int f = 0; f < nf2; ++f) {
@@ -1461,19 +1470,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                 const unsigned char* st = wait_full();
                 if (ct == 0 && f == nf2 - 1) mark(15);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int h = 0; h < kSlotsPerWarp; ++h) {
                     int u, c, ww, ng, off;
                     if (seq.epp == 1) {
+                        const int gs = w + kConsumers * h, half = gs / kChunkGroups;  // chunk c0 + half, group gs % 8
                         u = u0;
                         c = c0 + half;
-                        ww = w;
+                        ww = gs % kChunkGroups;
                         ng = c < c0 + nc ? fp4_chunk_groups(seq.G2k, c) : 0;
                         off = half * C::kChunkBytes;
                     } else {
-                        const int p = p2[half];
+                        const int p = p2[h];
                         u = u0 + p;
                         c = 0;
-                        ww = w2[half];
+                        ww = w2[h];
                         ng = p < nu_ ? seq.G2k : 0;
                         off = p * kTileRows * seq.G2k * C::kRowBytes;
                     }
