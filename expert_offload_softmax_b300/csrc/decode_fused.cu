@@ -619,6 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
     // visible after this; the next call's CTAs may be scheduled as ours exit
     const uint64_t t_entry = a.trace ? gtimer() : 0;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // per-token max |h| of the calls: two arrays by call parity; this call uses
+    // its own (zeroed by the previous call, or at moe_cache_config) and zeroes
+    // the next call's, which the previous call used and no one reads any more
+    if (b == 0 && tid < kDecodeMaxT) a.hmax[((a.dcall + 1) & 1) * kDecodeMaxT + tid] = 0u;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // trace only: per call, the first CTA's entry, CTA 0's return from the
     // dependency wait, the last CTA's exit
@@ -1363,8 +1367,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
                                 const float gate = v[h2] * m.gs[0] * R.xun[t], up = v[2 + h2] * m.gs[1] * R.xun[t];
                                 const float av = a.mode == 1 ? gate : silu(gate);
                                 hv = av * up * m.gate[nn];
-                                reinterpret_cast<__nv_bfloat16*>(a.hbuf)[static_cast<size_t>(r) * I + dpos(ut * 8 + g)] =
-                                    __float2bfloat16_rn(hv);
+                                const __nv_bfloat16 hb16 = __float2bfloat16_rn(hv);
+                                reinterpret_cast<__nv_bfloat16*>(a.hbuf)[static_cast<size_t>(r) * I + dpos(ut * 8 + g)] = hb16;
+                                // this CTA's max |h| of token t, as the bits of an fp32
+                                const uint32_t hbits = (static_cast<uint32_t>(__bfloat16_as_ushort(hb16)) << 16) & 0x7FFFFFFFu;
+                                atomicMax(&R.hmax[t], hbits);
                             }
                         }
                     }
@@ -1378,6 +1385,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         if (ct == 0) mark(6);
         if (b != 0) {
             if (ct == 0) {
+                // this CTA's per-token max |h| into the call's maxima, before its arrival publishes them
+                for (int t = 0; t < T; ++t)
+                    if (R.hmax[t]) atomicMax(a.hmax + (a.dcall & 1) * kDecodeMaxT + t, R.hmax[t]);
                 bar_arrive(a.bar_cnt + 2, 1);
                 R.ok = (bar_wait(a, a.bar_cnt + 2, tgt2, MOE_DEVERR_TIMEOUT_EPILOGUE) && !*abort_flag) ? 1 : 0;
             }
@@ -1387,67 +1397,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const __grid_constant__ 
         // ---------------- phase 2: down projection + combine
         if (nf2 > 0) {
             const int hrows = n + ns * T;
-            // Every h row of the call (bf16, read once): each token's largest |h|
-            // from the rows themselves, then the rows into shared memory as f16,
-            // scaled by a power of two per token (in place, when they fit).
+            // Every h row of the call (bf16, read once) into shared memory as f16,
+            // scaled by a power of two per token from the call's maxima (published
+            // by every worker before barrier 2), when the rows fit; otherwise the
+            // MMA operands are read from global memory with the same scales.
             {
                 const int per_row = I / 8;
                 const float inv_pr = 1.0f / static_cast<float>(per_row);
-                unsigned int mxt[kDecodeMaxT];
-#pragma unroll
-                for (int t = 0; t < kDecodeMaxT; ++t) mxt[t] = 0u;
-                const int nvec = hrows * per_row;  // row r holds vectors [r * per_row, (r + 1) * per_row): h is contiguous
-                const uint4* hv = reinterpret_cast<const uint4*>(hb);
-                for (int i0 = ct; i0 < nvec; i0 += 4 * 32 * kConsumers) {
-                    uint4 x[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {  // four loads in flight
-                        const int i = i0 + j * 32 * kConsumers;
-                        x[j] = i < nvec ? __ldcg(hv + i) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int i = i0 + j * 32 * kConsumers;
-                        if (i < nvec) {
-                            int r = __float2int_rz(static_cast<float>(i) * inv_pr);
-                            r += (r + 1) * per_row <= i;
-                            r -= r * per_row > i;
-                            if (geo.act_bytes) *reinterpret_cast<uint4*>(act + r * hp + 16 * (i - r * per_row)) = x[j];
-                            const uint32_t wv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-                            unsigned int m = 0u;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                m = max(m, max(wv[e] << 17 >> 1, (wv[e] & 0x7FFF0000u)));  // |bf16| as fp32 bits, both halves
-                            const int t = R.rowtok[r];
-#pragma unroll
-                            for (int tt = 0; tt < kDecodeMaxT; ++tt) mxt[tt] = tt == t ? max(mxt[tt], m) : mxt[tt];
-                        }
-                    }
+                if (ct < T) {
+                    const unsigned int mb = __ldcg(a.hmax + (a.dcall & 1) * kDecodeMaxT + ct);
+                    R.hmax[ct] = mb;
+                    pow2_scale(mb, R.hsc[ct], R.hun[ct]);
                 }
-#pragma unroll
-                for (int tt = 0; tt < kDecodeMaxT; ++tt) {
-                    if (tt < T) {
-                        const unsigned int mw = __reduce_max_sync(0xffffffffu, mxt[tt]);
-                        if (lane == 0) atomicMax(&R.hmax[tt], mw);
-                    }
-                }
-                consumer_sync();
-                if (ct < T) pow2_scale(R.hmax[ct], R.hsc[ct], R.hun[ct]);
                 consumer_sync();
                 if (geo.act_bytes) {
-                    for (int i = ct; i < hrows * per_row; i += 32 * kConsumers) {
-                        int r = __float2int_rz(static_cast<float>(i) * inv_pr);
-                        r += (r + 1) * per_row <= i;
-                        r -= r * per_row > i;
-                        uint4* pp = reinterpret_cast<uint4*>(act + r * hp + 16 * (i - r * per_row));
-                        const uint4 x = *pp;
-                        const float sc = R.hsc[R.rowtok[r]];
-                        uint4 o;
-                        o.x = f16x2_scaled(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u), sc);
-                        o.y = f16x2_scaled(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xFFFF0000u), sc);
-                        o.z = f16x2_scaled(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xFFFF0000u), sc);
-                        o.w = f16x2_scaled(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xFFFF0000u), sc);
-                        *pp = o;
+                    const int nvec = hrows * per_row;  // row r holds vectors [r * per_row, (r + 1) * per_row): h is contiguous
+                    const uint4* hv = reinterpret_cast<const uint4*>(hb);
+                    for (int i0 = ct; i0 < nvec; i0 += 4 * 32 * kConsumers) {
+                        uint4 x[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {  // four loads in flight
+                            const int i = i0 + j * 32 * kConsumers;
+                            x[j] = i < nvec ? __ldcg(hv + i) : make_uint4(0u, 0u, 0u, 0u);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int i = i0 + j * 32 * kConsumers;
+                            if (i < nvec) {
+                                int r = __float2int_rz(static_cast<float>(i) * inv_pr);
+                                r += (r + 1) * per_row <= i;
+                                r -= r * per_row > i;
+                                const float sc = R.hsc[R.rowtok[r]];
+                                uint4 o;
+                                o.x = f16x2_scaled(__uint_as_float(x[j].x << 16), __uint_as_float(x[j].x & 0xFFFF0000u), sc);
+                                o.y = f16x2_scaled(__uint_as_float(x[j].y << 16), __uint_as_float(x[j].y & 0xFFFF0000u), sc);
+                                o.z = f16x2_scaled(__uint_as_float(x[j].z << 16), __uint_as_float(x[j].z & 0xFFFF0000u), sc);
+                                o.w = f16x2_scaled(__uint_as_float(x[j].w << 16), __uint_as_float(x[j].w & 0xFFFF0000u), sc);
+                                *reinterpret_cast<uint4*>(act + r * hp + 16 * (i - r * per_row)) = o;
+                            }
+                        }
                     }
                     consumer_sync();
                 }

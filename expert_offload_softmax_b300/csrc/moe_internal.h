@@ -222,7 +222,7 @@ struct CallArgs {
     // fused decode (FP4 weights, T <= 8)
     const uint8_t* const* banks;  // [L] device views of the mapped pinned host banks
     float* xmax;           // [8] max |x| of each token row (this call)
-    unsigned int* hmax;    // [CTAs][8] each decode CTA's max |h| (float bits) per token
+    unsigned int* hmax;    // [2][8] decode: per-token max |h| of a call (float bits), by call parity
     DecPub* pub;           // miss slots for the kernel's CTAs
     int device_misses;     // 1: the decode kernel copies its misses itself; 0: the host does
     unsigned long long* trace;  // optional [CTAs][kTracePoints] %globaltimer marks of the decode kernel

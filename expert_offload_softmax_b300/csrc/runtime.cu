@@ -787,7 +787,7 @@ int moe_init(const moe_model_desc* desc, moe_handle** out) {
         {3 * 8, reinterpret_cast<void**>(&a.bar_cnt)},
         {static_cast<size_t>(moe::kDecodeMaxT) * E * 8, reinterpret_cast<void**>(&a.dlog)},
         {moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.xmax)},
-        {static_cast<size_t>(h->num_sms) * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
+        {2 * moe::kDecodeMaxT * 4, reinterpret_cast<void**>(&a.hmax)},
         {sizeof(moe::DecPub), reinterpret_cast<void**>(&a.pub)},
         {static_cast<size_t>(L) * 8, reinterpret_cast<void**>(const_cast<uint8_t***>(&a.banks))},
         {moe::kDecPlanHeader + static_cast<size_t>(E + ns) * sizeof(moe::DecExpert), reinterpret_cast<void**>(&a.dplan)},
@@ -980,6 +980,7 @@ int moe_cache_config(moe_handle* h, int capacity_slots, unsigned flags, void* po
     CK(h, cudaMemset(h->base.route_done, 0, 4));
     CK(h, cudaMemset(h->base.bar_cnt, 0, 3 * 8));
     CK(h, cudaMemset(h->base.dlog, 0, static_cast<size_t>(moe::kDecodeMaxT) * h->d.num_experts * 8));
+    CK(h, cudaMemset(h->base.hmax, 0, 2 * moe::kDecodeMaxT * 4));
     h->dcalls = 0;
 
     // the ready word continues from the last serviced call
