@@ -110,6 +110,14 @@ def test_fp8_linear_mode():
     _run(s, 26, 1, 8, [(0, 6, 0), (0, 40, 1), (0, 1, 2)])
 
 
+def test_prefill_more_than_512_routing_blocks():
+    """T = 4200: 525 routing CTAs of 8 tokens, so the permutation kernel sums
+    count columns past the first 512 (its tail loop); routing and permutation
+    bit-exact, outputs on 64 tokens."""
+    s = synth.Shape("long", L=1, E=16, k=2, H=256, I=128, fmt=synth.FMT_BF16, act=synth.ACT_BF16)
+    _run(s, 27, 1, 16, [(0, 4200, 0)], sample=64, max_tokens=4200)
+
+
 def test_prefill_prefetch_next_layer():
     s = synth.Shape("small", L=4, E=16, k=4, H=256, I=128, fmt=synth.FMT_NVFP4, act=synth.ACT_BF16)
     calls = [(l, 64, 0) for l in range(4)] + [(l, 64, 1) for l in range(4)]
