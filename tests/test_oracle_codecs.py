@@ -134,6 +134,25 @@ def test_dequant_fp4_matches_independent_decode(fmt):
         assert np.array_equal(ours, ref.astype(np.float32))
 
 
+def test_e4m3_golden_values_and_fp8_dequant():
+    """Hand-worked E4M3 values (tests/golden/e4m3_values.txt, from the OFP8
+    definition): the oracle's decode, and FP8 dequantisation with a per-tensor
+    scale of 0.25, reproduce them."""
+    pairs = []
+    for line in open(os.path.join(GOLDEN, "e4m3_values.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        b, v = line.split()
+        pairs.append((int(b, 16), float(v)))
+    for b, v in pairs:
+        got = oracle.e4m3fn(b)
+        assert got == v and np.signbit(got) == np.signbit(v), (hex(b), got, v)
+    codes = np.array([[b for b, _ in pairs] + [0x38] * (128 - len(pairs))], np.uint8)
+    w = oracle.dequant(oracle.FP8, {"codes": codes, "gscale": 0.25}, 1, 128)
+    assert list(w[0, :len(pairs)]) == [np.float32(v) * np.float32(0.25) for _, v in pairs]
+
+
 def test_dequant_fp8_matches_independent_decode():
     """FP8 weights: every E4M3 byte decoded by torch's float8_e4m3fn dtype,
     times the per-tensor scale, equals the oracle's dequantisation."""
