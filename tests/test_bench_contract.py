@@ -97,3 +97,24 @@ def test_bench_line_from_measurements():
     r = d["roofline"]
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and "tcgen05" in r["kernel"]
     assert r["algorithmic_flops_per_launch"] == 4.0 * 512 * 2048 * 4096 * 8
+
+
+def test_dtype_strings_and_fp8_workloads():
+    """The arithmetic each format's path computes in, as the JSON line states it,
+    and the FP8 workloads registered with the stacks' shapes."""
+    sys.path.insert(0, ROOT)
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    import synth
+    assert bench._dtype_str(synth.FMT_BF16, 1) == "bf16 x bf16, fp32 accumulate"
+    assert bench._dtype_str(synth.FMT_FP32, 4096) == "fp32"
+    assert bench._dtype_str(synth.FMT_NVFP4, 1).startswith("nvfp4 weights") and "into f16" in bench._dtype_str(synth.FMT_NVFP4, 1)
+    assert "fp8 weights (E4M3 code exact in f16" in bench._dtype_str(synth.FMT_FP8, 1)
+    assert "exact in bf16" in bench._dtype_str(synth.FMT_FP8, 4096) and "bf16 activations" in bench._dtype_str(synth.FMT_FP8, 4096)
+    assert "mxfp4" in bench._dtype_str(synth.FMT_MXFP4, 8)
+    shape, T = bench.WORKLOADS["decode_fp8"][:2]
+    assert shape.fmt == synth.FMT_FP8 and T == 1 and (shape.H, shape.E, shape.k, shape.I, shape.L) == (2048, 256, 8, 512, 40)
+    shape, T = bench.WORKLOADS["prefill_fp8"][:2]
+    assert shape.fmt == synth.FMT_FP8 and T == 4096
